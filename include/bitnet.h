@@ -1,0 +1,176 @@
+/*
+ * bitnet.h -- C ABI of the GB300 (sm_103a) W1.58A8 BitLinear library.
+ *
+ * One BitLinear projection, as the "BitNet Embeddings GGUF Conversion
+ * Implementation" page describes it (section 1, "Background"), is
+ *
+ *     x -> RMSNorm(x, norm.weight) -> 8-bit activation quant -> matmul with
+ *          ternary weights -> fp32 output
+ *
+ * with the per-projection norm weight applied after ggml_rms_norm (section 4.5,
+ * "load_tensors", graph code) and eps = 1e-6 (section 1, model table).  The
+ * "BitNet Inference Framework" page, "Quantization (W1.58A8)", fixes absmean
+ * ternary weights and per-token absmax 8-bit activations; it also states that
+ * neither linear nor norm layers carry a bias ("Architectural Details").
+ *
+ * Weight storage is I2_S ("I2_S Ternary Packing" in section 3 of the first page;
+ * "Quantization and Encoding" and "Data Layout" on the second page):
+ *   - w_scale = 1 / mean(|w|) over the whole tensor,
+ *     q = clamp(round(w * w_scale), -1, 1), code = q + 1 (-1 -> 0, 0 -> 1, +1 -> 2);
+ *   - 128 consecutive values of the flattened tensor form a block of 32 bytes;
+ *     every byte holds four codes as (c0 << 6) | (c1 << 4) | (c2 << 2) | c3;
+ *   - one float32 scale is appended after the last block.
+ * The pages leave open which four elements share a byte.  This library fixes it:
+ * byte j (0..31) of a block holds the block's elements j, 32+j, 64+j and 96+j as
+ * c0, c1, c2 and c3.  A weight matrix W is [N, K] (N outputs, K inputs, K
+ * contiguous), so with K % 128 == 0 ("gguf-gemv" page, "Requirements") no block
+ * straddles two rows: row n, block kb lives at byte offset 32 * (n*K/128 + kb),
+ * and the scale at byte offset N*K/4 (little endian).
+ *
+ * Readings taken where the pages are silent:
+ *   - "round" is round-half-to-even (rint) for weights and activations;
+ *   - mean(|w|) is accumulated in double; an all-zero tensor gets w_scale = 1;
+ *   - activations: a_scale = 127 / max(max|xn|, 1e-5), q = clamp(rint(xn * a_scale),
+ *     -128, 127), both multiplies in fp32 without FMA contraction;
+ *   - RMSNorm: rstd = (float)(1 / sqrt(sum(x^2)/K + eps)) with the sum and the
+ *     square root in double; xn = (x * rstd) * norm_w, two fp32 multiplies;
+ *   - output: y = ((float)acc * (1/a_scale)) * (1/w_scale), fp32, each reciprocal
+ *     and product correctly rounded, where acc = sum_k q_x[k] * q_w[k] exactly.
+ *
+ * Conventions shared by every entry point:
+ *   - all tensor pointers are DEVICE pointers to contiguous row-major buffers owned
+ *     by the caller; the library never frees or retains them;
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every call
+ *     is asynchronous on it unless its comment says otherwise;
+ *   - the return value is a bitnet_status; argument errors are detected on the
+ *     host before anything is launched and leave every output untouched;
+ *   - a device-side failure (a bounded wait that expired) is recorded in a
+ *     per-device error word that bitnet_last_device_status() reads and clears;
+ *     no kernel of this library traps or aborts;
+ *   - K must be a positive multiple of 128 and at most BITNET_MAX_K; M and N at
+ *     least 1; x, y and packed weights 16-byte aligned.
+ *   - temporary device memory (where a call needs it) comes from a stream-ordered
+ *     pool that the library owns per device; it is reused across calls and never
+ *     returned to the caller.
+ */
+#ifndef BITNET_GB300_H
+#define BITNET_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BITNET_I2S_BLOCK 128       /* values per I2_S block                         */
+#define BITNET_I2S_BLOCK_BYTES 32  /* bytes per I2_S block                          */
+#define BITNET_GGML_TYPE_I2_S 36   /* GGML type id ("gguf-py: I2_S Type", first page) */
+#define BITNET_MAX_K 65536         /* keeps every partial sum below 2^24 (exact in fp32) */
+#define BITNET_MAX_GROUP 16        /* projections per bitnet_bitlinear_forward_group  */
+
+/* Flag for bitnet_bitlinear_forward_group: the packed weights were written by
+ * work that finished before the previous kernel on `stream` began, so the kernel
+ * may start streaming them before that kernel has finished (programmatic
+ * dependent launch).  Activations are always read after the previous kernel. */
+#define BITNET_FLAG_WEIGHTS_STATIC 1u
+
+typedef enum {
+  BITNET_OK = 0,
+  BITNET_ERR_INVALID_ARG = 1,       /* null pointer, M/N < 1, eps <= 0, count out of range */
+  BITNET_ERR_UNSUPPORTED_SHAPE = 2, /* K not a positive multiple of 128, or K > BITNET_MAX_K */
+  BITNET_ERR_MISALIGNED = 3,        /* a pointer that must be 16-byte aligned is not       */
+  BITNET_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed                */
+  BITNET_ERR_TIMEOUT = 5,           /* a device-side bounded wait expired (see last_device_status) */
+  BITNET_ERR_NO_DEVICE = 6          /* no CUDA device, or it is not sm_103                 */
+} bitnet_status;
+
+typedef struct CUstream_st* bitnet_stream_t; /* == cudaStream_t */
+
+/* Bytes of an I2_S buffer for an [N, K] matrix: N*K/4 code bytes plus the 4-byte
+ * scale.  Returns 0 for an invalid shape (N < 1, K not a positive multiple of 128). */
+size_t bitnet_i2s_packed_bytes(int64_t N, int64_t K);
+
+/* Absmean ternary quantisation and I2_S packing of w[N, K] (fp32) into
+ * packed[bitnet_i2s_packed_bytes(N, K)] ("I2_S Ternary Packing", first page
+ * section 3; "Quantization and Encoding" / "Data Layout", second page).
+ * The scale is written to the buffer's last 4 bytes; if w_scale_out (a HOST
+ * pointer) is non-NULL the call synchronises `stream` and stores it there too.
+ * mean(|w|) is reduced in double in a fixed order, so repeated calls give
+ * identical bytes.  packed must be 16-byte aligned. */
+int bitnet_pack_i2s(const float* w, int64_t N, int64_t K, uint8_t* packed,
+                    float* w_scale_out, bitnet_stream_t stream);
+
+/* Decode an I2_S buffer into ternary int8 values w_ternary[N, K] = code - 1.
+ * A (malformed) code 3 decodes to +2, the same value every kernel here uses. */
+int bitnet_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_t* w_ternary,
+                      bitnet_stream_t stream);
+
+/* RMSNorm with the projection's norm weight followed by per-token absmax int8
+ * quantisation ("Background" and "load_tensors" on the first page; "Quantization
+ * (W1.58A8)" on the second).  x[M, K] fp32, norm_w[K] fp32 ->
+ *   a_codes[M, K] int8, a_scale[M] fp32 (= 127 / max(max|xn|, 1e-5)),
+ *   a_rowsum[M] int32 (sum of the row's codes; may be NULL),
+ *   xn_out[M, K] fp32 (the normalised row before quantisation; may be NULL).
+ * eps > 0 (the pages' models use 1e-6). */
+int bitnet_rmsnorm_quant_a8(const float* x, const float* norm_w, int64_t M, int64_t K,
+                            float eps, int8_t* a_codes, float* a_scale, int32_t* a_rowsum,
+                            float* xn_out, bitnet_stream_t stream);
+
+/* I2_S x int8 contraction and fp32 rescale (the int8 x ternary dot products of
+ * ggml_vec_dot_i2_i8_s named in section 6.4 of the first page, plus the two
+ * scales): for every m < M, n < N
+ *   acc[m, n] = sum_k a_codes[m, k] * (code(n, k) - 1)          (exact integer)
+ *   y[m, n]   = ((float)acc * (1 / a_scale[m])) * (1 / w_scale)
+ * a_codes[M, K] int8, a_scale[M] fp32, packed_w in I2_S layout (its trailing
+ * scale is ignored: w_scale is the argument), y[M, N] fp32; acc_out[M, N] int32
+ * receives acc when non-NULL.  M <= 8 runs a dp4a weight-streaming kernel,
+ * larger M the tcgen05 tensor-core kernel (pool memory: 2*M*K bytes). */
+int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* packed_w,
+                    float w_scale, int64_t M, int64_t K, int64_t N, float* y,
+                    int32_t* acc_out, bitnet_stream_t stream);
+
+/* The whole projection: y[M, N] = BitLinear(x[M, K]) with norm weight norm_w[K],
+ * weights packed_w (I2_S, [N, K]) and their scale w_scale.  Bit-for-bit the
+ * composition of bitnet_rmsnorm_quant_a8 and bitnet_i2s_gemm.  Small M runs
+ * one fused launch; larger M a norm/quant launch (pool memory: 2*M*K + 4*M
+ * bytes) followed by the tensor-core launch. */
+int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w,
+                             float w_scale, int64_t M, int64_t K, int64_t N, float eps,
+                             float* y, bitnet_stream_t stream);
+
+/* One projection of a group (all pointers device pointers, as above). */
+typedef struct {
+  const float* x;          /* [M, K] fp32 */
+  const float* norm_w;     /* [K] fp32 */
+  const uint8_t* packed_w; /* I2_S [N, K] */
+  float w_scale;           /* the weights' I2_S scale */
+  int64_t K;
+  int64_t N;
+  float* y;                /* [M, N] fp32 */
+} bitnet_projection;
+
+/* Several independent projections with the same token count M in ONE launch
+ * (e.g. the seven projections of a layer at decode, each with its own input
+ * and norm weight).  Each output equals bitnet_bitlinear_forward of that
+ * projection, bit for bit.  `projs` is a HOST array of `count` descriptors
+ * (1..BITNET_MAX_GROUP), read before the call returns.  Supported for
+ * M <= 8 and K <= 16384; other shapes return BITNET_ERR_UNSUPPORTED_SHAPE.
+ * flags: 0 or BITNET_FLAG_WEIGHTS_STATIC. */
+int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M,
+                                   float eps, uint32_t flags, bitnet_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* bitnet_status_string(int status);
+
+/* Synchronises `stream`, then returns BITNET_ERR_TIMEOUT if a kernel of this
+ * library on the current device gave up a bounded wait since the last call
+ * (and clears that record), BITNET_ERR_CUDA if the synchronisation failed, and
+ * BITNET_OK otherwise. */
+int bitnet_last_device_status(bitnet_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITNET_GB300_H */

@@ -1,0 +1,239 @@
+"""CPU oracle for the W1.58A8 BitLinear projection -- TEST INFRASTRUCTURE ONLY.
+
+Thin numpy/ctypes wrapper over ``bitnet_oracle.c`` (plain C, OpenMP over rows).
+Only ``tests/``, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline leg use
+it; the CUDA library never does.  The C file cites, per function, the passage of
+the pages it restates.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bitnet_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libbitnet_oracle.so")
+_lib = None
+
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i8p = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    lib.oracle_mean_abs.restype = ctypes.c_double
+    lib.oracle_mean_abs.argtypes = [_f32p, _i64]
+    lib.oracle_weight_scale.restype = ctypes.c_float
+    lib.oracle_weight_scale.argtypes = [_f32p, _i64]
+    lib.oracle_quantize_ternary.restype = None
+    lib.oracle_quantize_ternary.argtypes = [_f32p, _i64, ctypes.c_float, _i8p]
+    lib.oracle_encode_i2s.restype = ctypes.c_int
+    lib.oracle_encode_i2s.argtypes = [_i8p, _i64, _i64, ctypes.c_float, _u8p]
+    lib.oracle_pack_i2s_with_scale.restype = ctypes.c_int
+    lib.oracle_pack_i2s_with_scale.argtypes = [_f32p, _i64, _i64, ctypes.c_float, _u8p]
+    lib.oracle_pack_i2s.restype = ctypes.c_int
+    lib.oracle_pack_i2s.argtypes = [_f32p, _i64, _i64, _u8p, ctypes.POINTER(ctypes.c_float)]
+    lib.oracle_unpack_i2s.restype = ctypes.c_int
+    lib.oracle_unpack_i2s.argtypes = [_u8p, _i64, _i64, _i8p]
+    lib.oracle_count_invalid_codes.restype = ctypes.c_int64
+    lib.oracle_count_invalid_codes.argtypes = [_u8p, _i64, _i64]
+    lib.oracle_rmsnorm.restype = None
+    lib.oracle_rmsnorm.argtypes = [_f32p, _f32p, _i64, _i64, ctypes.c_float, _f32p, ctypes.c_void_p]
+    lib.oracle_quant_a8.restype = None
+    lib.oracle_quant_a8.argtypes = [_f32p, _i64, _i64, _i8p, _f32p, _i32p]
+    lib.oracle_i2s_matmul.restype = ctypes.c_int
+    lib.oracle_i2s_matmul.argtypes = [_i8p, _u8p, _i64, _i64, _i64, _i64p]
+    lib.oracle_rescale.restype = None
+    lib.oracle_rescale.argtypes = [_i64p, _f32p, ctypes.c_float, _i64, _i64, _f32p]
+    lib.oracle_bitlinear_forward_rows.restype = ctypes.c_int
+    lib.oracle_bitlinear_forward_rows.argtypes = [
+        _f32p, _f32p, _u8p, ctypes.c_float, _i64, _i64, _i64, ctypes.c_float,
+        ctypes.c_void_p, _i64, _f32p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p]
+    lib.oracle_dequant_dot_f64.restype = None
+    lib.oracle_dequant_dot_f64.argtypes = [_i8p, _i8p, _f32p, ctypes.c_float, _i64, _i64, _i64, _f64p]
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_set_num_threads.restype = None
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def mean_abs(w) -> float:
+    w = _f32(w).ravel()
+    return float(_load().oracle_mean_abs(w, w.size))
+
+
+def weight_scale(w) -> float:
+    w = _f32(w).ravel()
+    return float(_load().oracle_weight_scale(w, w.size))
+
+
+def quantize_ternary(w, w_scale: float) -> np.ndarray:
+    w = _f32(w)
+    q = np.empty(w.shape, dtype=np.int8)
+    _load().oracle_quantize_ternary(w.ravel(), w.size, ctypes.c_float(w_scale), q.reshape(-1))
+    return q
+
+
+def encode_i2s(q, w_scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    N, K = q.shape
+    out = np.empty(N * K // 4 + 4, dtype=np.uint8)
+    rc = _load().oracle_encode_i2s(q, N, K, ctypes.c_float(w_scale), out)
+    if rc:
+        raise ValueError(f"encode_i2s: bad shape {q.shape}")
+    return out
+
+
+def pack_i2s(w, w_scale: float | None = None):
+    """Return (packed bytes, w_scale) for w[N, K]."""
+    w = _f32(w)
+    N, K = w.shape
+    out = np.empty(N * K // 4 + 4, dtype=np.uint8)
+    lib = _load()
+    if w_scale is None:
+        s = ctypes.c_float(0.0)
+        rc = lib.oracle_pack_i2s(w, N, K, out, ctypes.byref(s))
+        w_scale = s.value
+    else:
+        rc = lib.oracle_pack_i2s_with_scale(w, N, K, ctypes.c_float(w_scale), out)
+    if rc:
+        raise ValueError(f"pack_i2s: bad shape {w.shape}")
+    return out, float(np.float32(w_scale))
+
+
+def unpack_i2s(packed, N: int, K: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    q = np.empty((N, K), dtype=np.int8)
+    rc = _load().oracle_unpack_i2s(packed, N, K, q)
+    if rc:
+        raise ValueError("unpack_i2s: bad shape")
+    return q
+
+
+def count_invalid_codes(packed, N: int, K: int) -> int:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    return int(_load().oracle_count_invalid_codes(packed, N, K))
+
+
+def rmsnorm(x, g, eps: float = 1e-6, return_rstd: bool = False):
+    x = _f32(x)
+    g = _f32(g)
+    M, K = x.shape
+    xn = np.empty_like(x)
+    rstd = np.empty(M, dtype=np.float32)
+    _load().oracle_rmsnorm(x, g, M, K, ctypes.c_float(eps), xn, _ptr(rstd))
+    return (xn, rstd) if return_rstd else xn
+
+
+def quant_a8(xn):
+    """Return (codes int8 [M,K], a_scale f32 [M], rowsum int32 [M])."""
+    xn = _f32(xn)
+    M, K = xn.shape
+    q = np.empty((M, K), dtype=np.int8)
+    s = np.empty(M, dtype=np.float32)
+    rs = np.empty(M, dtype=np.int32)
+    _load().oracle_quant_a8(xn, M, K, q, s, rs)
+    return q, s, rs
+
+
+def i2s_matmul(q, packed, N: int) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    M, K = q.shape
+    acc = np.empty((M, N), dtype=np.int64)
+    rc = _load().oracle_i2s_matmul(q, packed, M, K, N, acc)
+    if rc:
+        raise ValueError("i2s_matmul: bad shape")
+    return acc
+
+
+def rescale(acc, a_scale, w_scale: float) -> np.ndarray:
+    acc = np.ascontiguousarray(acc, dtype=np.int64)
+    a_scale = _f32(a_scale)
+    M, N = acc.shape
+    y = np.empty((M, N), dtype=np.float32)
+    _load().oracle_rescale(acc, a_scale, ctypes.c_float(w_scale), M, N, y)
+    return y
+
+
+def bitlinear_forward(x, g, packed, w_scale: float, N: int, eps: float = 1e-6, rows=None,
+                      intermediates: bool = False):
+    """y[rows, N] of the whole projection; all rows when rows is None.
+
+    With intermediates=True returns (y, xn, codes, a_scale, acc)."""
+    x = _f32(x)
+    g = _f32(g)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    M, K = x.shape
+    if rows is None:
+        r = None
+        n = M
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        n = r.size
+    y = np.empty((n, N), dtype=np.float32)
+    xn = np.empty((n, K), dtype=np.float32) if intermediates else None
+    q = np.empty((n, K), dtype=np.int8) if intermediates else None
+    s = np.empty(n, dtype=np.float32) if intermediates else None
+    acc = np.empty((n, N), dtype=np.int64) if intermediates else None
+    rc = _load().oracle_bitlinear_forward_rows(
+        x, g, packed, ctypes.c_float(w_scale), M, K, N, ctypes.c_float(eps), _ptr(r), n, y,
+        _ptr(xn), _ptr(q), _ptr(s), _ptr(acc))
+    if rc:
+        raise ValueError(f"bitlinear_forward: error {rc}")
+    return (y, xn, q, s, acc) if intermediates else y
+
+
+def dequant_dot_f64(q, t, a_scale, w_scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    a_scale = _f32(a_scale)
+    M, K = q.shape
+    N = t.shape[0]
+    y = np.empty((M, N), dtype=np.float64)
+    _load().oracle_dequant_dot_f64(q, t, a_scale, ctypes.c_float(w_scale), M, K, N, y)
+    return y

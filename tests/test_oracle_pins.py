@@ -1,0 +1,301 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each test ties one oracle function to what the pages or mathematics fix:
+hand-worked bytes of the I2_S packing passage, closed forms, library routines
+(torch rms_norm in float64, numpy integer matmul) and error bounds.
+"""
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+
+from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "i2s_worked_blocks.txt")
+
+
+def _golden_rows():
+    rows = {}
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, hx = line.rstrip("\n").split("\t")
+        rows[name] = bytes.fromhex(hx)
+    return rows
+
+
+def _pattern(name):
+    """The 128 ternary values each worked block describes."""
+    v = np.zeros(128, dtype=np.int8)
+    if name == "all_plus_one":
+        v[:] = 1
+    elif name == "all_zero":
+        pass
+    elif name == "all_minus_one":
+        v[:] = -1
+    elif name == "quarters":
+        v[0:32], v[32:64], v[64:96], v[96:128] = -1, 0, 1, 0
+    elif name == "first_plus":
+        v[0] = 1
+    elif name == "e97_minus":
+        v[97] = -1
+    elif name == "mod3":
+        v[:] = np.arange(128) % 3 - 1
+    else:
+        raise KeyError(name)
+    return v
+
+
+# ------------------------------------------------------------ packing pins ---
+
+@pytest.mark.parametrize("name", list(_golden_rows().keys()))
+def test_worked_block_encode(oracle_mod, name):
+    expected = _golden_rows()[name]
+    q = _pattern(name).reshape(1, 128)
+    out = oracle_mod.encode_i2s(q, 1.0)
+    assert bytes(out[:32]) == expected
+    assert bytes(out[32:]) == struct.pack("<f", 1.0)
+
+
+@pytest.mark.parametrize("name", [n for n in _golden_rows() if n != "all_zero"])
+def test_worked_block_pack_from_float(oracle_mod, name):
+    """Absmean quantisation of c * pattern recovers the pattern (every non-zero
+    entry lands at >= 1 after scaling and clamps to +-1) and the same bytes."""
+    expected = _golden_rows()[name]
+    q = _pattern(name)
+    c = 0.37
+    w = (q.astype(np.float32) * np.float32(c)).reshape(1, 128)
+    packed, s = oracle_mod.pack_i2s(w)
+    assert bytes(packed[:32]) == expected
+    nnz = int(np.count_nonzero(q))
+    assert s == pytest.approx(128.0 / (c * nnz), rel=2 ** -22)
+    assert struct.unpack("<f", bytes(packed[32:36]))[0] == s
+
+
+def test_all_zero_tensor_scale_is_one(oracle_mod):
+    packed, s = oracle_mod.pack_i2s(np.zeros((2, 128), np.float32))
+    assert s == 1.0
+    assert bytes(packed[:64]) == b"\x55" * 64
+
+
+def test_multi_row_block_order(oracle_mod):
+    """Row n, block kb sits at byte offset 32 * (n*K/128 + kb): use distinct
+    constant rows/blocks so any misplacement changes the bytes."""
+    N, K = 3, 256
+    q = np.zeros((N, K), np.int8)
+    q[0, :128] = 1
+    q[0, 128:] = -1
+    q[1, :128] = 0
+    q[1, 128:] = 1
+    q[2, :] = -1
+    out = oracle_mod.encode_i2s(q, 2.0)
+    exp = b"\xaa" * 32 + b"\x00" * 32 + b"\x55" * 32 + b"\xaa" * 32 + b"\x00" * 64
+    assert bytes(out[:192]) == exp
+    assert bytes(out[192:]) == struct.pack("<f", 2.0)
+
+
+def test_round_half_to_even(oracle_mod):
+    """Reading of "round": rint.  mean|w| = 1 so w_scale = 1 and the products
+    are exactly +-0.5 / +-1.5: 0.5 -> 0, 1.5 -> 2 -> clamped 1."""
+    w = np.array([1.5] * 32 + [0.5] * 32 + [-0.5] * 32 + [-1.5] * 32, np.float32).reshape(1, 128)
+    assert oracle_mod.weight_scale(w) == 1.0
+    q = oracle_mod.quantize_ternary(w, 1.0)
+    assert (q[0, :32] == 1).all() and (q[0, 32:96] == 0).all() and (q[0, 96:] == -1).all()
+
+
+def test_mean_abs_matches_numpy(oracle_mod):
+    w = wl.gen_latent_w(257, 384, seed=11)
+    ref = float(np.mean(np.abs(w.astype(np.float64))))
+    assert oracle_mod.mean_abs(w) == pytest.approx(ref, rel=1e-13)
+
+
+def test_gaussian_ternary_statistics(oracle_mod):
+    """For w ~ N(0, s), w_scale = 1/E|w| = 1/(s sqrt(2/pi)), so P(q = 0) =
+    P(|z| < 0.5 sqrt(2/pi)) = erf(0.5/sqrt(pi)) = 0.3101 and P(+1) = P(-1)."""
+    w = wl.gen_latent_w(1024, 1024, seed=5)
+    packed, s = oracle_mod.pack_i2s(w)
+    q = oracle_mod.unpack_i2s(packed, 1024, 1024)
+    p0 = math.erf(0.5 / math.sqrt(math.pi))
+    assert abs(p0 - 0.3101) < 1e-4
+    frac0 = float(np.mean(q == 0))
+    assert abs(frac0 - p0) < 0.003
+    assert abs(float(np.mean(q == 1)) - (1 - p0) / 2) < 0.003
+    assert abs(float(np.mean(q == -1)) - (1 - p0) / 2) < 0.003
+    assert set(np.unique(q).tolist()) <= {-1, 0, 1}
+    assert oracle_mod.count_invalid_codes(packed, 1024, 1024) == 0
+    # the scale is the reciprocal of the double-precision mean, rounded once
+    assert s * oracle_mod.mean_abs(w) == pytest.approx(1.0, abs=2 ** -23)
+
+
+def test_unpack_inverts_encode(oracle_mod):
+    rng = np.random.default_rng(3)
+    q = rng.integers(-1, 2, size=(5, 384), dtype=np.int8)
+    packed = oracle_mod.encode_i2s(q, 1.5)
+    assert np.array_equal(oracle_mod.unpack_i2s(packed, 5, 384), q)
+
+
+def test_encode_inverts_unpack_on_valid_bytes(oracle_mod):
+    """Every byte whose four fields avoid code 3 survives decode + encode."""
+    vals = [b for b in range(256) if all(((b >> s) & 3) != 3 for s in (0, 2, 4, 6))]
+    assert len(vals) == 81
+    stream = np.array((vals * 2)[:160] + [0x55] * 96, np.uint8)  # 256 bytes = 8 blocks
+    packed = np.concatenate([stream, np.frombuffer(struct.pack("<f", 1.0), np.uint8)])
+    q = oracle_mod.unpack_i2s(packed, 2, 512)
+    assert np.array_equal(oracle_mod.encode_i2s(q, 1.0), packed)
+
+
+def test_invalid_code_count(oracle_mod):
+    packed = np.full(32 + 4, 0x55, np.uint8)
+    packed[3] = 0xFF  # four fields of code 3
+    packed[7] = 0x57  # one
+    assert oracle_mod.count_invalid_codes(packed, 1, 128) == 5
+    q = oracle_mod.unpack_i2s(packed, 1, 128)
+    assert q[0, 3] == 2 and q[0, 32 + 3] == 2 and q[0, 96 + 7] == 2
+
+
+# ------------------------------------------------------------- RMSNorm pins ---
+
+def _torch_rmsnorm64(x, g, eps):
+    import torch
+
+    xt = torch.from_numpy(x.astype(np.float64))
+    return (torch.nn.functional.rms_norm(xt, (x.shape[1],), eps=eps) *
+            torch.from_numpy(g.astype(np.float64))).numpy()
+
+
+@pytest.mark.parametrize("K", [128, 640, 1024, 3072])
+def test_rmsnorm_matches_torch_f64(oracle_mod, K):
+    x = wl.gen_x(9, K, seed=K)
+    x[3] = 0.0  # a zero row stays zero (eps keeps rstd finite)
+    x[4] *= 1e-3
+    g = wl.gen_norm_w(K, seed=K + 1)
+    xn = oracle_mod.rmsnorm(x, g, wl.EPS)
+    ref = _torch_rmsnorm64(x, g, wl.EPS)
+    # three roundings (rstd to float, then two float multiplies), each at most
+    # 2^-24 relative
+    tol = 3.01 * 2.0 ** -24 * np.abs(ref) + 1e-30
+    assert np.all(np.abs(xn - ref) <= tol)
+    assert np.all(xn[3] == 0.0)
+
+
+def test_rmsnorm_eps_placement(oracle_mod):
+    """eps is added to the mean square, inside the square root: for a constant
+    row x = c with g = 1, xn = c / sqrt(c^2 + eps)."""
+    c = 1e-3
+    x = np.full((1, 128), c, np.float32)
+    g = np.ones(128, np.float32)
+    xn = oracle_mod.rmsnorm(x, g, 1e-6)
+    want = float(np.float32(c)) / math.sqrt(float(np.float32(c)) ** 2 + float(np.float32(1e-6)))
+    assert xn[0, 0] == pytest.approx(want, rel=3e-7)
+    assert abs(want - 0.7071) < 1e-3  # c^2 = eps: the eps term halves the mean square
+
+
+# ---------------------------------------------------------- activation pins ---
+
+def test_quant_a8_invariants(oracle_mod):
+    K = 1024
+    x = wl.gen_x(6, K, seed=21, outlier_frac=0.01)
+    x[2] = 0.0
+    x[3] = 0.75
+    g = wl.gen_norm_w(K, seed=22)
+    xn = oracle_mod.rmsnorm(x, g, wl.EPS)
+    xn[3] = oracle_mod.rmsnorm(x[3:4], np.ones(K, np.float32), wl.EPS)[0]
+    q, s, rs = oracle_mod.quant_a8(xn)
+    assert np.all(np.abs(q.astype(np.int32)) <= 127)
+    assert np.array_equal(rs, q.astype(np.int64).sum(axis=1).astype(np.int32))
+    for m in range(6):
+        amax = float(np.max(np.abs(xn[m])))
+        if amax == 0.0:
+            assert np.all(q[m] == 0)
+            assert s[m] == np.float32(127.0) / np.float32(1e-5)
+            continue
+        # the largest entry lands on +-127
+        k = int(np.argmax(np.abs(xn[m])))
+        assert abs(int(q[m, k])) == 127
+        # scale is 127 / amax up to one rounding
+        assert float(s[m]) * amax == pytest.approx(127.0, rel=2 ** -23)
+        # each code is the nearest integer to xn * a_scale
+        err = np.abs(xn[m].astype(np.float64) * float(s[m]) - q[m])
+        assert float(err.max()) <= 0.5 + 1e-5
+    assert np.all(np.abs(q[3]) == 127)  # constant row, unit norm weight
+
+
+# --------------------------------------------------------- contraction pins ---
+
+def test_matmul_matches_numpy(oracle_mod):
+    rng = np.random.default_rng(7)
+    M, K, N = 5, 384, 7
+    q = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    t = rng.integers(-1, 2, size=(N, K), dtype=np.int8)
+    packed = oracle_mod.encode_i2s(t, 1.0)
+    acc = oracle_mod.i2s_matmul(q, packed, N)
+    assert np.array_equal(acc, q.astype(np.int64) @ t.astype(np.int64).T)
+
+
+def test_matmul_special_weights(oracle_mod):
+    rng = np.random.default_rng(8)
+    M, K = 4, 128
+    q = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    rowsum = q.astype(np.int64).sum(axis=1)
+    for val, want in ((1, rowsum), (0, 0 * rowsum), (-1, -rowsum)):
+        t = np.full((3, K), val, np.int8)
+        acc = oracle_mod.i2s_matmul(q, oracle_mod.encode_i2s(t, 1.0), 3)
+        assert np.array_equal(acc, np.repeat(np.asarray(want)[:, None], 3, axis=1))
+    eye = np.eye(128, dtype=np.int8)  # one-hot rows pick single features
+    acc = oracle_mod.i2s_matmul(q, oracle_mod.encode_i2s(eye, 1.0), 128)
+    assert np.array_equal(acc, q.astype(np.int64))
+
+
+def test_matmul_extreme_sums(oracle_mod):
+    """Largest magnitudes the int32 accumulator meets at K = 16384."""
+    K = 16384
+    q = np.full((2, K), 127, np.int8)
+    q[1, 1::2] = -127
+    t = np.ones((2, K), np.int8)
+    t[1, 1::2] = -1
+    acc = oracle_mod.i2s_matmul(q, oracle_mod.encode_i2s(t, 1.0), 2)
+    assert acc[0, 0] == 127 * K and acc[1, 1] == 127 * K
+    assert acc[0, 1] == 0 and acc[1, 0] == 0
+
+
+def test_rescale_against_f64(oracle_mod):
+    rng = np.random.default_rng(9)
+    acc = rng.integers(-2_000_000, 2_000_000, size=(6, 11), dtype=np.int64)
+    a_scale = rng.uniform(1.0, 200.0, size=6).astype(np.float32)
+    w_scale = np.float32(37.25)
+    y = oracle_mod.rescale(acc, a_scale, float(w_scale))
+    ref = acc / a_scale.astype(np.float64)[:, None] / float(w_scale)
+    # two reciprocals and two products, each rounded once
+    assert np.all(np.abs(y - ref) <= 4 * 2.0 ** -24 * np.abs(ref))
+
+
+# ------------------------------------------------------------ whole chain ---
+
+@pytest.mark.parametrize("M,K,N", [(3, 128, 5), (4, 640, 33), (2, 1024, 17)])
+def test_forward_within_quantisation_bound(oracle_mod, M, K, N):
+    """y against the unquantised activations: sum_k t * (q/a_scale - xn) is at
+    most sum_k |t| * 0.5 / a_scale, all divided by w_scale."""
+    x = wl.gen_x(M, K, seed=M * K, outlier_frac=0.01)
+    g = wl.gen_norm_w(K, seed=N)
+    w = wl.gen_latent_w(N, K, seed=K + N)
+    packed, ws = oracle_mod.pack_i2s(w)
+    y, xn, q, a_s, acc = oracle_mod.bitlinear_forward(x, g, packed, ws, N, intermediates=True)
+    t = oracle_mod.quantize_ternary(w, ws).astype(np.float64)  # independent of unpack
+    xn64 = _torch_rmsnorm64(x, g, wl.EPS)
+    ideal = xn64 @ (t / float(ws)).T
+    bound = (np.abs(t).sum(axis=1)[None, :] * 0.5 / a_s.astype(np.float64)[:, None]) / float(ws)
+    assert np.all(np.abs(y - ideal) <= 1.01 * bound + 1e-5 * np.abs(ideal) + 1e-6)
+    # and exactly the integer product of the codes
+    assert np.array_equal(acc, q.astype(np.int64) @ t.astype(np.int64).T)
+
+
+def test_forward_rows_subset(oracle_mod):
+    M, K, N = 7, 256, 9
+    x, g, w = wl.gen_projection(0, 0, 0, M, K, N)
+    packed, ws = oracle_mod.pack_i2s(w)
+    full = oracle_mod.bitlinear_forward(x, g, packed, ws, N)
+    rows = np.array([6, 0, 3])
+    part = oracle_mod.bitlinear_forward(x, g, packed, ws, N, rows=rows)
+    assert np.array_equal(part, full[rows])
