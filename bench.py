@@ -1,0 +1,629 @@
+#!/usr/bin/env python3
+"""Throughput of the W1.58A8 BitLinear hot path on one GB300 (or N replicas).
+
+Default workload (one step = one decode layer): all seven BitLinear projections
+of one Qwen3-shaped 0.6B layer at M=1 token (q 1024->2048, k/v 1024->1024,
+o 2048->1024, gate/up 1024->3072, down 3072->1024), each with its own seeded
+input, norm weight and ternary weights, run as ONE grouped launch
+(bitnet_bitlinear_forward_group).  Steps rotate through a pool of distinct
+layers whose I2_S weights total more than twice the L2 cache, so every step
+streams its weights from HBM.  Metric: weight-stream GB/s = algorithmic bytes
+(packed weights + scale + x + norm weight + y) per step / time.
+
+Other workloads (--workload): q_proj_m8 (M=8, K=1024, N=2048), gemma3_prefill
+(seven Gemma3-shaped projections at M=32768 with 1% x20 outlier features),
+qwen3_prefill_stack (28 layers x 7 projections at M=32768), sweep (K, N in
+{1024,4096,8192,16384} x M in {1,16,128,2048,16384}).
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on the
+host cores on a bounded sample of the same workload.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torchrun, one replica per GPU (the projection shards by token rows and needs
+no exchange; this benchmark runs independent replicas, weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BitLinear int8-TOPS (prefill) and weight-stream GB/s (M=1) vs GB300 roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "bitlinear_rmsnorm_token_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile_md, sha):
+    """dram bytes per launch recorded by an ncu capture of this exact kernel
+    source (a line 'traffic_bytes_per_launch: <int> source_sha: <sha>'), else None."""
+    path = os.path.join(ROOT, "profiles", profile_md)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha:\s*([0-9a-f]+)", text)
+    if m and m.group(2) == sha:
+        return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples with wall-clock timestamps."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.flush()
+
+    def summary(self, t0, t1):
+        rows = []
+        try:
+            with open(self.out.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                        frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                        rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[5:9]))
+                    except (ValueError, IndexError):
+                        continue
+        finally:
+            os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "whole run"
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def dist_setup(gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = os.environ.get("BENCH_DIST_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def reduce_max(value, world):
+    """Max of a float over ranks (gloo or nccl)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------- decode workload
+
+def decode_layer_bytes(layer_shapes, M=1):
+    """Algorithmic bytes of one step: I2_S weights + scale, x, norm weight, y."""
+    return sum(p.N * p.K // 4 + 4 + M * p.K * 4 + p.K * 4 + M * p.N * 4 for p in layer_shapes)
+
+
+def build_decode_pool(torch, bn, wl, n_layers, device, M=1):
+    """n_layers distinct Qwen3-shaped layers: weights packed on the device from
+    seeded latents; x / norm weights seeded.  Inputs for one layer are views of
+    one contiguous buffer (one host<->device copy per step in the e2e loop)."""
+    shapes = wl.QWEN3_0P6B_LAYER
+    kx = sum(p.K for p in shapes)
+    ny = sum(p.N for p in shapes)
+    layers = []
+    for layer in range(n_layers):
+        xbuf = torch.empty((M * kx,), dtype=torch.float32, device=device)
+        ybuf = torch.zeros((M * ny,), dtype=torch.float32, device=device)
+        items = []
+        ox = oy = 0
+        for i, p in enumerate(shapes):
+            seed_w = wl.seed_for(1, layer, i, wl.T_W)
+            w = wl.gen_device((p.N, p.K), seed_w, device, std=0.02)
+            packed, ws = bn.pack_i2s(w)
+            del w
+            x = wl.gen_x(M, p.K, wl.seed_for(1, layer, i, wl.T_X))
+            g = wl.gen_norm_w(p.K, wl.seed_for(1, layer, i, wl.T_G))
+            xv = xbuf[ox:ox + M * p.K].view(M, p.K)
+            xv.copy_(torch.from_numpy(x))
+            yv = ybuf[oy:oy + M * p.N].view(M, p.N)
+            ox += M * p.K
+            oy += M * p.N
+            items.append((xv, torch.from_numpy(g).to(device), packed, ws, p.N, yv))
+        layers.append({"items": items, "desc": bn.make_group(items), "xbuf": xbuf, "ybuf": ybuf})
+    return layers
+
+
+def check_decode_layer(oracle, layer, M=1):
+    """Oracle check of one pool layer (run after timing): every projection's y."""
+    worst = 0.0
+    for (xv, g, packed, ws, N, yv) in layer["items"]:
+        x = xv.cpu().numpy()
+        ref = oracle.bitlinear_forward(x, g.cpu().numpy(), packed.cpu().numpy(), ws, N)
+        y = yv.cpu().numpy()
+        rel = np.linalg.norm(y - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+        worst = max(worst, float(rel.max()))
+    return worst
+
+
+def run_decode(args, rank, world, local):
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    bn.lib()
+    M = 1
+    shapes = wl.QWEN3_0P6B_LAYER
+    step_bytes = decode_layer_bytes(shapes, M)
+    weight_bytes = sum(p.N * p.K // 4 + 4 for p in shapes)
+    n_layers = max(8, int(np.ceil(2.0 * L2_BYTES / weight_bytes)))  # pool > 2x L2
+    pool = build_decode_pool(torch, bn, wl, n_layers, device, M)
+    flags = bn.FLAG_WEIGHTS_STATIC
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+
+    # one graph holds `chunk` consecutive steps; replays continue the rotation
+    chunk = n_layers * max(1, 512 // n_layers)
+    with torch.cuda.stream(stream):
+        for i in range(n_layers):  # eager warm-up (also loads the module)
+            bn.bitlinear_forward_group(pool[i]["desc"], M, wl.EPS, flags, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+    # tail graph so that exactly `steps` steps are timed
+    tail_n = args.steps % chunk
+    tail = None
+    if tail_n:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for i in range(tail_n):
+                bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+
+    def run_steps(n):
+        with torch.cuda.stream(stream):
+            for _ in range(n // chunk):
+                graph.replay()
+            if n % chunk:
+                assert tail is not None and n % chunk == tail_n
+                tail.replay()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    warm_reps = max(1, -(-args.warmup // chunk))  # at least `warmup` steps, whole graphs
+    with torch.cuda.stream(stream):
+        for _ in range(warm_reps):
+            graph.replay()
+    args.warmup = warm_reps * chunk
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    run_steps(args.steps)
+    ev1.record(stream)
+    ev1.synchronize()
+    t1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.stop()
+    ms_local = ev0.elapsed_time(ev1)
+    ms = reduce_max(ms_local, world)
+    units = reduce_sum(float(step_bytes) * args.steps, world)
+    value = units / (ms * 1e-3) / 1e9
+    clocks = sampler.summary(t0, t1)
+
+    # parity of the timed configuration: every projection of two pool layers
+    import oracle
+
+    worst = 0.0
+    for li in (0, n_layers - 1):
+        worst = max(worst, check_decode_layer(oracle, pool[li], M))
+    dev_status = bn.last_device_status()
+
+    # e2e through the public API with host buffers: per step, H2D of the
+    # layer's activations from pinned memory, the grouped call, D2H of y
+    kx = pool[0]["xbuf"].numel()
+    ny = pool[0]["ybuf"].numel()
+    e2e_steps = min(args.steps, 2000)
+    xh = torch.empty((n_layers, kx), dtype=torch.float32).pin_memory()
+    for i in range(n_layers):
+        xh[i].copy_(pool[i]["xbuf"].cpu())
+    yh = torch.empty((n_layers, ny), dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(stream):
+        for i in range(min(n_layers, 64)):
+            pool[i % n_layers]["xbuf"].copy_(xh[i % n_layers], non_blocking=True)
+            bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+            yh[i % n_layers].copy_(pool[i % n_layers]["ybuf"], non_blocking=True)
+    stream.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e2e_steps):
+            L = pool[i % n_layers]
+            L["xbuf"].copy_(xh[i % n_layers], non_blocking=True)
+            bn.bitlinear_forward_group(L["desc"], M, wl.EPS, flags, stream=stream)
+            yh[i % n_layers].copy_(L["ybuf"], non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_units = reduce_sum(float(step_bytes) * e2e_steps, world)
+
+    hbm, _, _, peak_kind = peaks()
+    per_launch_ms = ms_local / args.steps
+    achieved = step_bytes / (per_launch_ms * 1e-3) / 1e9
+    sha = source_sha("gemv.cu", "rowquant.cuh", "common.cuh")
+    traffic = profiled_traffic("decode_group_qwen3_layer.md", sha)
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 x ternary -> int32, fp32 I/O", "data": "synthetic",
+        "config": {"workload": "qwen3_0p6b_decode_layer_M1_7proj", "tokens": M,
+                   "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes],
+                   "bytes_per_step": step_bytes, "weight_pool_layers": n_layers,
+                   "weight_pool_bytes": n_layers * weight_bytes,
+                   "l2": "inputs larger than L2: steps rotate through a weight pool > 2x L2 (no flush)",
+                   "launch": "one grouped kernel per step, CUDA graph replay, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "k_decode (grouped BitLinear GEMV)", "achieved": round(achieved, 2),
+                     "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": step_bytes},
+        "e2e": {"value": round(e2e_units / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": kx * 4, "d2h_bytes_per_step": ny * 4, "steps": e2e_steps,
+                "api": "bitnet_bitlinear_forward_group from Python, one call per step"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "parity": {"oracle_worst_row_rel_l2": worst, "device_status": bn.status_string(dev_status)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_decode(args)
+    return out
+
+
+def cpu_baseline_decode(args, budget_s=None):
+    """The oracle, as it stands, on the host cores: whole decode layers (7
+    projections at M=1, packed on the host by the oracle) until ~budget_s."""
+    import oracle
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    budget_s = args.cpu_seconds if budget_s is None else budget_s
+    shapes = wl.QWEN3_0P6B_LAYER
+    step_bytes = decode_layer_bytes(shapes, 1)
+    layers = []
+    for layer in range(2):
+        items = []
+        for i, p in enumerate(shapes):
+            x, g, w = wl.gen_projection(1, layer, i, 1, p.K, p.N)
+            packed, ws = oracle.pack_i2s(w)
+            items.append((x, g, packed, ws, p.N))
+        layers.append(items)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for (x, g, packed, ws, N) in layers[n % 2]:
+            oracle.bitlinear_forward(x, g, packed, ws, N)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{n} decode layers (7 projections each, M=1) in {dt:.1f} s"}
+
+
+# ----------------------------------------------------- other workloads
+
+def time_region(torch, stream, fn, steps, warmup):
+    for _ in range(warmup):
+        fn()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_q_proj_m8(args, rank, world, local):
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    M, K, N = 8, 1024, 2048
+    pool = []
+    nl = int(np.ceil(2.0 * L2_BYTES / (N * K / 4)))
+    for l in range(nl):
+        x, g, w = wl.gen_projection(0, l, 0, M, K, N)
+        packed, ws = bn.pack_i2s(torch.from_numpy(w).to(device))
+        pool.append((torch.from_numpy(x).to(device), torch.from_numpy(g).to(device), packed, ws,
+                     torch.empty((M, N), dtype=torch.float32, device=device)))
+    stream = torch.cuda.Stream(device)
+    it = [0]
+
+    def step():
+        x, g, packed, ws, y = pool[it[0] % nl]
+        it[0] += 1
+        bn.bitlinear_forward(x, g, packed, ws, N, wl.EPS, y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(nl):
+            step()
+    stream.synchronize()
+    g_ = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_, stream=stream):
+        for _ in range(nl):
+            step()
+    reps = max(1, args.steps // nl)
+    with torch.cuda.stream(stream):
+        ms = time_region(torch, stream, g_.replay, reps, max(3, args.warmup // nl)) / nl
+    step_bytes = N * K // 4 + 4 + M * K * 4 + K * 4 + M * N * 4
+    return {"metric": METRIC, "value": round(step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": reps * nl, "ms_per_step": ms, "us_per_projection": ms * 1e3,
+            "tops": 2.0 * M * N * K / (ms * 1e-3) / 1e12,
+            "config": {"workload": "q_proj_M8_K1024_N2048", "launch": "CUDA graph, weight pool > 2x L2"}}
+
+
+def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, outlier_frac, stream):
+    """Buffers for one layer's projections at M tokens (x drawn on the device)."""
+    items = []
+    for i, p in enumerate(shapes):
+        x = wl.gen_device((M, p.K), wl.seed_for(config, layer, i, wl.T_X), device)
+        if outlier_frac > 0:
+            cols = torch.from_numpy(wl.gen_device_outlier_cols(p.K, wl.seed_for(config, layer, i, wl.T_OUTLIER),
+                                                               outlier_frac)).to(device)
+            x[:, cols] *= 20.0
+        g = torch.from_numpy(wl.gen_norm_w(p.K, wl.seed_for(config, layer, i, wl.T_G))).to(device)
+        w = wl.gen_device((p.N, p.K), wl.seed_for(config, layer, i, wl.T_W), device, std=0.02)
+        packed, ws = bn.pack_i2s(w)
+        del w
+        y = torch.empty((M, p.N), dtype=torch.float32, device=device)
+        items.append((p, x, g, packed, ws, y))
+    return items
+
+
+def run_prefill(args, rank, world, local, which):
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    import oracle
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    M = 32768
+    if which == "gemma3_prefill":
+        shapes, n_layers, frac, cfg = wl.GEMMA3_270M_LAYER, 1, 0.01, 2
+    else:
+        shapes, n_layers, frac, cfg = wl.QWEN3_0P6B_LAYER, wl.QWEN3_0P6B_LAYERS, 0.0, 3
+    stream = torch.cuda.Stream(device)
+    layers = [prefill_projection_step(torch, bn, wl, shapes, M, device, cfg, l, frac, stream)
+              for l in range(n_layers)]
+    torch.cuda.synchronize()
+
+    def step():
+        for items in layers:
+            for (p, x, g, packed, ws, y) in items:
+                bn.bitlinear_forward(x, g, packed, ws, p.N, wl.EPS, y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_region(torch, stream, step, max(1, args.steps), max(1, min(args.warmup, 3)))
+    flops = sum(2.0 * M * p.N * p.K for p in shapes) * n_layers
+    alg_bytes = sum(M * p.K * 4 + p.K * 4 + p.N * p.K / 4 + 4 + M * p.N * 4 for p in shapes) * n_layers
+    # sampled-row parity of the first and last projection
+    worst = 0.0
+    rows = np.random.default_rng(0).choice(M, 32, replace=False)
+    for (p, x, g, packed, ws, y) in (layers[0][0], layers[-1][-1]):
+        ref = oracle.bitlinear_forward(x[rows].cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws, p.N)
+        yy = y[rows].cpu().numpy()
+        worst = max(worst, float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max()))
+    return {"metric": METRIC, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "n_gpus": world,
+            "ms_per_step": ms, "steps": args.steps, "alg_GBps": alg_bytes / (ms * 1e-3) / 1e9,
+            "config": {"workload": which, "tokens": M, "layers": n_layers,
+                       "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
+            "parity": {"oracle_worst_row_rel_l2": worst}}
+
+
+def run_sweep(args, rank, world, local):
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    hbm, bf16, _, _ = peaks()
+    rows = []
+    for K in wl.SWEEP_KN:
+        for N in wl.SWEEP_KN:
+            wb = N * K // 4
+            nw = max(1, int(np.ceil(2.0 * L2_BYTES / wb))) if wb < 2 * L2_BYTES else 1
+            nw = min(nw, 64)
+            ws_list = []
+            for i in range(nw):
+                w = wl.gen_device((N, K), wl.seed_for(4, K, N, i), device, std=0.02)
+                ws_list.append(bn.pack_i2s(w))
+                del w
+            g = torch.from_numpy(wl.gen_norm_w(K, seed=K)).to(device)
+            for M in wl.SWEEP_M:
+                x = wl.gen_device((M, K), wl.seed_for(4, M, K, N), device)
+                y = torch.empty((M, N), dtype=torch.float32, device=device)
+                it = [0]
+
+                def step():
+                    packed, s = ws_list[it[0] % nw]
+                    it[0] += 1
+                    bn.bitlinear_forward(x, g, packed, s, N, wl.EPS, y, stream=stream)
+
+                with torch.cuda.stream(stream):
+                    reps = 20 if M * N * K < 2**36 else 5
+                    ms = time_region(torch, stream, step, reps, 3)
+                b = wb + 4 + M * K * 4 + K * 4 + M * N * 4
+                rows.append({"M": M, "K": K, "N": N, "us": ms * 1e3, "GBps": b / (ms * 1e-3) / 1e9,
+                             "TOPS": 2.0 * M * N * K / (ms * 1e-3) / 1e12,
+                             "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm,
+                             "tensor_frac": 2.0 * M * N * K / (ms * 1e-3) / 1e12 / bf16})
+                del x, y
+            del ws_list
+            torch.cuda.empty_cache()
+    return {"metric": METRIC, "workload": "sweep", "rows": rows}
+
+
+# ------------------------------------------------------------ reference
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    cb = cpu_baseline_decode(args, budget_s=None)
+    steps = args.steps_ref
+    shapes = __import__("bitlinear_rmsnorm_token_gb300.workloads", fromlist=["x"]).QWEN3_0P6B_LAYER
+    step_bytes = decode_layer_bytes(shapes, 1)
+    value = cb["value"]
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": step_bytes / (value * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary -> int64, fp32",
+            "data": "synthetic",
+            "config": {"workload": "qwen3_0p6b_decode_layer_M1_7proj", "tokens": 1,
+                       "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300000)
+    ap.add_argument("--warmup", type=int, default=20000)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_decode_layer",
+                    choices=["qwen3_decode_layer", "q_proj_m8", "gemma3_prefill", "qwen3_prefill_stack", "sweep"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.steps_ref = args.steps
+
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    elif args.workload == "qwen3_decode_layer":
+        out = run_decode(args, rank, world, local)
+    elif args.workload == "q_proj_m8":
+        out = run_q_proj_m8(args, rank, world, local)
+    elif args.workload == "sweep":
+        out = run_sweep(args, rank, world, local)
+    else:
+        out = run_prefill(args, rank, world, local, args.workload)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

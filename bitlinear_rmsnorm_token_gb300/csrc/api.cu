@@ -1,0 +1,279 @@
+// api.cu -- the C ABI declared in include/bitnet.h: argument checks, dispatch
+// between the decode and tensor-core paths, per-device state.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace bitnet {
+
+// Per-device record of device-side failures (bitnet_last_device_status).
+__device__ unsigned g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceContext g_ctx[kMaxDevices];
+bool g_ready[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_shape(int64_t M, int64_t K, int64_t N) {
+  if (M < 1 || N < 1) return BITNET_ERR_INVALID_ARG;
+  if (K < BITNET_I2S_BLOCK || K % BITNET_I2S_BLOCK != 0 || K > BITNET_MAX_K) return BITNET_ERR_UNSUPPORTED_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1) return BITNET_ERR_UNSUPPORTED_SHAPE;
+  return BITNET_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA; }
+
+}  // namespace
+
+int device_context(DeviceContext** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return BITNET_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ready[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BITNET_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return BITNET_ERR_NO_DEVICE;  // built for sm_103a only
+    DeviceContext c;
+    c.device = dev;
+    c.num_sms = prop.multiProcessorCount;
+    void* ew = nullptr;
+    if (cudaGetSymbolAddress(&ew, g_error_word) != cudaSuccess) return BITNET_ERR_CUDA;
+    c.err_word = static_cast<unsigned*>(ew);
+    if (cudaMemset(c.err_word, 0, sizeof(unsigned)) != cudaSuccess) return BITNET_ERR_CUDA;
+    cudaMemPoolProps pp = {};
+    pp.allocType = cudaMemAllocationTypePinned;
+    pp.handleTypes = cudaMemHandleTypeNone;
+    pp.location.type = cudaMemLocationTypeDevice;
+    pp.location.id = dev;
+    if (cudaMemPoolCreate(&c.pool, &pp) != cudaSuccess) return BITNET_ERR_CUDA;
+    uint64_t keep = UINT64_MAX;  // keep freed blocks cached in the pool
+    cudaMemPoolSetAttribute(c.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_ctx[dev] = c;
+    g_ready[dev] = true;
+  }
+  *out = &g_ctx[dev];
+  return BITNET_OK;
+}
+
+int pool_alloc(DeviceContext* ctx, void** p, size_t bytes, cudaStream_t stream) {
+  if (cudaMallocFromPoolAsync(p, bytes, ctx->pool, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return BITNET_ERR_CUDA;
+  }
+  return BITNET_OK;
+}
+
+void pool_free(void* p, cudaStream_t stream) {
+  if (p) cudaFreeAsync(p, stream);
+}
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+}  // namespace bitnet
+
+using namespace bitnet;
+
+extern "C" {
+
+size_t bitnet_i2s_packed_bytes(int64_t N, int64_t K) {
+  if (N < 1 || K < BITNET_I2S_BLOCK || K % BITNET_I2S_BLOCK != 0) return 0;
+  return static_cast<size_t>(N) * static_cast<size_t>(K) / 4 + 4;
+}
+
+const char* bitnet_status_string(int status) {
+  switch (status) {
+    case BITNET_OK: return "ok";
+    case BITNET_ERR_INVALID_ARG: return "invalid argument";
+    case BITNET_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (K must be a positive multiple of 128, <= 65536)";
+    case BITNET_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case BITNET_ERR_CUDA: return "CUDA error";
+    case BITNET_ERR_TIMEOUT: return "device-side wait timed out";
+    case BITNET_ERR_NO_DEVICE: return "no sm_103 CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int bitnet_pack_i2s(const float* w, int64_t N, int64_t K, uint8_t* packed, float* w_scale_out,
+                    bitnet_stream_t stream) {
+  if (!w || !packed) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(1, K, N);
+  if (rc) return rc;
+  if (!aligned16(w) || !aligned16(packed)) return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int np = pack_num_partials(N * K);
+  double* partials = nullptr;
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&partials), np * sizeof(double), s))) return rc;
+  cudaError_t e = launch_pack_i2s(ctx, w, N, K, packed, partials, np, s);
+  pool_free(partials, s);
+  if (e != cudaSuccess) return BITNET_ERR_CUDA;
+  if (w_scale_out) {
+    e = cudaMemcpyAsync(w_scale_out, packed + N * K / 4, sizeof(float), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return BITNET_ERR_CUDA;
+  }
+  return BITNET_OK;
+}
+
+int bitnet_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_t* w_ternary, bitnet_stream_t stream) {
+  if (!packed || !w_ternary) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(1, K, N);
+  if (rc) return rc;
+  if (!aligned16(packed) || !aligned16(w_ternary)) return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  return cuda_status(launch_unpack_i2s(packed, N, K, w_ternary, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bitnet_rmsnorm_quant_a8(const float* x, const float* norm_w, int64_t M, int64_t K, float eps, int8_t* a_codes,
+                            float* a_scale, int32_t* a_rowsum, float* xn_out, bitnet_stream_t stream) {
+  if (!x || !norm_w || !a_codes || !a_scale) return BITNET_ERR_INVALID_ARG;
+  if (!(eps > 0.0f)) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(M, K, 1);
+  if (rc) return rc;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(a_codes) || !aligned4(a_scale) ||
+      (a_rowsum && !aligned4(a_rowsum)) || (xn_out && !aligned16(xn_out)))
+    return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  return cuda_status(launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, a_codes, nullptr, a_scale,
+                                          a_rowsum, xn_out, false, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* packed_w, float w_scale, int64_t M,
+                    int64_t K, int64_t N, float* y, int32_t* acc_out, bitnet_stream_t stream) {
+  if (!a_codes || !a_scale || !packed_w || !y) return BITNET_ERR_INVALID_ARG;
+  if (!(w_scale > 0.0f) || w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(M, K, N);
+  if (rc) return rc;
+  if (!aligned16(a_codes) || !aligned4(a_scale) || !aligned16(packed_w) || !aligned16(y) ||
+      (acc_out && !aligned16(acc_out)))
+    return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (decode_supported(M, K)) {
+    DecodeJob j = {};
+    j.codes = a_codes;
+    j.a_scale = a_scale;
+    j.w = packed_w;
+    j.w_scale = w_scale;
+    j.K = static_cast<int>(K);
+    j.N = static_cast<int>(N);
+    j.y = y;
+    j.acc_out = acc_out;
+    return cuda_status(launch_decode(ctx, &j, 1, static_cast<int>(M), 0.0f, false, false, s));
+  }
+  __half* f16 = nullptr;
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&f16), static_cast<size_t>(M * K) * 2, s))) return rc;
+  cudaError_t e = launch_codes_to_f16(a_codes, f16, M * K, s);
+  int st = BITNET_OK;
+  if (e == cudaSuccess) e = launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, true, s, &st);
+  pool_free(f16, s);
+  if (st != BITNET_OK) return st;
+  return cuda_status(e);
+}
+
+int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w, float w_scale, int64_t M,
+                             int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream) {
+  if (!x || !norm_w || !packed_w || !y) return BITNET_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !(w_scale > 0.0f) || w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(M, K, N);
+  if (rc) return rc;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y)) return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (decode_supported(M, K)) {
+    DecodeJob j = {};
+    j.x = x;
+    j.g = norm_w;
+    j.w = packed_w;
+    j.w_scale = w_scale;
+    j.K = static_cast<int>(K);
+    j.N = static_cast<int>(N);
+    j.y = y;
+    return cuda_status(launch_decode(ctx, &j, 1, static_cast<int>(M), eps, true, false, s));
+  }
+  // norm + quant to fp16 codes, then the tensor-core contraction
+  const size_t code_bytes = (static_cast<size_t>(M * K) * 2 + 255) & ~size_t(255);
+  uint8_t* ws = nullptr;
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + static_cast<size_t>(M) * 4, s))) return rc;
+  __half* f16 = reinterpret_cast<__half*>(ws);
+  float* as = reinterpret_cast<float*>(ws + code_bytes);
+  cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr,
+                                       false, s);
+  int st = BITNET_OK;
+  if (e == cudaSuccess) e = launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, true, s, &st);
+  pool_free(ws, s);
+  if (st != BITNET_OK) return st;
+  return cuda_status(e);
+}
+
+int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M, float eps,
+                                   uint32_t flags, bitnet_stream_t stream) {
+  if (!projs || count < 1 || count > BITNET_MAX_GROUP) return BITNET_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || (flags & ~BITNET_FLAG_WEIGHTS_STATIC)) return BITNET_ERR_INVALID_ARG;
+  if (M < 1) return BITNET_ERR_INVALID_ARG;
+  DecodeJob jobs[BITNET_MAX_GROUP];
+  for (int i = 0; i < count; ++i) {
+    const bitnet_projection& p = projs[i];
+    if (!p.x || !p.norm_w || !p.packed_w || !p.y) return BITNET_ERR_INVALID_ARG;
+    if (!(p.w_scale > 0.0f) || p.w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
+    int rc = check_shape(M, p.K, p.N);
+    if (rc) return rc;
+    if (!aligned16(p.x) || !aligned16(p.norm_w) || !aligned16(p.packed_w) || !aligned16(p.y))
+      return BITNET_ERR_MISALIGNED;
+    if (!decode_supported(M, p.K)) return BITNET_ERR_UNSUPPORTED_SHAPE;
+    DecodeJob j = {};
+    j.x = p.x;
+    j.g = p.norm_w;
+    j.w = p.packed_w;
+    j.w_scale = p.w_scale;
+    j.K = static_cast<int>(p.K);
+    j.N = static_cast<int>(p.N);
+    j.y = p.y;
+    jobs[i] = j;
+  }
+  DeviceContext* ctx;
+  int rc = device_context(&ctx);
+  if (rc) return rc;
+  return cuda_status(launch_decode(ctx, jobs, count, static_cast<int>(M), eps, true,
+                                   (flags & BITNET_FLAG_WEIGHTS_STATIC) != 0,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bitnet_last_device_status(bitnet_stream_t stream) {
+  DeviceContext* ctx;
+  int rc = device_context(&ctx);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return BITNET_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ctx->err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return BITNET_ERR_CUDA;
+  if (word == 0) return BITNET_OK;
+  if (cudaMemset(ctx->err_word, 0, sizeof(unsigned)) != cudaSuccess) return BITNET_ERR_CUDA;
+  return BITNET_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,353 @@
+// gemm_tc.cu -- prefill BitLinear contraction on the 5th-generation tensor cores.
+//
+// acc[m, n] = sum_k q[m, k] * (code(n, k) - 1)   (int8 activations x ternary
+// weights, the product of ggml_vec_dot_i2_i8_s named in section 6.4 of "BitNet
+// Embeddings GGUF Conversion Implementation"), then y = (acc / a_scale[m]) /
+// w_scale in fp32 ("BitNet Inference Framework", "Quantization (W1.58A8)").
+//
+// sm_103a has no integer tcgen05 MMA, so the contraction runs as kind::f16 with
+// fp16 operands that hold integers: activation codes in [-128, 127] and
+// ternary weights are exact in fp16, every product is exact, and every partial
+// sum is an integer of magnitude <= 127 * K < 2^24 (K <= 65536), so the fp32
+// TMEM accumulator holds the exact integer.
+//
+// One CTA per SM, persistent over output tiles of 128 weight rows x BN tokens:
+//   warp 8     TMA producer: token codes (fp16, 64-wide K slabs, 128B swizzle)
+//              and the tile's raw I2_S bytes (one 128-value block per row)
+//   warps 0-3  unpack: thread t decodes weight row t of the tile from its 32
+//              packed bytes into fp16 (magic-number conversion: 0x6400|c is
+//              1024+c, minus 1025) straight into the 128B-swizzled K-major
+//              layout the MMA reads; each block feeds two 64-wide stages
+//   warp 9     allocates TMEM (2 x BN columns: two accumulators) and one lane
+//              issues tcgen05.mma (M=128 weights, N=BN tokens, K=16) per slab
+//   warps 4-7  epilogue: tcgen05.ld of their TMEM lane quadrant, rescale,
+//              coalesced fp32 stores (a warp writes 32 consecutive outputs of
+//              one token), overlapping the next tile's MMAs
+// Every wait is bounded; an expired wait sets the device error word and the
+// CTA unwinds without trapping.
+#include "common.cuh"
+#include "internal.h"
+#include "rowquant.cuh"
+
+namespace bitnet {
+namespace {
+
+constexpr int kBM = 128;                   // weight rows per tile (MMA M)
+constexpr int kBK = 64;                    // K per stage: one 128-byte swizzle row of fp16
+constexpr int kStages = 4;                 // operand stages
+constexpr int kPkSlots = 4;                // packed-weight slots (one I2_S block column each)
+constexpr int kThreads = 320;
+constexpr int kAStageBytes = kBM * kBK * 2;           // 16 KB
+constexpr int kPkSlotBytes = kBM * 32;                // 4 KB
+
+template <int BN>
+struct TcLayout {
+  static constexpr int kBStageBytes = BN * kBK * 2;
+  static constexpr int offA = 0;
+  static constexpr int offB = offA + kStages * kAStageBytes;
+  static constexpr int offP = offB + kStages * kBStageBytes;
+  static constexpr int offInv = offP + kPkSlots * kPkSlotBytes;     // [4 warps][BN] float
+  static constexpr int offBar = offInv + 4 * BN * 4;
+  static constexpr int kNumBars = 3 * kStages + 2 * kPkSlots + 4;
+  static constexpr int offMisc = offBar + kNumBars * 8;             // tmem base, abort flag
+  static constexpr int kBytes = offMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;                      // room to align the base to 1 KB
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Four 2-bit codes (one per byte, values 0..2) -> two half2 words holding code-1.
+__device__ __forceinline__ void codes_to_h2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+  const uint32_t kMagic = 0x64646464u;     // high byte of fp16 1024.0
+  const uint32_t kBias = 0x64016401u;      // half2(1025, 1025)
+  uint32_t a = prmt(v, kMagic, 0x4140u);   // {1024 + c0, 1024 + c1}
+  uint32_t b = prmt(v, kMagic, 0x4342u);   // {1024 + c2, 1024 + c3}
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<const __half2*>(&kBias));
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), *reinterpret_cast<const __half2*>(&kBias));
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
+              const float* __restrict__ a_scale, float inv_w, int M, int N, int K, float* __restrict__ y,
+              int32_t* __restrict__ acc_out, unsigned* err) {
+  using L = TcLayout<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sA = smem + L::offA;
+  uint8_t* sB = smem + L::offB;
+  uint8_t* sP = smem + L::offP;
+  float* sInv = reinterpret_cast<float*>(smem + L::offInv);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
+  uint64_t* tok_full = bars;
+  uint64_t* a_full = bars + kStages;
+  uint64_t* st_empty = bars + 2 * kStages;
+  uint64_t* pk_full = bars + 3 * kStages;
+  uint64_t* pk_empty = pk_full + kPkSlots;
+  uint64_t* acc_full = pk_empty + kPkSlots;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_wt = (N + kBM - 1) / kBM;
+  const int n_mt = (M + BN - 1) / BN;
+  const int num_tiles = n_wt * n_mt;
+  const int nkb = K >> 7;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&tok_full[i], 1);
+      mbar_init(&a_full[i], 4);
+      mbar_init(&st_empty[i], 1);
+    }
+    for (int i = 0; i < kPkSlots; ++i) {
+      mbar_init(&pk_full[i], 1);
+      mbar_init(&pk_empty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 2 * BN);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_tok);
+    prefetch_tensormap(&tm_w);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // everything below reads what the previous kernel on the stream produced
+  pdl_wait();
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0, sph = 0, p = 0, pph = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int n0 = (tile % n_wt) * kBM;
+        const int m0 = (tile / n_wt) * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&pk_empty[p], pph ^ 1, err, abort_flag)) goto producer_done;
+          mbar_arrive_expect_tx(&pk_full[p], kPkSlotBytes);
+          tma_load_2d(sP + p * kPkSlotBytes, &tm_w, kb * 32, n0, &pk_full[p]);
+          if (++p == kPkSlots) { p = 0; pph ^= 1; }
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto producer_done;
+            mbar_arrive_expect_tx(&tok_full[s], L::kBStageBytes);
+            tma_load_2d(sB + s * L::kBStageBytes, &tm_tok, kb * 128 + hf * kBK, m0, &tok_full[s]);
+            if (++s == kStages) { s = 0; sph ^= 1; }
+          }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+      int s = 0, sph = 0, tl = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
+        const int a = tl & 1;
+        if (!mbar_wait(&acc_empty[a], ((tl >> 1) & 1) ^ 1, err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        bool ok = true;
+        for (int ks = 0; ks < 2 * nkb; ++ks) {
+          if (!mbar_wait(&tok_full[s], sph, err, abort_flag) || !mbar_wait(&a_full[s], sph, err, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * kAStageBytes));
+          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + s * L::kBStageBytes));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0 ? 1u : 0u);
+          tc_commit(&st_empty[s]);
+          if (++s == kStages) { s = 0; sph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[a]);
+      }
+    }
+  } else if (warp < 4) {
+    // --------------------------------------------------------------- unpack
+    const int t = threadIdx.x;  // weight row of the tile
+    uint8_t* const arow_base = sA + (t >> 3) * 1024 + (t & 7) * 128;
+    const int sw = t & 7;
+    int s = 0, sph = 0, p = 0, pph = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
+        const uint4* src = reinterpret_cast<const uint4*>(sP + p * kPkSlotBytes + t * 32);
+        const uint4 lo4 = src[0];
+        const uint4 hi4 = src[1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pk_empty[p]);
+        if (++p == kPkSlots) { p = 0; pph ^= 1; }
+        const uint32_t wd[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto unpack_done;
+          uint8_t* arow = arow_base + s * kAStageBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int sl = 2 * hf + (c >> 2);   // slot of the block: elements 32*sl + j
+            const int jw = 2 * (c & 3);         // words jw, jw+1 = bytes j = 8*(c&3) .. +7
+            const int sh = 6 - 2 * sl;
+            const uint32_t v0 = (wd[jw] >> sh) & 0x03030303u;
+            const uint32_t v1 = (wd[jw + 1] >> sh) & 0x03030303u;
+            uint4 out;
+            codes_to_h2(v0, out.x, out.y);
+            codes_to_h2(v1, out.z, out.w);
+            *reinterpret_cast<uint4*>(arow + ((c ^ sw) << 4)) = out;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[s]);
+          if (++s == kStages) { s = 0; sph ^= 1; }
+        }
+      }
+    }
+  unpack_done:;
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    float* inv = sInv + (warp - 4) * BN;
+    int tl = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
+      const int a = tl & 1;
+      const int n0 = (tile % n_wt) * kBM;
+      const int m0 = (tile / n_wt) * BN;
+      __syncwarp();
+      for (int j = lane; j < BN; j += 32) {
+        const int m = m0 + j;
+        inv[j] = m < M ? __fdiv_rn(1.0f, __ldg(a_scale + m)) : 0.0f;
+      }
+      __syncwarp();
+      if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
+      tc_fence_after();
+      const int n = n0 + q * 32 + lane;
+      const bool n_ok = n < N;
+#pragma unroll 1
+      for (int j0 = 0; j0 < BN; j0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN + j0),
+                           r);
+        tmem_ld_wait();
+        const int mlim = M - (m0 + j0);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          if (jj < mlim && n_ok) {
+            const int64_t off = static_cast<int64_t>(m0 + j0 + jj) * N + n;
+            const float accf = __uint_as_float(r[jj]);
+            y[off] = rescale_elem(accf, inv[j0 + jj], inv_w);
+            if (acc_out) acc_out[off] = __float2int_rn(accf);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+template <int BN>
+cudaError_t launch_bn(const DeviceContext* ctx, const CUtensorMap& tm_tok, const CUtensorMap& tm_w,
+                      const float* a_scale, float inv_w, int M, int N, int K, float* y, int32_t* acc_out, bool pdl,
+                      cudaStream_t s) {
+  using L = TcLayout<BN>;
+  auto kern = k_gemm_tc<BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int grid = tiles < ctx->num_sms ? tiles : ctx->num_sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, inv_w, M, N, K, y, acc_out, ctx->err_word);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
+                           const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
+                           int32_t* acc_out, bool pdl, cudaStream_t s, int* status) {
+  *status = BITNET_OK;
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (!encode) {
+    *status = BITNET_ERR_CUDA;
+    return cudaErrorNotSupported;
+  }
+  const int BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  CUtensorMap tm_tok, tm_w;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(BN)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_tok, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(codes_f16), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
+    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kBM)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed_w), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  const float inv_w = 1.0f / w_scale;  // IEEE division, as in the oracle
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  switch (BN) {
+    case 64: return launch_bn<64>(ctx, tm_tok, tm_w, a_scale, inv_w, m, n, k, y, acc_out, pdl, s);
+    case 128: return launch_bn<128>(ctx, tm_tok, tm_w, a_scale, inv_w, m, n, k, y, acc_out, pdl, s);
+    default: return launch_bn<256>(ctx, tm_tok, tm_w, a_scale, inv_w, m, n, k, y, acc_out, pdl, s);
+  }
+}
+
+}  // namespace bitnet

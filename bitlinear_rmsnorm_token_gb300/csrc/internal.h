@@ -1,0 +1,78 @@
+// internal.h -- host-side interfaces between the translation units of the
+// library (launchers, per-device context).  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bitnet.h"
+
+namespace bitnet {
+
+struct DeviceContext {
+  int device = -1;
+  int num_sms = 0;
+  unsigned* err_word = nullptr;  // device address of this device's error word
+  cudaMemPool_t pool = nullptr;  // stream-ordered pool for temporary buffers
+};
+
+// Returns BITNET_OK and fills *ctx for the current device (lazily initialised,
+// thread safe), or BITNET_ERR_NO_DEVICE / BITNET_ERR_CUDA.
+int device_context(DeviceContext** ctx);
+
+// Temporary device memory ordered on `stream` (freed with pool_free on the
+// same stream after its last use has been enqueued).
+int pool_alloc(DeviceContext* ctx, void** p, size_t bytes, cudaStream_t stream);
+void pool_free(void* p, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled fetched through the runtime (no link to libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// ---------------------------------------------------------------- launchers
+// All launchers return cudaError_t of the launch (cudaSuccess when fine).
+
+// I2_S packing: absmean (two deterministic reduction launches) + pack.
+cudaError_t launch_pack_i2s(const DeviceContext* ctx, const float* w, int64_t N, int64_t K, uint8_t* packed,
+                            double* partials, int num_partials, cudaStream_t s);
+int pack_num_partials(int64_t count);
+cudaError_t launch_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_t* out, cudaStream_t s);
+
+// RMSNorm + absmax int8 quantisation, one warp per row.  Exactly one of
+// codes_i8 / codes_f16 is non-null.
+cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int K, float eps, int8_t* codes_i8,
+                                 __half* codes_f16, float* a_scale, int32_t* rowsum, float* xn_out,
+                                 bool pdl, cudaStream_t s);
+
+// int8 codes -> fp16 codes (for the tensor-core path of the int8 API).
+cudaError_t launch_codes_to_f16(const int8_t* codes, __half* out, int64_t count, cudaStream_t s);
+
+// Decode (small M) weight-streaming kernels.
+constexpr int kDecodeMaxM = 8;
+constexpr int64_t kDecodeMaxCodeBytes = 65536;  // M * K bytes of codes held in shared memory
+
+struct DecodeJob {
+  const float* x;          // fused: activations [M, K]
+  const float* g;          // fused: norm weight [K]
+  const int8_t* codes;     // unfused: int8 codes [M, K]
+  const float* a_scale;    // unfused: activation scales [M]
+  const uint8_t* w;        // I2_S codes [N, K/4]
+  float w_scale;
+  int K;
+  int N;
+  float* y;                // [M, N]
+  int32_t* acc_out;        // [M, N] or null
+};
+bool decode_supported(int64_t M, int64_t K);
+cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
+                          bool weights_static, cudaStream_t s);
+
+// Tensor-core (tcgen05) contraction on fp16 codes.
+cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
+                           const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
+                           int32_t* acc_out, bool pdl, cudaStream_t s, int* status);
+
+}  // namespace bitnet

@@ -63,6 +63,12 @@
 extern "C" {
 #endif
 
+#if defined(__GNUC__)
+#define BITNET_API __attribute__((visibility("default")))
+#else
+#define BITNET_API
+#endif
+
 #define BITNET_I2S_BLOCK 128       /* values per I2_S block                         */
 #define BITNET_I2S_BLOCK_BYTES 32  /* bytes per I2_S block                          */
 #define BITNET_GGML_TYPE_I2_S 36   /* GGML type id ("gguf-py: I2_S Type", first page) */
@@ -89,7 +95,7 @@ typedef struct CUstream_st* bitnet_stream_t; /* == cudaStream_t */
 
 /* Bytes of an I2_S buffer for an [N, K] matrix: N*K/4 code bytes plus the 4-byte
  * scale.  Returns 0 for an invalid shape (N < 1, K not a positive multiple of 128). */
-size_t bitnet_i2s_packed_bytes(int64_t N, int64_t K);
+BITNET_API size_t bitnet_i2s_packed_bytes(int64_t N, int64_t K);
 
 /* Absmean ternary quantisation and I2_S packing of w[N, K] (fp32) into
  * packed[bitnet_i2s_packed_bytes(N, K)] ("I2_S Ternary Packing", first page
@@ -98,12 +104,12 @@ size_t bitnet_i2s_packed_bytes(int64_t N, int64_t K);
  * pointer) is non-NULL the call synchronises `stream` and stores it there too.
  * mean(|w|) is reduced in double in a fixed order, so repeated calls give
  * identical bytes.  packed must be 16-byte aligned. */
-int bitnet_pack_i2s(const float* w, int64_t N, int64_t K, uint8_t* packed,
+BITNET_API int bitnet_pack_i2s(const float* w, int64_t N, int64_t K, uint8_t* packed,
                     float* w_scale_out, bitnet_stream_t stream);
 
 /* Decode an I2_S buffer into ternary int8 values w_ternary[N, K] = code - 1.
  * A (malformed) code 3 decodes to +2, the same value every kernel here uses. */
-int bitnet_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_t* w_ternary,
+BITNET_API int bitnet_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_t* w_ternary,
                       bitnet_stream_t stream);
 
 /* RMSNorm with the projection's norm weight followed by per-token absmax int8
@@ -113,7 +119,7 @@ int bitnet_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_t* w_ter
  *   a_rowsum[M] int32 (sum of the row's codes; may be NULL),
  *   xn_out[M, K] fp32 (the normalised row before quantisation; may be NULL).
  * eps > 0 (the pages' models use 1e-6). */
-int bitnet_rmsnorm_quant_a8(const float* x, const float* norm_w, int64_t M, int64_t K,
+BITNET_API int bitnet_rmsnorm_quant_a8(const float* x, const float* norm_w, int64_t M, int64_t K,
                             float eps, int8_t* a_codes, float* a_scale, int32_t* a_rowsum,
                             float* xn_out, bitnet_stream_t stream);
 
@@ -126,7 +132,7 @@ int bitnet_rmsnorm_quant_a8(const float* x, const float* norm_w, int64_t M, int6
  * scale is ignored: w_scale is the argument), y[M, N] fp32; acc_out[M, N] int32
  * receives acc when non-NULL.  M <= 8 runs a dp4a weight-streaming kernel,
  * larger M the tcgen05 tensor-core kernel (pool memory: 2*M*K bytes). */
-int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* packed_w,
+BITNET_API int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* packed_w,
                     float w_scale, int64_t M, int64_t K, int64_t N, float* y,
                     int32_t* acc_out, bitnet_stream_t stream);
 
@@ -135,7 +141,7 @@ int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* 
  * composition of bitnet_rmsnorm_quant_a8 and bitnet_i2s_gemm.  Small M runs
  * one fused launch; larger M a norm/quant launch (pool memory: 2*M*K + 4*M
  * bytes) followed by the tensor-core launch. */
-int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w,
+BITNET_API int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w,
                              float w_scale, int64_t M, int64_t K, int64_t N, float eps,
                              float* y, bitnet_stream_t stream);
 
@@ -157,17 +163,17 @@ typedef struct {
  * (1..BITNET_MAX_GROUP), read before the call returns.  Supported for
  * M <= 8 and K <= 16384; other shapes return BITNET_ERR_UNSUPPORTED_SHAPE.
  * flags: 0 or BITNET_FLAG_WEIGHTS_STATIC. */
-int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M,
+BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M,
                                    float eps, uint32_t flags, bitnet_stream_t stream);
 
 /* Static description of a status code (never NULL). */
-const char* bitnet_status_string(int status);
+BITNET_API const char* bitnet_status_string(int status);
 
 /* Synchronises `stream`, then returns BITNET_ERR_TIMEOUT if a kernel of this
  * library on the current device gave up a bounded wait since the last call
  * (and clears that record), BITNET_ERR_CUDA if the synchronisation failed, and
  * BITNET_OK otherwise. */
-int bitnet_last_device_status(bitnet_stream_t stream);
+BITNET_API int bitnet_last_device_status(bitnet_stream_t stream);
 
 #ifdef __cplusplus
 }
