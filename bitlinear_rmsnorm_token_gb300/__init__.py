@@ -17,7 +17,7 @@ from . import build_lib
 __all__ = [
     "BitnetError", "lib", "packed_bytes", "pack_i2s", "unpack_i2s", "rmsnorm_quant_a8", "i2s_gemm",
     "bitlinear_forward", "bitlinear_forward_group", "last_device_status", "status_string",
-    "FLAG_WEIGHTS_STATIC", "MAX_GROUP", "EXPORTED_FUNCTIONS",
+    "FLAG_WEIGHTS_STATIC", "MAX_GROUP", "EXPORTED_FUNCTIONS", "bitlinear_forward_noalloc",
 ]
 
 OK = 0
@@ -27,13 +27,15 @@ ERR_MISALIGNED = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
 ERR_NO_DEVICE = 6
+ERR_SCRATCH_LIMIT = 7
+NOALLOC_SCRATCH_BYTES = 16 << 20
 FLAG_WEIGHTS_STATIC = 1
 MAX_GROUP = 16
 
 EXPORTED_FUNCTIONS = (
     "bitnet_i2s_packed_bytes", "bitnet_pack_i2s", "bitnet_unpack_i2s", "bitnet_rmsnorm_quant_a8",
     "bitnet_i2s_gemm", "bitnet_bitlinear_forward", "bitnet_bitlinear_forward_group",
-    "bitnet_status_string", "bitnet_last_device_status",
+    "bitnet_status_string", "bitnet_last_device_status", "bitnet_bitlinear_forward_noalloc",
 )
 
 
@@ -78,6 +80,8 @@ def lib(build: bool = False) -> ctypes.CDLL:
     L.bitnet_bitlinear_forward.argtypes = [vp, vp, vp, f32, i64, i64, i64, f32, vp, vp]
     L.bitnet_bitlinear_forward_group.restype = ctypes.c_int
     L.bitnet_bitlinear_forward_group.argtypes = [ctypes.POINTER(Projection), i32, i64, f32, ctypes.c_uint32, vp]
+    L.bitnet_bitlinear_forward_noalloc.restype = ctypes.c_int
+    L.bitnet_bitlinear_forward_noalloc.argtypes = [vp, vp, vp, f32, i64, i64, i64, f32, vp, vp]
     L.bitnet_status_string.restype = ctypes.c_char_p
     L.bitnet_status_string.argtypes = [ctypes.c_int]
     L.bitnet_last_device_status.restype = ctypes.c_int
@@ -198,6 +202,24 @@ def bitlinear_forward(x, norm_w, packed_w, w_scale: float, N: int, eps: float = 
         _dev(packed_w, torch.uint8, "packed_w"), float(w_scale), M, K, N, float(eps),
         _dev(y, torch.float32, "y"), _stream(stream))
     _check(rc, "bitnet_bitlinear_forward")
+    return y
+
+
+def bitlinear_forward_noalloc(x, norm_w, packed_w, w_scale: float, N: int, eps: float = 1e-6, y=None,
+                              stream=None):
+    """bitlinear_forward without any allocation inside the library (the
+    temporary data lives in a fixed 16 MiB device array; see bitnet.h).  `y`
+    must be supplied by callers that cannot allocate."""
+    import torch
+
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    rc = lib().bitnet_bitlinear_forward_noalloc(
+        _dev(x, torch.float32, "x"), _dev(norm_w, torch.float32, "norm_w"),
+        _dev(packed_w, torch.uint8, "packed_w"), float(w_scale), M, K, N, float(eps),
+        _dev(y, torch.float32, "y"), _stream(stream))
+    _check(rc, "bitnet_bitlinear_forward_noalloc")
     return y
 
 

@@ -64,6 +64,35 @@ int device_context(DeviceContext** out) {
   return BITNET_OK;
 }
 
+namespace {
+DeviceContext g_ctx_np[kMaxDevices];
+bool g_ready_np[kMaxDevices];
+}  // namespace
+
+int device_context_nopool(DeviceContext** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return BITNET_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ready_np[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return BITNET_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return BITNET_ERR_NO_DEVICE;
+    DeviceContext c;
+    c.device = dev;
+    c.num_sms = prop.multiProcessorCount;
+    void* ew = nullptr;
+    if (cudaGetSymbolAddress(&ew, g_error_word) != cudaSuccess) return BITNET_ERR_CUDA;
+    c.err_word = static_cast<unsigned*>(ew);
+    g_ctx_np[dev] = c;
+    g_ready_np[dev] = true;
+  }
+  *out = &g_ctx_np[dev];
+  return BITNET_OK;
+}
+
 int pool_alloc(DeviceContext* ctx, void** p, size_t bytes, cudaStream_t stream) {
   if (cudaMallocFromPoolAsync(p, bytes, ctx->pool, stream) != cudaSuccess) {
     cudaGetLastError();
@@ -109,6 +138,8 @@ const char* bitnet_status_string(int status) {
     case BITNET_ERR_CUDA: return "CUDA error";
     case BITNET_ERR_TIMEOUT: return "device-side wait timed out";
     case BITNET_ERR_NO_DEVICE: return "no sm_103 CUDA device";
+    case BITNET_ERR_SCRATCH_LIMIT:
+      return "problem needs more than the 16 MiB no-alloc scratch (2*M*K + 4*M bytes); use bitnet_bitlinear_forward";
     default: return "unknown status";
   }
 }

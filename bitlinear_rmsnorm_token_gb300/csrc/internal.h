@@ -21,6 +21,10 @@ struct DeviceContext {
 // thread safe), or BITNET_ERR_NO_DEVICE / BITNET_ERR_CUDA.
 int device_context(DeviceContext** ctx);
 
+// Same as device_context but never creates the memory pool (ctx->pool stays
+// null): for entry points that must not allocate.
+int device_context_nopool(DeviceContext** ctx);
+
 // Temporary device memory ordered on `stream` (freed with pool_free on the
 // same stream after its last use has been enqueued).
 int pool_alloc(DeviceContext* ctx, void** p, size_t bytes, cudaStream_t stream);

@@ -1,0 +1,104 @@
+// noalloc.cu -- bitnet_bitlinear_forward_noalloc: the whole projection without
+// any device-memory allocation by the library.
+//
+// Who needs it: callers that may not allocate device memory once they are
+// running -- for example a serving process that reserved all of HBM for its own
+// caching allocator at start-up (so a cudaMalloc from a library would fail or
+// fragment), or a latency-critical loop where an allocation's cost or possible
+// failure is not acceptable.  They still pass their own inputs and outputs.
+//
+// How: the prefill path needs temporary space for the fp16 activation codes and
+// the per-token scales.  Here that space is one file-scope device array of
+// fixed size, loaded with the library (every GPU the library is used on keeps
+// it until the process exits).  Its device address is looked up once per device
+// with cudaGetSymbolAddress -- the array's name in host code is only a host-side
+// stand-in and must never be handed to a kernel.  Small token counts take the
+// decode path, which needs no temporary space at all.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace bitnet {
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[BITNET_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDev = 64;
+std::mutex g_np_mu;
+void* g_np_scratch[kMaxDev];
+bool g_np_ready[kMaxDev];
+
+// Device address of this device's copy of the scratch array (looked up once
+// per device, with that device current).
+int scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return BITNET_ERR_NO_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_np_mu);
+  if (!g_np_ready[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return BITNET_ERR_CUDA;
+    }
+    g_np_scratch[dev] = p;
+    g_np_ready[dev] = true;
+  }
+  *out = g_np_scratch[dev];
+  return BITNET_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace bitnet
+
+using namespace bitnet;
+
+extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* norm_w, const uint8_t* packed_w,
+                                                float w_scale, int64_t M, int64_t K, int64_t N, float eps,
+                                                float* y, bitnet_stream_t stream) {
+  if (!x || !norm_w || !packed_w || !y) return BITNET_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !(w_scale > 0.0f) || w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
+  if (M < 1 || N < 1) return BITNET_ERR_INVALID_ARG;
+  if (K < BITNET_I2S_BLOCK || K % BITNET_I2S_BLOCK != 0 || K > BITNET_MAX_K) return BITNET_ERR_UNSUPPORTED_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1) return BITNET_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y)) return BITNET_ERR_MISALIGNED;
+  const bool small = decode_supported(M, K);
+  // scratch layout: fp16 codes [M, K], then fp32 scales [M] (256-byte aligned)
+  const size_t code_bytes = (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) & ~size_t(255);
+  if (!small && code_bytes + static_cast<size_t>(M) * 4 > static_cast<size_t>(BITNET_NOALLOC_SCRATCH_BYTES))
+    return BITNET_ERR_SCRATCH_LIMIT;
+
+  DeviceContext* ctx;
+  int rc = device_context_nopool(&ctx);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (small) {
+    DecodeJob j = {};
+    j.x = x;
+    j.g = norm_w;
+    j.w = packed_w;
+    j.w_scale = w_scale;
+    j.K = static_cast<int>(K);
+    j.N = static_cast<int>(N);
+    j.y = y;
+    return launch_decode(ctx, &j, 1, static_cast<int>(M), eps, true, false, s) == cudaSuccess ? BITNET_OK
+                                                                                          : BITNET_ERR_CUDA;
+  }
+  void* scratch = nullptr;
+  if ((rc = scratch_for_current_device(&scratch))) return rc;
+  __half* f16 = static_cast<__half*>(scratch);
+  float* as = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + code_bytes);
+  // every element of the used scratch region is written by the norm launch
+  // before the contraction reads it, so nothing has to be cleared first
+  cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr,
+                                       false, s);
+  int st = BITNET_OK;
+  if (e == cudaSuccess) e = launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, true, s, &st);
+  if (st != BITNET_OK) return st;
+  return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
+}

@@ -88,7 +88,8 @@ typedef enum {
   BITNET_ERR_MISALIGNED = 3,        /* a pointer that must be 16-byte aligned is not       */
   BITNET_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed                */
   BITNET_ERR_TIMEOUT = 5,           /* a device-side bounded wait expired (see last_device_status) */
-  BITNET_ERR_NO_DEVICE = 6          /* no CUDA device, or it is not sm_103                 */
+  BITNET_ERR_NO_DEVICE = 6,         /* no CUDA device, or it is not sm_103                 */
+  BITNET_ERR_SCRATCH_LIMIT = 7      /* too large for bitnet_bitlinear_forward_noalloc      */
 } bitnet_status;
 
 typedef struct CUstream_st* bitnet_stream_t; /* == cudaStream_t */
@@ -165,6 +166,31 @@ typedef struct {
  * flags: 0 or BITNET_FLAG_WEIGHTS_STATIC. */
 BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M,
                                    float eps, uint32_t flags, bitnet_stream_t stream);
+
+/* Size of the fixed device array bitnet_bitlinear_forward_noalloc works in. */
+#define BITNET_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB per GPU */
+
+/* bitnet_bitlinear_forward without any device-memory allocation.  The pages have
+ * no counterpart: this exists for callers that may not allocate once running --
+ * e.g. a server that reserved all device memory for its own allocator at start-up,
+ * or a latency-critical loop where an allocation's cost or failure is not
+ * acceptable.  Same arguments and the same y as bitnet_bitlinear_forward.
+ *   - Temporary data (fp16 activation codes and per-token scales, 2*M*K + 4*M
+ *     bytes, rounded up) lives in one fixed 16 MiB device array that every GPU
+ *     using the library keeps until the process exits.  Larger problems return
+ *     BITNET_ERR_SCRATCH_LIMIT without launching anything; token counts small
+ *     enough for the decode path (M <= 8 and M*K <= 65536) need no scratch.
+ *   - The first call on each device does one-time set-up (device properties and
+ *     the array's device address); make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the one array, and it keeps whatever the last
+ *     call left (every byte a call reads it first writes).  Calls whose work can
+ *     overlap on the GPU -- different streams without ordering between them, or
+ *     several host threads -- race on it and must be serialised by the caller. */
+BITNET_API int bitnet_bitlinear_forward_noalloc(const float* x, const float* norm_w,
+                                                const uint8_t* packed_w, float w_scale, int64_t M,
+                                                int64_t K, int64_t N, float eps, float* y,
+                                                bitnet_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 BITNET_API const char* bitnet_status_string(int status);
