@@ -236,7 +236,7 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
   DeviceContext* ctx;
   if ((rc = device_context(&ctx))) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (decode_supported(M, K)) {
+  if (decode_fused_supported(M, K)) {
     DecodeJob j = {};
     j.x = x;
     j.g = norm_w;
@@ -246,6 +246,30 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
     j.N = static_cast<int>(N);
     j.y = y;
     return cuda_status(launch_decode(ctx, &j, 1, static_cast<int>(M), eps, true, false, s));
+  }
+  if (decode_supported(M, K)) {
+    // few tokens but long rows: int8 codes through the pool, then the decode kernel
+    const size_t code_bytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
+    uint8_t* ws = nullptr;
+    if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + static_cast<size_t>(M) * 4, s)))
+      return rc;
+    int8_t* codes = reinterpret_cast<int8_t*>(ws);
+    float* as = reinterpret_cast<float*>(ws + code_bytes);
+    cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, codes, nullptr, as, nullptr,
+                                         nullptr, false, s);
+    if (e == cudaSuccess) {
+      DecodeJob j = {};
+      j.codes = codes;
+      j.a_scale = as;
+      j.w = packed_w;
+      j.w_scale = w_scale;
+      j.K = static_cast<int>(K);
+      j.N = static_cast<int>(N);
+      j.y = y;
+      e = launch_decode(ctx, &j, 1, static_cast<int>(M), eps, false, false, s);
+    }
+    pool_free(ws, s);
+    return cuda_status(e);
   }
   // norm + quant to fp16 codes, then the tensor-core contraction
   const size_t code_bytes = (static_cast<size_t>(M * K) * 2 + 255) & ~size_t(255);
@@ -276,7 +300,7 @@ int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count
     if (rc) return rc;
     if (!aligned16(p.x) || !aligned16(p.norm_w) || !aligned16(p.packed_w) || !aligned16(p.y))
       return BITNET_ERR_MISALIGNED;
-    if (!decode_supported(M, p.K)) return BITNET_ERR_UNSUPPORTED_SHAPE;
+    if (!decode_fused_supported(M, p.K)) return BITNET_ERR_UNSUPPORTED_SHAPE;
     DecodeJob j = {};
     j.x = p.x;
     j.g = p.norm_w;

@@ -31,10 +31,10 @@
 namespace bitnet {
 namespace {
 
-constexpr int kDecWarps = 8;                       // compute warps
+constexpr int kDecWarps = 16;                      // compute warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
-constexpr int kDecStageBytes = 16384;
-constexpr int kDecStages = 6;
+constexpr int kDecStageBytes = 24576;
+constexpr int kDecStages = 3;
 
 struct DecodeProj {
   const float* x;
@@ -62,6 +62,9 @@ struct DecodeParams {
 struct DecodeSmemTail {
   uint64_t full[kDecStages];
   uint64_t empty[kDecStages];
+  uint64_t in_full;  // activations (and norm weight) staged
+  unsigned ss_part[kDecWarps][kDecodeMaxM][6];  // per-warp limb sums (each < 2^29)
+  int emax_part[kDecWarps][kDecodeMaxM];
   float rstd[kDecodeMaxM];
   float amax_part[kDecWarps][kDecodeMaxM];
   int rs_part[kDecWarps][kDecodeMaxM];
@@ -70,6 +73,34 @@ struct DecodeSmemTail {
   int abort_flag;
 };
 
+// Shared-memory carve-up for one CTA: weight ring | x fp32 [M,K] (fused) or
+// the incoming int8 codes [M,K] (unfused) | g fp32 [K] (fused) | codes int8
+// [M,K] in slot-major order | tail.
+//
+// Slot-major codes: the 16-byte chunk c of a weight row (block c/2, bytes
+// 16(c&1)..+15) pairs, for slot s, with activation elements
+// 128(c/2) + 32s + 16(c&1) + 0..15.  They are stored at ((s*cpr + c) * 16),
+// cpr = K/64 chunks per row, so lanes reading consecutive chunks of one slot
+// read consecutive 16-byte words (no bank conflicts).
+struct DecodeLayout {
+  int xs, gs, xq, tail, total;
+  __host__ __device__ DecodeLayout(int M, int K, bool fused) {
+    xs = kDecStages * kDecStageBytes;
+    gs = xs + (fused ? M * K * 4 : ((M * K + 127) & ~127));
+    xq = gs + (fused ? K * 4 : 0);
+    tail = xq + ((M * K + 127) & ~127);
+    total = tail + static_cast<int>(sizeof(DecodeSmemTail));
+  }
+};
+
+// Offset of activation element k (k % 4 == 0: the 4 elements k..k+3 stay
+// together) in the slot-major layout.
+__device__ __forceinline__ int slot_major(int k, int cpr) {
+  const int b = k >> 7, e = k & 127;
+  const int sl = e >> 5, j = e & 31;
+  return ((sl * cpr + 2 * b + (j >> 4)) << 4) + (j & 15);
+}
+
 __device__ __forceinline__ void compute_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
 }
@@ -77,8 +108,6 @@ __device__ __forceinline__ void compute_bar() {
 template <int MT, bool kFused>
 __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ DecodeParams P, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* ring = smem;
-  int8_t* xq = reinterpret_cast<int8_t*>(smem + kDecStages * kDecStageBytes);
 
   // which projection this CTA serves
   int pi = 0;
@@ -88,14 +117,27 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   const DecodeProj& pr = P.p[pi];
   const int K = pr.K;
   const int N = pr.N;
+  const int M = P.M;
   const int row_bytes = K >> 2;
   const int r0 = (static_cast<int>(blockIdx.x) - pr.cta_begin) * pr.rows_per_cta;
   const int r1 = min(N, r0 + pr.rows_per_cta);
-  const int rps = kDecStageBytes / row_bytes;  // rows per stage (K <= 65536 keeps it >= 1)
+  // lpr lanes share a weight row (each taking cpr/lpr of its 16-byte chunks);
+  // start at 4 and widen while the CTA has fewer rows than one pass of all
+  // warps, so every warp gets work.  A stage holds a whole number of passes.
+  const int cpr = K >> 6;
+  int lpr = (cpr & 3) ? 2 : 4;
+  while (lpr < 32 && cpr % (2 * lpr) == 0 && (r1 - r0) < kDecWarps * (32 / lpr)) lpr *= 2;
+  const int rpp = 32 / lpr;  // rows per warp pass
+  int rps = kDecStageBytes / row_bytes;  // rows per stage (K <= 65536 keeps it >= 1)
+  if (rps >= kDecWarps * rpp) rps -= rps % (kDecWarps * rpp);
   const int nst = (r1 - r0 + rps - 1) / rps;
 
-  DecodeSmemTail* tail =
-      reinterpret_cast<DecodeSmemTail*>(smem + kDecStages * kDecStageBytes + ((MT * K + 127) & ~127));
+  const DecodeLayout lay(M, K, kFused);
+  uint8_t* ring = smem;
+  float* xs = reinterpret_cast<float*>(smem + lay.xs);
+  float* gs = reinterpret_cast<float*>(smem + lay.gs);
+  int8_t* xq = reinterpret_cast<int8_t*>(smem + lay.xq);
+  DecodeSmemTail* tail = reinterpret_cast<DecodeSmemTail*>(smem + lay.tail);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -104,6 +146,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
       mbar_init(&tail->full[s], 1);
       mbar_init(&tail->empty[s], kDecWarps);
     }
+    mbar_init(&tail->in_full, 1);
     tail->abort_flag = 0;
     fence_barrier_init();
   }
@@ -113,22 +156,41 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   if (warp == kDecWarps) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      if (!P.weights_static) pdl_wait();
       const uint8_t* src = pr.w + static_cast<int64_t>(r0) * row_bytes;
-      int issued = 0;
-      for (int st = 0; st < nst; ++st) {
+      const unsigned in_bytes = kFused ? static_cast<unsigned>((M + 1) * K * 4) : static_cast<unsigned>(M * K);
+      mbar_arrive_expect_tx(&tail->in_full, in_bytes);
+      const int first = min(nst, kDecStages);
+      auto issue = [&](int st) {
         const int s = st % kDecStages;
-        if (st >= kDecStages &&
-            !mbar_wait(&tail->empty[s], ((st / kDecStages) - 1) & 1, err, &tail->abort_flag))
-          break;
         const int rows = min(rps, r1 - r0 - st * rps);
         const unsigned bytes = static_cast<unsigned>(rows * row_bytes);
         mbar_arrive_expect_tx(&tail->full[s], bytes);
         bulk_load(ring + s * kDecStageBytes, src + static_cast<int64_t>(st) * rps * row_bytes, bytes,
                   &tail->full[s]);
+      };
+      // parameters (packed weights, norm weight) may be requested before the
+      // previous kernel has finished when the caller declared them static
+      if (P.weights_static) {
+        if (kFused) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
+        for (int st = 0; st < first; ++st) issue(st);
+      }
+      pdl_wait();
+      if (!P.weights_static) {
+        if (kFused) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
+        for (int st = 0; st < first; ++st) issue(st);
+      }
+      if (kFused)
+        bulk_load(xs, pr.x, static_cast<unsigned>(M * K * 4), &tail->in_full);
+      else
+        bulk_load(xs, pr.codes, static_cast<unsigned>(M * K), &tail->in_full);
+      int issued = first;
+      for (int st = first; st < nst; ++st) {
+        if (!mbar_wait(&tail->empty[st % kDecStages], ((st / kDecStages) - 1) & 1, err, &tail->abort_flag)) break;
+        issue(st);
         issued = st + 1;
       }
       // leave no copy in flight when the CTA retires
+      mbar_wait(&tail->in_full, 0, err, nullptr);
       for (int st = max(0, issued - kDecStages); st < issued; ++st)
         mbar_wait(&tail->full[st % kDecStages], (st / kDecStages) & 1, err, nullptr);
     }
@@ -136,35 +198,72 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   }
 
   // ------------------------------------------------------------ compute warps
-  pdl_wait();
   const int tid = threadIdx.x;  // 0 .. kDecWarps*32-1
-  const int M = P.M;
+  constexpr int kThr = kDecWarps * 32;
+  if (!mbar_wait(&tail->in_full, 0, err, &tail->abort_flag)) return;
   if (kFused) {
-    // sum of squares: one warp per token row (the shared canonical reduction)
-    if (warp < M) {
-      const double ss = warp_row_sumsq(pr.x + static_cast<int64_t>(warp) * K, K, lane);
-      if (lane == 0) tail->rstd[warp] = rstd_from_sumsq(ss, K, P.eps);
-    }
-    compute_bar();
-    // absmax of the normalised rows
+    // exact sum of squares, all warps: largest exponent first, then the
+    // fixed-point sum (order-free, so it equals the norm kernel's bit for bit)
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m < M) {
-        const float* xr = pr.x + static_cast<int64_t>(m) * K;
+        int e = 0;
+        for (int k = 4 * tid; k < K; k += 4 * kThr) e = max(e, sq_exp4(*reinterpret_cast<const float4*>(xs + m * K + k)));
+        e = warp_max_int(e);
+        if (lane == 0) tail->emax_part[warp][m] = e;
+      }
+    }
+    compute_bar();
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m < M) {
+        int emax = 0;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) emax = max(emax, tail->emax_part[w][m]);
+        U128 acc{0ull, 0ull};
+        for (int k = 4 * tid; k < K; k += 4 * kThr) sq_add4(acc, *reinterpret_cast<const float4*>(xs + m * K + k), emax);
+        const LimbSums ls = warp_limb_sums(acc);
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < 6; ++i) tail->ss_part[warp][m][i] = static_cast<unsigned>(ls.l[i]);
+        }
+      }
+    }
+    compute_bar();
+    if (tid < M) {
+      int emax = 0;
+      LimbSums acc;
+#pragma unroll
+      for (int i = 0; i < 6; ++i) acc.l[i] = 0ull;
+      for (int w = 0; w < kDecWarps; ++w) {
+        emax = max(emax, tail->emax_part[w][tid]);
+#pragma unroll
+        for (int i = 0; i < 6; ++i) acc.l[i] += tail->ss_part[w][tid][i];
+      }
+      tail->rstd[tid] = rstd_from_sumsq(sq_to_df(limb_sums_to_u128(acc), emax), K, P.eps);
+    }
+    compute_bar();
+    // normalise in place and take the absmax
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      if (m < M) {
+        float* xr = xs + m * K;
         const float rstd = tail->rstd[m];
         float amax = 0.0f;
-        for (int k = 4 * tid; k < K; k += 4 * kDecWarps * 32) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
-          const float4 gv = __ldg(reinterpret_cast<const float4*>(pr.g + k));
-          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(norm_elem(v.x, rstd, gv.x)), fabsf(norm_elem(v.y, rstd, gv.y))),
-                                   fmaxf(fabsf(norm_elem(v.z, rstd, gv.z)), fabsf(norm_elem(v.w, rstd, gv.w)))));
+        for (int k = 4 * tid; k < K; k += 4 * kThr) {
+          const float4 v = *reinterpret_cast<const float4*>(xr + k);
+          const float4 gv = *reinterpret_cast<const float4*>(gs + k);
+          const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
+                                       norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
+          *reinterpret_cast<float4*>(xr + k) = n;
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(n.x), fabsf(n.y)), fmaxf(fabsf(n.z), fabsf(n.w))));
         }
         amax = warp_max(amax);
         if (lane == 0) tail->amax_part[warp][m] = amax;
       }
     }
     compute_bar();
-    // quantise into shared memory
+    // quantise into the slot-major code layout
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m < M) {
@@ -172,18 +271,14 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
 #pragma unroll
         for (int w = 0; w < kDecWarps; ++w) amax = fmaxf(amax, tail->amax_part[w][m]);
         const float as = act_scale_from_amax(amax);
-        const float* xr = pr.x + static_cast<int64_t>(m) * K;
-        const float rstd = tail->rstd[m];
+        const float* xr = xs + m * K;
         int rs = 0;
-        for (int k = 4 * tid; k < K; k += 4 * kDecWarps * 32) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
-          const float4 gv = __ldg(reinterpret_cast<const float4*>(pr.g + k));
-          const int q0 = quant_elem(norm_elem(v.x, rstd, gv.x), as);
-          const int q1 = quant_elem(norm_elem(v.y, rstd, gv.y), as);
-          const int q2 = quant_elem(norm_elem(v.z, rstd, gv.z), as);
-          const int q3 = quant_elem(norm_elem(v.w, rstd, gv.w), as);
+        for (int k = 4 * tid; k < K; k += 4 * kThr) {
+          const float4 n = *reinterpret_cast<const float4*>(xr + k);
+          const int q0 = quant_elem(n.x, as), q1 = quant_elem(n.y, as);
+          const int q2 = quant_elem(n.z, as), q3 = quant_elem(n.w, as);
           rs += q0 + q1 + q2 + q3;
-          *reinterpret_cast<uint32_t*>(xq + m * K + k) =
+          *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) =
               (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
               ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
         }
@@ -193,18 +288,23 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
       }
     }
   } else {
-    // codes computed elsewhere: copy them in and sum them
+    // codes computed elsewhere (staged in natural order): reorder to slot-major,
+    // sum them, fetch the scales
+    pdl_wait();
+    const int8_t* stg = reinterpret_cast<const int8_t*>(xs);
+    const int upr = K >> 4;  // 16-byte units per row
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       if (m < M) {
-        const int8_t* src = pr.codes + static_cast<int64_t>(m) * K;
         int rs = 0;
-        for (int k = 16 * tid; k < K; k += 16 * kDecWarps * 32) {
-          const int4 v = __ldg(reinterpret_cast<const int4*>(src + k));
-          *reinterpret_cast<int4*>(xq + m * K + k) = v;
-          const int vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) rs = __dp4a(vv[e], 0x01010101, rs);
+        for (int u = tid; u < upr; u += kThr) {
+          const int4 v = *reinterpret_cast<const int4*>(stg + m * K + 16 * u);
+          const int b = u >> 3, r = u & 7;
+          *reinterpret_cast<int4*>(xq + m * K + (((r >> 1) * cpr + 2 * b + (r & 1)) << 4)) = v;
+          rs = __dp4a(v.x, 0x01010101, rs);
+          rs = __dp4a(v.y, 0x01010101, rs);
+          rs = __dp4a(v.z, 0x01010101, rs);
+          rs = __dp4a(v.w, 0x01010101, rs);
         }
         rs = warp_sum_int(rs);
         if (lane == 0) tail->rs_part[warp][m] = rs;
@@ -219,13 +319,17 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
     tail->rowsum[tid] = rs;
   }
   compute_bar();
+  // Writing y needs the previous kernel finished: on the unfused path this
+  // thread waited above; on the fused path the activations arrived by a copy the
+  // producer issued only after its own wait returned.
 
   // ------------------------------------------------------------ main loop
-  const int cpr = K >> 6;  // 16-byte chunks per row
-  int lpr = 32;            // lanes per row: largest power of two <= 32 dividing cpr
-  while (cpr % lpr) lpr >>= 1;
-  const int rpp = 32 / lpr;  // rows per warp pass
+  // Odd rows start lpr chunks further on, so with 4 lanes per row the 8 lanes of
+  // a shared-memory phase (two rows) touch 8 different 16-byte bank groups for
+  // weights and codes alike.
+  const int cpl = cpr / lpr;
   const int sub = lane & (lpr - 1);
+  const int rot = lpr * ((lane / lpr) & 1);
   int rowsum[MT];
   float inv_a[MT];
 #pragma unroll
@@ -234,6 +338,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
     inv_a[m] = m < M ? tail->inv_a[m] : 0.0f;
   }
   const float inv_w = pr.inv_w;
+  const int slot_stride = cpr << 4;
 
   for (int st = 0; st < nst; ++st) {
     const int s = st % kDecStages;
@@ -250,10 +355,13 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
         for (int q = 0; q < 4; ++q) acc[m][q] = 0;
       if (valid) {
         const uint8_t* wrow = stage + r * row_bytes;
-        for (int c = sub; c < cpr; c += lpr) {
+        int c = sub + rot;
+        if (c >= cpr) c -= cpr;
+#pragma unroll 2
+        for (int i = 0; i < cpl; ++i) {
           const uint4 wv = *reinterpret_cast<const uint4*>(wrow + c * 16);
           const unsigned wd[4] = {wv.x, wv.y, wv.z, wv.w};
-          const int8_t* xb = xq + (c >> 1) * 128 + 16 * (c & 1);
+          const int8_t* xb = xq + (c << 4);
 #pragma unroll
           for (int sl = 0; sl < 4; ++sl) {
             const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
@@ -261,7 +369,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
               if (m < M) {
-                const int4 xv = *reinterpret_cast<const int4*>(xb + m * K + 32 * sl);
+                const int4 xv = *reinterpret_cast<const int4*>(xb + m * K + sl * slot_stride);
                 int a = acc[m][sl];
                 a = dp4a_us(m0, xv.x, a);
                 a = dp4a_us(m1, xv.y, a);
@@ -271,6 +379,8 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
               }
             }
           }
+          c += lpr;
+          if (c >= cpr) c -= cpr;
         }
       }
       const int n = r0 + st * rps + r;
@@ -288,11 +398,6 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
     __syncwarp();
     if (lane == 0) mbar_arrive(&tail->empty[s]);
   }
-}
-
-size_t decode_smem_bytes(int M, int K) {
-  return static_cast<size_t>(kDecStages) * kDecStageBytes + ((static_cast<size_t>(M) * K + 127) & ~size_t(127)) +
-         sizeof(DecodeSmemTail);
 }
 
 template <int MT, bool kFused>
@@ -314,12 +419,11 @@ cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool p
 }
 
 template <bool kFused>
-cudaError_t dispatch_m(int M, const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err,
+cudaError_t dispatch_m(int mt, const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err,
                        cudaStream_t s) {
-  switch (M) {
+  switch (mt) {
     case 1: return launch_decode_t<1, kFused>(P, grid, smem, pdl, err, s);
     case 2: return launch_decode_t<2, kFused>(P, grid, smem, pdl, err, s);
-    case 3:
     case 4: return launch_decode_t<4, kFused>(P, grid, smem, pdl, err, s);
     default: return launch_decode_t<8, kFused>(P, grid, smem, pdl, err, s);
   }
@@ -329,6 +433,10 @@ cudaError_t dispatch_m(int M, const DecodeParams& P, int grid, size_t smem, bool
 
 bool decode_supported(int64_t M, int64_t K) {
   return M >= 1 && M <= kDecodeMaxM && M * K <= kDecodeMaxCodeBytes;
+}
+
+bool decode_fused_supported(int64_t M, int64_t K) {
+  return M >= 1 && M <= kDecodeMaxM && 5 * M * K + 4 * K <= kDecodeFusedMaxStageBytes;
 }
 
 cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
@@ -341,18 +449,37 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
   double total = 0.0;
   int maxK = 0;
   for (int i = 0; i < njobs; ++i) {
-    total += static_cast<double>(jobs[i].N) * jobs[i].K / 4.0;
+    total += static_cast<double>(jobs[i].N) * jobs[i].K;
     maxK = jobs[i].K > maxK ? jobs[i].K : maxK;
   }
-  const int target = 2 * ctx->num_sms;  // about two resident CTAs per SM
+  // One CTA per SM in total (never a second wave, and room for the next
+  // dependent launch to become resident early), apportioned to the
+  // projections by weight bytes with the largest-remainder rule.
+  int target = ctx->num_sms > njobs ? ctx->num_sms : njobs;
+  int want[BITNET_MAX_GROUP];
+  double frac[BITNET_MAX_GROUP];
+  int used = 0;
+  for (int i = 0; i < njobs; ++i) {
+    const double q = target * (static_cast<double>(jobs[i].N) * jobs[i].K) / total;
+    want[i] = static_cast<int>(q);
+    if (want[i] < 1) want[i] = 1;
+    frac[i] = q - static_cast<int>(q);
+    used += want[i];
+  }
+  while (used < target) {
+    int best = -1;
+    for (int i = 0; i < njobs; ++i)
+      if (want[i] < jobs[i].N && (best < 0 || frac[i] > frac[best])) best = i;
+    if (best < 0) break;
+    ++want[best];
+    frac[best] = -1.0;
+    ++used;
+  }
   int cta = 0;
   for (int i = 0; i < njobs; ++i) {
     const DecodeJob& j = jobs[i];
-    const double bytes = static_cast<double>(j.N) * j.K / 4.0;
-    int want = static_cast<int>(target * bytes / total + 0.5);
-    if (want < 1) want = 1;
-    if (want > j.N) want = j.N;
-    const int rpc = (j.N + want - 1) / want;
+    int w = want[i] > j.N ? j.N : want[i];
+    const int rpc = (j.N + w - 1) / w;
     const int n_ctas = (j.N + rpc - 1) / rpc;
     DecodeProj& p = P.p[i];
     p.x = j.x;
@@ -369,11 +496,12 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
     p.rows_per_cta = rpc;
     cta += n_ctas;
   }
-  int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
-  const size_t smem = decode_smem_bytes(mt, maxK);
-  const bool pdl = true;  // without BITNET_FLAG_WEIGHTS_STATIC every thread waits before reading
-  return fused ? dispatch_m<true>(M, P, cta, smem, pdl, ctx->err_word, s)
-               : dispatch_m<false>(M, P, cta, smem, pdl, ctx->err_word, s);
+  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+  const size_t smem = static_cast<size_t>(DecodeLayout(M, maxK, fused).total);
+  if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;  // unreachable with the dispatch limits
+  const bool pdl = true;  // without BITNET_FLAG_WEIGHTS_STATIC every read waits for the previous kernel
+  return fused ? dispatch_m<true>(mt, P, cta, smem, pdl, ctx->err_word, s)
+               : dispatch_m<false>(mt, P, cta, smem, pdl, ctx->err_word, s);
 }
 
 }  // namespace bitnet

@@ -57,6 +57,9 @@ cudaError_t launch_codes_to_f16(const int8_t* codes, __half* out, int64_t count,
 // Decode (small M) weight-streaming kernels.
 constexpr int kDecodeMaxM = 8;
 constexpr int64_t kDecodeMaxCodeBytes = 65536;  // M * K bytes of codes held in shared memory
+// fused launch: x (4 B) and codes (1 B) per element plus the norm weight (4 B
+// per feature) staged in shared memory next to the 72 KB weight ring
+constexpr int64_t kDecodeFusedMaxStageBytes = 144 * 1024;
 
 struct DecodeJob {
   const float* x;          // fused: activations [M, K]
@@ -70,7 +73,8 @@ struct DecodeJob {
   float* y;                // [M, N]
   int32_t* acc_out;        // [M, N] or null
 };
-bool decode_supported(int64_t M, int64_t K);
+bool decode_supported(int64_t M, int64_t K);        // codes given (int8 in global memory)
+bool decode_fused_supported(int64_t M, int64_t K);  // norm + quant in the same launch
 cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
                           bool weights_static, cudaStream_t s);
 

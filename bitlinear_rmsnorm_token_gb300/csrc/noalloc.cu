@@ -67,17 +67,20 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   if (K < BITNET_I2S_BLOCK || K % BITNET_I2S_BLOCK != 0 || K > BITNET_MAX_K) return BITNET_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1) return BITNET_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y)) return BITNET_ERR_MISALIGNED;
-  const bool small = decode_supported(M, K);
-  // scratch layout: fp16 codes [M, K], then fp32 scales [M] (256-byte aligned)
-  const size_t code_bytes = (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) & ~size_t(255);
-  if (!small && code_bytes + static_cast<size_t>(M) * 4 > static_cast<size_t>(BITNET_NOALLOC_SCRATCH_BYTES))
+  const bool fused = decode_fused_supported(M, K);
+  const bool decode = decode_supported(M, K);
+  // scratch layout: codes [M, K] (int8 for the decode kernel, fp16 for the
+  // tensor-core kernel), then fp32 scales [M], 256-byte aligned
+  const size_t code_bytes =
+      (static_cast<size_t>(M) * static_cast<size_t>(K) * (decode ? 1 : 2) + 255) & ~size_t(255);
+  if (!fused && code_bytes + static_cast<size_t>(M) * 4 > static_cast<size_t>(BITNET_NOALLOC_SCRATCH_BYTES))
     return BITNET_ERR_SCRATCH_LIMIT;
 
   DeviceContext* ctx;
   int rc = device_context_nopool(&ctx);
   if (rc) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (small) {
+  if (fused) {
     DecodeJob j = {};
     j.x = x;
     j.g = norm_w;
@@ -91,10 +94,27 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   }
   void* scratch = nullptr;
   if ((rc = scratch_for_current_device(&scratch))) return rc;
-  __half* f16 = static_cast<__half*>(scratch);
   float* as = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + code_bytes);
   // every element of the used scratch region is written by the norm launch
   // before the contraction reads it, so nothing has to be cleared first
+  if (decode) {
+    int8_t* codes = static_cast<int8_t*>(scratch);
+    cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, codes, nullptr, as, nullptr,
+                                         nullptr, false, s);
+    if (e == cudaSuccess) {
+      DecodeJob j = {};
+      j.codes = codes;
+      j.a_scale = as;
+      j.w = packed_w;
+      j.w_scale = w_scale;
+      j.K = static_cast<int>(K);
+      j.N = static_cast<int>(N);
+      j.y = y;
+      e = launch_decode(ctx, &j, 1, static_cast<int>(M), eps, false, false, s);
+    }
+    return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
+  }
+  __half* f16 = static_cast<__half*>(scratch);
   cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr,
                                        false, s);
   int st = BITNET_OK;

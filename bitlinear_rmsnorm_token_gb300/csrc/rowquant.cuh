@@ -5,10 +5,16 @@
 // "BitNet Embeddings GGUF Conversion Implementation", section 1 ("Background")
 // and section 4.5 (ggml_rms_norm, then ggml_mul by the projection's norm
 // weight); "BitNet Inference Framework", "Quantization (W1.58A8)" (per-token
-// absmax 8-bit activations).  Readings: sum of squares and square root in
-// double, rstd rounded once to float; xn = (x * rstd) * g; a_scale = 127 /
-// max(max|xn|, 1e-5); q = clamp(rint(xn * a_scale), -128, 127); every float
-// operation a single correctly rounded one (no FMA contraction).
+// absmax 8-bit activations).  Definition: rstd = 1/sqrt(sum(x^2)/K + eps)
+// rounded once to float; xn = (x * rstd) * g; a_scale = 127 / max(max|xn|,
+// 1e-5); q = clamp(rint(xn * a_scale), -128, 127); every float operation a
+// single correctly rounded one (no FMA contraction).
+//
+// GB300 has almost no FP64 throughput: the sum of squares is exact integer
+// arithmetic (below) and rstd is carried in an fp32 pair (hi + lo) to ~2^-44
+// before its single rounding to float, so it equals the float rounding of the
+// exact value unless that value lies within ~2^-44 (relative) of a float
+// rounding boundary.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -16,7 +22,7 @@
 
 namespace bitnet {
 
-// Unevaluated sum hi + lo of two floats (about 48 significant bits).
+// Unevaluated sum hi + lo of two floats.
 struct DF {
   float hi, lo;
 };
@@ -31,43 +37,183 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
   return DF{hi, lo};
 }
 
-// x*x split exactly into a rounded product and its rounding error.
-__device__ __forceinline__ DF df_sq(float x) {
-  float p = __fmul_rn(x, x);
-  return DF{p, __fmaf_rn(x, x, -p)};
+// ----------------------------------------------------------- sum of squares
+// The sum of squares of a row is accumulated EXACTLY in 128-bit fixed point
+// relative to the row's largest exponent, so it does not depend on how a
+// kernel splits the row over lanes, warps or passes: every launch path gets
+// the same bits.  With x = m * 2^(e-150) (m the 24-bit significand, e the
+// biased exponent, 1 for subnormals) the term m^2 * 2^(62 - 2(emax - e)) is
+// added; the largest term is below 2^110, so 65536 of them fit in 128 bits.
+// Terms more than 2^-110 below the largest are truncated (relative effect
+// under 2^-94 for K <= 65536).  The row's value is acc * 2^(2 emax - 362).
+struct U128 {
+  unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ U128 u128_add(U128 a, U128 b) {
+  U128 r;
+  r.lo = a.lo + b.lo;
+  r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
+  return r;
 }
 
-// Sum of squares of one row, computed by one full warp.  Lane l owns the float4
-// groups at k = 4*l + 128*c (c = 0 .. K/128-1); each of its four components
-// accumulates in its own DF over c ascending; the four are combined as
-// (0+1)+(2+3); the 32 lanes by an xor butterfly 16, 8, 4, 2, 1.  The result
-// (identical in every lane) is accurate to about 2^-44 relative, far inside
-// double rounding of the oracle's sequential sum, and bit-identical wherever
-// this function is called.  |x| must stay below 1.8e19 (x*x finite in float).
-__device__ __forceinline__ double warp_row_sumsq(const float* __restrict__ xrow, int K, int lane) {
-  DF a0{0.f, 0.f}, a1{0.f, 0.f}, a2{0.f, 0.f}, a3{0.f, 0.f};
-  const int nc = K >> 7;
-#pragma unroll 4
-  for (int c = 0; c < nc; ++c) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(xrow + 4 * lane + 128 * c));
-    a0 = df_add(a0, df_sq(v.x));
-    a1 = df_add(a1, df_sq(v.y));
-    a2 = df_add(a2, df_sq(v.z));
-    a3 = df_add(a3, df_sq(v.w));
+// Biased exponent key of |x| (0 for zero, 1 for subnormals).
+__device__ __forceinline__ int sq_exp(float x) {
+  const unsigned b = __float_as_uint(x) & 0x7fffffffu;
+  const int ef = static_cast<int>(b >> 23);
+  return ef ? ef : (b ? 1 : 0);
+}
+
+__device__ __forceinline__ int sq_exp4(float4 v) {
+  return max(max(sq_exp(v.x), sq_exp(v.y)), max(sq_exp(v.z), sq_exp(v.w)));
+}
+
+__device__ __forceinline__ void sq_add(U128& acc, float x, int emax) {
+  const unsigned b = __float_as_uint(x) & 0x7fffffffu;
+  if (b == 0) return;
+  const int ef = static_cast<int>(b >> 23);
+  const unsigned m = (b & 0x7fffffu) | (ef ? 0x800000u : 0u);
+  const int e = ef ? ef : 1;
+  const unsigned long long sq = static_cast<unsigned long long>(m) * m;  // < 2^48
+  const int sh = 62 - 2 * (emax - e);
+  U128 t;
+  if (sh >= 0) {
+    t.lo = sq << sh;
+    t.hi = sh ? (sq >> (64 - sh)) : 0ull;
+  } else if (sh > -48) {
+    t.lo = sq >> (-sh);
+    t.hi = 0ull;
+  } else {
+    return;
   }
-  DF t = df_add(df_add(a0, a1), df_add(a2, a3));
+  acc = u128_add(acc, t);
+}
+
+__device__ __forceinline__ void sq_add4(U128& acc, float4 v, int emax) {
+  sq_add(acc, v.x, emax);
+  sq_add(acc, v.y, emax);
+  sq_add(acc, v.z, emax);
+  sq_add(acc, v.w, emax);
+}
+
+// Warp-wide exact sum of per-lane 128-bit values: each value is cut into six
+// 24-bit limbs, every limb summed across the warp by one redux instruction
+// (32 * 2^24 < 2^32, no overflow); limb_sums_to_u128 reassembles (also after
+// adding the limb sums of several warps in 64-bit).
+struct LimbSums {
+  unsigned long long l[6];
+};
+
+__device__ __forceinline__ LimbSums warp_limb_sums(U128 a) {
+  const unsigned l0 = static_cast<unsigned>(a.lo) & 0xffffffu;
+  const unsigned l1 = static_cast<unsigned>(a.lo >> 24) & 0xffffffu;
+  const unsigned l2 = static_cast<unsigned>(a.lo >> 48) | ((static_cast<unsigned>(a.hi) & 0xffu) << 16);
+  const unsigned l3 = static_cast<unsigned>(a.hi >> 8) & 0xffffffu;
+  const unsigned l4 = static_cast<unsigned>(a.hi >> 32) & 0xffffffu;
+  const unsigned l5 = static_cast<unsigned>(a.hi >> 56);
+  LimbSums s;
+  s.l[0] = __reduce_add_sync(0xffffffffu, l0);
+  s.l[1] = __reduce_add_sync(0xffffffffu, l1);
+  s.l[2] = __reduce_add_sync(0xffffffffu, l2);
+  s.l[3] = __reduce_add_sync(0xffffffffu, l3);
+  s.l[4] = __reduce_add_sync(0xffffffffu, l4);
+  s.l[5] = __reduce_add_sync(0xffffffffu, l5);
+  return s;
+}
+
+__device__ __forceinline__ void limb_sums_add(LimbSums& a, const LimbSums& b) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    DF o{__shfl_xor_sync(0xffffffffu, t.hi, off), __shfl_xor_sync(0xffffffffu, t.lo, off)};
-    // xor partners add in opposite orders; make the pair order canonical so both
-    // get bit-identical sums (lower lane's value first).
-    t = (lane & off) ? df_add(o, t) : df_add(t, o);
-  }
-  return static_cast<double>(t.hi) + static_cast<double>(t.lo);
+  for (int i = 0; i < 6; ++i) a.l[i] += b.l[i];
 }
 
-__device__ __forceinline__ float rstd_from_sumsq(double ss, int K, float eps) {
-  return static_cast<float>(1.0 / sqrt(ss / static_cast<double>(K) + static_cast<double>(eps)));
+__device__ __forceinline__ U128 limb_sums_to_u128(const LimbSums& s) {
+  U128 r{0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    const int sh = 24 * i;
+    U128 t;
+    t.lo = sh < 64 ? (s.l[i] << sh) : 0ull;
+    t.hi = sh == 0 ? 0ull : (sh < 64 ? (s.l[i] >> (64 - sh)) : (s.l[i] << (sh - 64)));
+    r = u128_add(r, t);
+  }
+  return r;
+}
+
+__device__ __forceinline__ int warp_max_int(int v) {
+  return static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(v)));
+}
+
+// f * 2^e, exact whenever the result is a normal float (f a small integer).
+__device__ __forceinline__ float mul_pow2(float f, int e) {
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const int step = e > 127 ? 127 : (e < -126 ? -126 : e);
+    f = __fmul_rn(f, __int_as_float((step + 127) << 23));
+    e -= step;
+  }
+  return f;
+}
+
+// The fixed-point sum as an fp32 pair (top 48 bits, relative error < 2^-47).
+__device__ __forceinline__ DF sq_to_df(U128 acc, int emax) {
+  if (acc.hi == 0ull && acc.lo == 0ull) return DF{0.0f, 0.0f};
+  const int p = acc.hi ? 127 - __clzll(static_cast<long long>(acc.hi)) : 63 - __clzll(static_cast<long long>(acc.lo));
+  unsigned long long t;  // the top 64 bits, leading one at bit 63
+  if (p > 63) {
+    const int r = p - 63;
+    t = r == 64 ? acc.hi : ((acc.lo >> r) | (acc.hi << (64 - r)));
+  } else {
+    t = acc.lo << (63 - p);
+  }
+  const int base = p - 63 + 2 * emax - 362;  // acc ~= t * 2^base
+  const float fh = static_cast<float>(static_cast<unsigned>(t >> 40));                  // exact (< 2^24)
+  const float fl = static_cast<float>(static_cast<unsigned>((t >> 16) & 0xffffffull));  // exact (< 2^24)
+  const float h = mul_pow2(fh, base + 40);
+  const float l = mul_pow2(fl, base + 16);
+  const float s = __fadd_rn(h, l);
+  return DF{s, __fsub_rn(l, __fsub_rn(s, h))};
+}
+
+// Sum of squares of a row read by one full warp (global or shared memory).
+template <bool kGlobal>
+__device__ __forceinline__ DF warp_row_sumsq(const float* __restrict__ xrow, int K, int lane) {
+  const float* p = xrow + 4 * lane;
+  const int nc = K >> 7;
+  int e = 0;
+  for (int c = 0; c < nc; ++c)
+    e = max(e, sq_exp4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
+                               : *reinterpret_cast<const float4*>(p + 128 * c)));
+  const int emax = warp_max_int(e);
+  U128 acc{0ull, 0ull};
+  for (int c = 0; c < nc; ++c)
+    sq_add4(acc, kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
+                         : *reinterpret_cast<const float4*>(p + 128 * c),
+            emax);
+  return sq_to_df(limb_sums_to_u128(warp_limb_sums(acc)), emax);
+}
+
+// rstd = 1 / sqrt(ss/K + eps), rounded once to float.  ss/K + eps is formed as
+// an fp32 pair (quotient by the reciprocal of K; the remainder hi - q*K is
+// exact by fma since q is within a few ulp of hi/K and K < 2^23); 1/sqrt by the
+// hardware estimate refined with one Newton step whose residual 1 - v*y0^2 is
+// evaluated to ~2^-47.
+__device__ __forceinline__ float rstd_from_sumsq(DF ss, int K, float eps) {
+  const float kf = static_cast<float>(K);  // exact
+  const float rk = __frcp_rn(kf);
+  const float q = __fmul_rn(ss.hi, rk);
+  const float rem = __fmaf_rn(-q, kf, ss.hi);  // exact
+  const float ql = __fmul_rn(__fadd_rn(rem, ss.lo), rk);
+  DF v = df_add(DF{q, ql}, DF{eps, 0.0f});
+  const float y0 = rsqrtf(v.hi);
+  const float s_hi = __fmul_rn(y0, y0);
+  const float s_lo = __fmaf_rn(y0, y0, -s_hi);  // y0^2 = s_hi + s_lo exactly
+  const float t_hi = __fmul_rn(v.hi, s_hi);
+  const float t_err = __fmaf_rn(v.hi, s_hi, -t_hi);
+  // e = 1 - v*y0^2; 1 - t_hi is exact (t_hi is within a few ulp of 1)
+  const float small = __fadd_rn(__fadd_rn(t_err, __fmul_rn(v.hi, s_lo)), __fmul_rn(v.lo, s_hi));
+  const float e = __fsub_rn(__fsub_rn(1.0f, t_hi), small);
+  const float c = __fmul_rn(__fmul_rn(y0, e), 0.5f);
+  return __fadd_rn(y0, c);
 }
 
 __device__ __forceinline__ float norm_elem(float x, float rstd, float g) {
@@ -89,16 +235,13 @@ __device__ __forceinline__ float rescale_elem(float acc_f, float inv_a, float in
   return __fmul_rn(__fmul_rn(acc_f, inv_a), inv_w);
 }
 
+// Max of non-negative floats across the warp (their bit patterns order alike).
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
 __device__ __forceinline__ int warp_sum_int(int v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+  return static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(v)));
 }
 
 }  // namespace bitnet

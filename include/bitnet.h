@@ -75,10 +75,11 @@ extern "C" {
 #define BITNET_MAX_K 65536         /* keeps every partial sum below 2^24 (exact in fp32) */
 #define BITNET_MAX_GROUP 16        /* projections per bitnet_bitlinear_forward_group  */
 
-/* Flag for bitnet_bitlinear_forward_group: the packed weights were written by
- * work that finished before the previous kernel on `stream` began, so the kernel
- * may start streaming them before that kernel has finished (programmatic
- * dependent launch).  Activations are always read after the previous kernel. */
+/* Flag for bitnet_bitlinear_forward_group: the packed weights and norm weights
+ * were written by work that finished before the previous kernel on `stream`
+ * began, so the kernel may start streaming them before that kernel has finished
+ * (programmatic dependent launch).  Activations are always read, and outputs
+ * written, after the previous kernel. */
 #define BITNET_FLAG_WEIGHTS_STATIC 1u
 
 typedef enum {
@@ -162,7 +163,8 @@ typedef struct {
  * and norm weight).  Each output equals bitnet_bitlinear_forward of that
  * projection, bit for bit.  `projs` is a HOST array of `count` descriptors
  * (1..BITNET_MAX_GROUP), read before the call returns.  Supported for
- * M <= 8 and K <= 16384; other shapes return BITNET_ERR_UNSUPPORTED_SHAPE.
+ * M <= 8 and 5*M*K + 4*K <= 147456 (activations, codes and norm weight staged
+ * in shared memory); other shapes return BITNET_ERR_UNSUPPORTED_SHAPE.
  * flags: 0 or BITNET_FLAG_WEIGHTS_STATIC. */
 BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M,
                                    float eps, uint32_t flags, bitnet_stream_t stream);
@@ -178,8 +180,8 @@ BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, in
  *   - Temporary data (fp16 activation codes and per-token scales, 2*M*K + 4*M
  *     bytes, rounded up) lives in one fixed 16 MiB device array that every GPU
  *     using the library keeps until the process exits.  Larger problems return
- *     BITNET_ERR_SCRATCH_LIMIT without launching anything; token counts small
- *     enough for the decode path (M <= 8 and M*K <= 65536) need no scratch.
+ *     BITNET_ERR_SCRATCH_LIMIT without launching anything; M <= 8 with
+ *     5*M*K + 4*K <= 147456 needs no scratch at all (one fused launch).
  *   - The first call on each device does one-time set-up (device properties and
  *     the array's device address); make that first call before any stream
  *     capture.

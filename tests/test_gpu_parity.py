@@ -190,8 +190,13 @@ def test_accumulator_exactness_extremes(oracle_mod, M, K):
 
 # ---------------------------------------------------------------- forward
 
-FWD_CASES = [(1, 128, 1), (1, 1024, 2048), (3, 2048, 1024), (8, 1024, 2048), (16, 640, 256), (64, 1024, 2048),
-             (257, 3072, 1024), (1000, 640, 130), (2048, 2048, 384)]
+FWD_CASES = [
+    # fused decode launch (M <= 8, 5*M*K + 4*K <= 160 KiB)
+    (1, 128, 1), (1, 1024, 2048), (3, 2048, 1024), (8, 1024, 2048), (8, 3072, 100), (1, 16384, 96),
+    # norm launch + decode launch on int8 codes (M <= 8, M*K <= 65536)
+    (3, 16384, 300), (8, 8192, 64), (2, 32768, 40),
+    # norm launch + tensor-core launch
+    (16, 640, 256), (64, 1024, 2048), (257, 3072, 1024), (1000, 640, 130), (2048, 2048, 384), (40, 8192, 256)]
 
 
 @pytest.mark.parametrize("M,K,N", FWD_CASES)
@@ -205,8 +210,13 @@ def test_forward_matches_oracle(oracle_mod, M, K, N):
     assert_rows_close(host(y), ref, f"forward M={M} K={K} N={N}")
 
 
-def test_forward_is_composition_of_the_two_calls():
-    M, K, N = 40, 1024, 300
+@pytest.mark.parametrize("K", [1024, 3072, 16384])
+def test_forward_is_composition_of_the_two_calls(K):
+    """The row reduction is implemented three ways (registers, global re-read,
+    shared memory); all must round identically, so the fused decode launch, the
+    norm launch + decode launch and the norm launch + tensor-core launch agree
+    bit for bit."""
+    M, N = 40, 300
     x = dev(wl.gen_x(M, K, seed=1))
     g = dev(wl.gen_norm_w(K, seed=2))
     packed, ws = bn.pack_i2s(dev(wl.gen_latent_w(N, K, seed=3)))
@@ -214,11 +224,11 @@ def test_forward_is_composition_of_the_two_calls():
     codes, a_scale, _ = bn.rmsnorm_quant_a8(x, g)
     y2 = bn.i2s_gemm(codes, a_scale, packed, ws, N)
     assert torch.equal(y1, y2)
-    xs = x[:4].contiguous()
-    y3 = bn.bitlinear_forward(xs, g, packed, ws, N)       # decode path
+    xs = x[:1].contiguous()
+    y3 = bn.bitlinear_forward(xs, g, packed, ws, N)       # fused decode launch
     c4, s4, _ = bn.rmsnorm_quant_a8(xs, g)
     assert torch.equal(y3, bn.i2s_gemm(c4, s4, packed, ws, N))
-    assert torch.equal(y3, y1[:4])
+    assert torch.equal(y3, y1[:1])
 
 
 def test_forward_on_side_stream(oracle_mod):
