@@ -238,11 +238,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int a = tl & 1;
       const int n0 = (tile % n_wt) * kBM;
       const int m0 = (tile / n_wt) * BN;
-      __syncwarp();
-      for (int j = lane; j < BN; j += 32) {
-        const int m = m0 + j;
-        inv[j] = m < M ? __fdiv_rn(1.0f, __ldg(a_scale + m)) : 0.0f;
+      // the tile's activation scales: all loads in flight at once, then the
+      // correctly rounded reciprocals (rcp.rn == 1.0f / a in IEEE arithmetic)
+      float av[BN / 32];
+#pragma unroll
+      for (int i = 0; i < BN / 32; ++i) {
+        const int m = m0 + lane + 32 * i;
+        av[i] = m < M ? __ldg(a_scale + m) : 1.0f;
       }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < BN / 32; ++i) inv[lane + 32 * i] = __frcp_rn(av[i]);
       __syncwarp();
       if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
       tc_fence_after();

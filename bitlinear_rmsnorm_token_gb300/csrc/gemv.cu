@@ -63,13 +63,14 @@ struct DecodeSmemTail {
   uint64_t full[kDecStages];
   uint64_t empty[kDecStages];
   uint64_t in_full;  // activations (and norm weight) staged
-  unsigned ss_part[kDecWarps][kDecodeMaxM][6];  // per-warp limb sums (each < 2^29)
-  int emax_part[kDecWarps][kDecodeMaxM];
-  float rstd[kDecodeMaxM];
-  float amax_part[kDecWarps][kDecodeMaxM];
-  int rs_part[kDecWarps][kDecodeMaxM];
-  float inv_a[kDecodeMaxM];
+  // per-row reductions, combined across warps with shared-memory atomics
+  // (integer or max: the result does not depend on the order)
+  unsigned long long ss[kDecodeMaxM];
+  int emax[kDecodeMaxM];
+  unsigned amax_bits[kDecodeMaxM];
   int rowsum[kDecodeMaxM];
+  float rstd[kDecodeMaxM];
+  float inv_a[kDecodeMaxM];
   int abort_flag;
 };
 
@@ -147,6 +148,12 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
       mbar_init(&tail->empty[s], kDecWarps);
     }
     mbar_init(&tail->in_full, 1);
+    for (int m = 0; m < kDecodeMaxM; ++m) {
+      tail->ss[m] = 0ull;
+      tail->emax[m] = 0;
+      tail->amax_bits[m] = 0u;
+      tail->rowsum[m] = 0;
+    }
     tail->abort_flag = 0;
     fence_barrier_init();
   }
@@ -200,123 +207,94 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   // ------------------------------------------------------------ compute warps
   const int tid = threadIdx.x;  // 0 .. kDecWarps*32-1
   constexpr int kThr = kDecWarps * 32;
+  // (row, float4 group) of this thread's first element in the flat prologue
+  // loops, worked out while the inputs are still in flight
+  const int G = K >> 2;      // float4 groups per row
+  const int total = M * G;
+  const int m_start = tid / G;
+  const int g_start = tid - m_start * G;
   if (!mbar_wait(&tail->in_full, 0, err, &tail->abort_flag)) return;
+  // Prologue loops run over all (row, float4 group) pairs of the M x K block in
+  // one flat, non-unrolled loop; K/4 is a multiple of 32, so the 32 lanes of a
+  // warp always hold groups of the same row and one warp reduction plus one
+  // shared atomic per warp combines them (integer sums and maxima: order-free).
   if (kFused) {
-    // exact sum of squares, all warps: largest exponent first, then the
-    // fixed-point sum (order-free, so it equals the norm kernel's bit for bit)
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < M) {
-        int e = 0;
-        for (int k = 4 * tid; k < K; k += 4 * kThr) e = max(e, sq_exp4(*reinterpret_cast<const float4*>(xs + m * K + k)));
-        e = warp_max_int(e);
-        if (lane == 0) tail->emax_part[warp][m] = e;
-      }
+#pragma unroll 1
+    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+      while (gi >= G) { gi -= G; ++m; }
+      int e = sq_exp4(*reinterpret_cast<const float4*>(xs + 4 * i));
+      e = warp_max_int(e);
+      if (lane == 0 && e) atomicMax(&tail->emax[m], e);
     }
     compute_bar();
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < M) {
-        int emax = 0;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) emax = max(emax, tail->emax_part[w][m]);
-        U128 acc{0ull, 0ull};
-        for (int k = 4 * tid; k < K; k += 4 * kThr) sq_add4(acc, *reinterpret_cast<const float4*>(xs + m * K + k), emax);
-        const LimbSums ls = warp_limb_sums(acc);
-        if (lane == 0) {
-#pragma unroll
-          for (int i = 0; i < 6; ++i) tail->ss_part[warp][m][i] = static_cast<unsigned>(ls.l[i]);
-        }
-      }
+#pragma unroll 1
+    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+      while (gi >= G) { gi -= G; ++m; }
+      unsigned long long acc = sq_term4(*reinterpret_cast<const float4*>(xs + 4 * i), tail->emax[m]);
+      acc = warp_sum_u64(acc);
+      if (lane == 0 && acc) atomicAdd(&tail->ss[m], acc);
     }
     compute_bar();
-    if (tid < M) {
-      int emax = 0;
-      LimbSums acc;
-#pragma unroll
-      for (int i = 0; i < 6; ++i) acc.l[i] = 0ull;
-      for (int w = 0; w < kDecWarps; ++w) {
-        emax = max(emax, tail->emax_part[w][tid]);
-#pragma unroll
-        for (int i = 0; i < 6; ++i) acc.l[i] += tail->ss_part[w][tid][i];
-      }
-      tail->rstd[tid] = rstd_from_sumsq(sq_to_df(limb_sums_to_u128(acc), emax), K, P.eps);
-    }
+    if (tid < M) tail->rstd[tid] = rstd_from_sumsq(sq_to_df(tail->ss[tid], tail->emax[tid]), K, P.eps);
     compute_bar();
     // normalise in place and take the absmax
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < M) {
-        float* xr = xs + m * K;
-        const float rstd = tail->rstd[m];
-        float amax = 0.0f;
-        for (int k = 4 * tid; k < K; k += 4 * kThr) {
-          const float4 v = *reinterpret_cast<const float4*>(xr + k);
-          const float4 gv = *reinterpret_cast<const float4*>(gs + k);
-          const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
-                                       norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
-          *reinterpret_cast<float4*>(xr + k) = n;
-          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(n.x), fabsf(n.y)), fmaxf(fabsf(n.z), fabsf(n.w))));
-        }
-        amax = warp_max(amax);
-        if (lane == 0) tail->amax_part[warp][m] = amax;
-      }
+#pragma unroll 1
+    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+      while (gi >= G) { gi -= G; ++m; }
+      const int k = 4 * gi;
+      const float rstd = tail->rstd[m];
+      const float4 v = *reinterpret_cast<const float4*>(xs + 4 * i);
+      const float4 gv = *reinterpret_cast<const float4*>(gs + k);
+      const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
+                                   norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
+      *reinterpret_cast<float4*>(xs + 4 * i) = n;
+      const float amax = warp_max(fmaxf(fmaxf(fabsf(n.x), fabsf(n.y)), fmaxf(fabsf(n.z), fabsf(n.w))));
+      if (lane == 0) atomicMax(&tail->amax_bits[m], __float_as_uint(amax));
     }
     compute_bar();
-    // quantise into the slot-major code layout
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < M) {
-        float amax = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) amax = fmaxf(amax, tail->amax_part[w][m]);
-        const float as = act_scale_from_amax(amax);
-        const float* xr = xs + m * K;
-        int rs = 0;
-        for (int k = 4 * tid; k < K; k += 4 * kThr) {
-          const float4 n = *reinterpret_cast<const float4*>(xr + k);
-          const int q0 = quant_elem(n.x, as), q1 = quant_elem(n.y, as);
-          const int q2 = quant_elem(n.z, as), q3 = quant_elem(n.w, as);
-          rs += q0 + q1 + q2 + q3;
-          *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) =
-              (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-              ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
-        }
-        rs = warp_sum_int(rs);
-        if (lane == 0) tail->rs_part[warp][m] = rs;
-        if (tid == 0) tail->inv_a[m] = __fdiv_rn(1.0f, as);
-      }
+    // quantise into the slot-major code layout; lane m of every warp computes
+    // row m's scale and passes it round
+    const float my_as = act_scale_from_amax(lane < M ? __uint_as_float(tail->amax_bits[lane]) : 1.0f);
+#pragma unroll 1
+    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+      while (gi >= G) { gi -= G; ++m; }
+      const int k = 4 * gi;
+      const float as = __shfl_sync(0xffffffffu, my_as, m);
+      const float4 n = *reinterpret_cast<const float4*>(xs + 4 * i);
+      const int q0 = quant_elem(n.x, as), q1 = quant_elem(n.y, as);
+      const int q2 = quant_elem(n.z, as), q3 = quant_elem(n.w, as);
+      *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) =
+          (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+          ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+      const int rs = warp_sum_int(q0 + q1 + q2 + q3);
+      if (lane == 0 && rs) atomicAdd(&tail->rowsum[m], rs);
     }
+    if (tid < M) tail->inv_a[tid] = __frcp_rn(my_as);
   } else {
-    // codes computed elsewhere (staged in natural order): reorder to slot-major,
-    // sum them, fetch the scales
+    // codes computed elsewhere (staged in natural order): reorder to slot-major
+    // 16 bytes at a time, sum them, fetch the scales
     pdl_wait();
     const int8_t* stg = reinterpret_cast<const int8_t*>(xs);
-    const int upr = K >> 4;  // 16-byte units per row
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < M) {
-        int rs = 0;
-        for (int u = tid; u < upr; u += kThr) {
-          const int4 v = *reinterpret_cast<const int4*>(stg + m * K + 16 * u);
-          const int b = u >> 3, r = u & 7;
-          *reinterpret_cast<int4*>(xq + m * K + (((r >> 1) * cpr + 2 * b + (r & 1)) << 4)) = v;
-          rs = __dp4a(v.x, 0x01010101, rs);
-          rs = __dp4a(v.y, 0x01010101, rs);
-          rs = __dp4a(v.z, 0x01010101, rs);
-          rs = __dp4a(v.w, 0x01010101, rs);
-        }
+    const int upr = K >> 4;  // 16-byte units per row (a multiple of 8)
+#pragma unroll 1
+    for (int i = tid, m = tid / upr, u = tid - (tid / upr) * upr; i < M * upr; i += kThr, u += kThr) {
+      while (u >= upr) { u -= upr; ++m; }
+      const int4 v = *reinterpret_cast<const int4*>(stg + 16 * i);
+      const int b = u >> 3, r = u & 7;
+      *reinterpret_cast<int4*>(xq + m * K + (((r >> 1) * cpr + 2 * b + (r & 1)) << 4)) = v;
+      int rs = __dp4a(v.x, 0x01010101, 0);
+      rs = __dp4a(v.y, 0x01010101, rs);
+      rs = __dp4a(v.z, 0x01010101, rs);
+      rs = __dp4a(v.w, 0x01010101, rs);
+      // a warp's 32 units may span two rows when K/16 is not a multiple of 32
+      if (upr % 32 == 0) {
         rs = warp_sum_int(rs);
-        if (lane == 0) tail->rs_part[warp][m] = rs;
-        if (tid == 0) tail->inv_a[m] = __fdiv_rn(1.0f, __ldg(pr.a_scale + m));
+        if (lane == 0 && rs) atomicAdd(&tail->rowsum[m], rs);
+      } else if (rs) {
+        atomicAdd(&tail->rowsum[m], rs);
       }
     }
-  }
-  compute_bar();
-  if (tid < M) {
-    int rs = 0;
-    for (int w = 0; w < kDecWarps; ++w) rs += tail->rs_part[w][tid];
-    tail->rowsum[tid] = rs;
+    if (tid < M) tail->inv_a[tid] = __frcp_rn(__ldg(pr.a_scale + tid));
   }
   compute_bar();
   // Writing y needs the previous kernel finished: on the unfused path this

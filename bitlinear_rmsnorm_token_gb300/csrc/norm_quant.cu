@@ -70,11 +70,11 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
     for (int c = 0; c < kNC; ++c)
       if (c < nc) e = max(e, sq_exp4(v[c]));
     const int emax = warp_max_int(e);
-    U128 acc{0ull, 0ull};
+    unsigned long long acc = 0ull;
 #pragma unroll
     for (int c = 0; c < kNC; ++c)
-      if (c < nc) sq_add4(acc, v[c], emax);
-    const float rstd = rstd_from_sumsq(sq_to_df(limb_sums_to_u128(warp_limb_sums(acc)), emax), K, eps);
+      if (c < nc) acc += sq_term4(v[c], emax);
+    const float rstd = rstd_from_sumsq(sq_to_df(warp_sum_u64(acc), emax), K, eps);
 #pragma unroll
     for (int c = 0; c < kNC; ++c) {
       if (c < nc) {

@@ -10,11 +10,11 @@
 // 1e-5); q = clamp(rint(xn * a_scale), -128, 127); every float operation a
 // single correctly rounded one (no FMA contraction).
 //
-// GB300 has almost no FP64 throughput: the sum of squares is exact integer
-// arithmetic (below) and rstd is carried in an fp32 pair (hi + lo) to ~2^-44
-// before its single rounding to float, so it equals the float rounding of the
-// exact value unless that value lies within ~2^-44 (relative) of a float
-// rounding boundary.
+// GB300 has almost no FP64 throughput: the sum of squares is integer arithmetic
+// (below, exact up to a per-term truncation under 2^-46 of the largest square)
+// and rstd is carried in an fp32 pair (hi + lo) to ~2^-44 before its single
+// rounding to float, so it equals the float rounding of the exact value unless
+// that value lies within ~2^-43 (relative) of a float rounding boundary.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -38,26 +38,14 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
 }
 
 // ----------------------------------------------------------- sum of squares
-// The sum of squares of a row is accumulated EXACTLY in 128-bit fixed point
-// relative to the row's largest exponent, so it does not depend on how a
-// kernel splits the row over lanes, warps or passes: every launch path gets
-// the same bits.  With x = m * 2^(e-150) (m the 24-bit significand, e the
-// biased exponent, 1 for subnormals) the term m^2 * 2^(62 - 2(emax - e)) is
-// added; the largest term is below 2^110, so 65536 of them fit in 128 bits.
-// Terms more than 2^-110 below the largest are truncated (relative effect
-// under 2^-94 for K <= 65536).  The row's value is acc * 2^(2 emax - 362).
-struct U128 {
-  unsigned long long lo, hi;
-};
-
-__device__ __forceinline__ U128 u128_add(U128 a, U128 b) {
-  U128 r;
-  r.lo = a.lo + b.lo;
-  r.hi = a.hi + b.hi + (r.lo < a.lo ? 1ull : 0ull);
-  return r;
-}
-
-// Biased exponent key of |x| (0 for zero, 1 for subnormals).
+// The sum of squares of a row is an exact integer sum, so it does not depend on
+// how a kernel splits the row over lanes, warps or passes: every launch path
+// gets the same bits.  With x = m * 2^(e-150) (m the 24-bit significand, e the
+// biased exponent, 1 for subnormals) and emax the row's largest e, each square
+// contributes the integer m^2 >> (2(emax - e) + 1), i.e. x^2 in units of
+// 2^(2 emax - 299) truncated to an integer.  The largest term is below 2^47, so
+// 65536 of them fit in 64 bits; each truncation is below 2^-46 of the row's
+// largest square.
 __device__ __forceinline__ int sq_exp(float x) {
   const unsigned b = __float_as_uint(x) & 0x7fffffffu;
   const int ef = static_cast<int>(b >> 23);
@@ -68,75 +56,30 @@ __device__ __forceinline__ int sq_exp4(float4 v) {
   return max(max(sq_exp(v.x), sq_exp(v.y)), max(sq_exp(v.z), sq_exp(v.w)));
 }
 
-__device__ __forceinline__ void sq_add(U128& acc, float x, int emax) {
+__device__ __forceinline__ unsigned long long sq_term(float x, int emax) {
   const unsigned b = __float_as_uint(x) & 0x7fffffffu;
-  if (b == 0) return;
   const int ef = static_cast<int>(b >> 23);
   const unsigned m = (b & 0x7fffffu) | (ef ? 0x800000u : 0u);
   const int e = ef ? ef : 1;
-  const unsigned long long sq = static_cast<unsigned long long>(m) * m;  // < 2^48
-  const int sh = 62 - 2 * (emax - e);
-  U128 t;
-  if (sh >= 0) {
-    t.lo = sq << sh;
-    t.hi = sh ? (sq >> (64 - sh)) : 0ull;
-  } else if (sh > -48) {
-    t.lo = sq >> (-sh);
-    t.hi = 0ull;
-  } else {
-    return;
-  }
-  acc = u128_add(acc, t);
+  const int d = max(2 * (emax - e) + 1, 1);  // >= 1; emax == 0 only for an all-zero row
+  const unsigned long long sq = static_cast<unsigned long long>(m) * m;
+  return d < 64 ? (sq >> d) : 0ull;
 }
 
-__device__ __forceinline__ void sq_add4(U128& acc, float4 v, int emax) {
-  sq_add(acc, v.x, emax);
-  sq_add(acc, v.y, emax);
-  sq_add(acc, v.z, emax);
-  sq_add(acc, v.w, emax);
+__device__ __forceinline__ unsigned long long sq_term4(float4 v, int emax) {
+  return (sq_term(v.x, emax) + sq_term(v.y, emax)) + (sq_term(v.z, emax) + sq_term(v.w, emax));
 }
 
-// Warp-wide exact sum of per-lane 128-bit values: each value is cut into six
-// 24-bit limbs, every limb summed across the warp by one redux instruction
-// (32 * 2^24 < 2^32, no overflow); limb_sums_to_u128 reassembles (also after
-// adding the limb sums of several warps in 64-bit).
-struct LimbSums {
-  unsigned long long l[6];
-};
-
-__device__ __forceinline__ LimbSums warp_limb_sums(U128 a) {
-  const unsigned l0 = static_cast<unsigned>(a.lo) & 0xffffffu;
-  const unsigned l1 = static_cast<unsigned>(a.lo >> 24) & 0xffffffu;
-  const unsigned l2 = static_cast<unsigned>(a.lo >> 48) | ((static_cast<unsigned>(a.hi) & 0xffu) << 16);
-  const unsigned l3 = static_cast<unsigned>(a.hi >> 8) & 0xffffffu;
-  const unsigned l4 = static_cast<unsigned>(a.hi >> 32) & 0xffffffu;
-  const unsigned l5 = static_cast<unsigned>(a.hi >> 56);
-  LimbSums s;
-  s.l[0] = __reduce_add_sync(0xffffffffu, l0);
-  s.l[1] = __reduce_add_sync(0xffffffffu, l1);
-  s.l[2] = __reduce_add_sync(0xffffffffu, l2);
-  s.l[3] = __reduce_add_sync(0xffffffffu, l3);
-  s.l[4] = __reduce_add_sync(0xffffffffu, l4);
-  s.l[5] = __reduce_add_sync(0xffffffffu, l5);
-  return s;
-}
-
-__device__ __forceinline__ void limb_sums_add(LimbSums& a, const LimbSums& b) {
-#pragma unroll
-  for (int i = 0; i < 6; ++i) a.l[i] += b.l[i];
-}
-
-__device__ __forceinline__ U128 limb_sums_to_u128(const LimbSums& s) {
-  U128 r{0ull, 0ull};
-#pragma unroll
-  for (int i = 0; i < 6; ++i) {
-    const int sh = 24 * i;
-    U128 t;
-    t.lo = sh < 64 ? (s.l[i] << sh) : 0ull;
-    t.hi = sh == 0 ? 0ull : (sh < 64 ? (s.l[i] >> (64 - sh)) : (s.l[i] << (sh - 64)));
-    r = u128_add(r, t);
-  }
-  return r;
+// Warp-wide exact sum of per-lane partial sums (the total stays below 2^63):
+// three 22-bit limbs, each summed by one redux instruction.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+  const unsigned l0 = static_cast<unsigned>(v) & 0x3fffffu;
+  const unsigned l1 = static_cast<unsigned>(v >> 22) & 0x3fffffu;
+  const unsigned l2 = static_cast<unsigned>(v >> 44);
+  const unsigned long long s0 = __reduce_add_sync(0xffffffffu, l0);
+  const unsigned long long s1 = __reduce_add_sync(0xffffffffu, l1);
+  const unsigned long long s2 = __reduce_add_sync(0xffffffffu, l2);
+  return s0 + (s1 << 22) + (s2 << 44);
 }
 
 __device__ __forceinline__ int warp_max_int(int v) {
@@ -154,18 +97,12 @@ __device__ __forceinline__ float mul_pow2(float f, int e) {
   return f;
 }
 
-// The fixed-point sum as an fp32 pair (top 48 bits, relative error < 2^-47).
-__device__ __forceinline__ DF sq_to_df(U128 acc, int emax) {
-  if (acc.hi == 0ull && acc.lo == 0ull) return DF{0.0f, 0.0f};
-  const int p = acc.hi ? 127 - __clzll(static_cast<long long>(acc.hi)) : 63 - __clzll(static_cast<long long>(acc.lo));
-  unsigned long long t;  // the top 64 bits, leading one at bit 63
-  if (p > 63) {
-    const int r = p - 63;
-    t = r == 64 ? acc.hi : ((acc.lo >> r) | (acc.hi << (64 - r)));
-  } else {
-    t = acc.lo << (63 - p);
-  }
-  const int base = p - 63 + 2 * emax - 362;  // acc ~= t * 2^base
+// The fixed-point sum as an fp32 pair (its top 48 bits).
+__device__ __forceinline__ DF sq_to_df(unsigned long long acc, int emax) {
+  if (acc == 0ull) return DF{0.0f, 0.0f};
+  const int p = 63 - __clzll(static_cast<long long>(acc));
+  const unsigned long long t = acc << (63 - p);  // leading one at bit 63
+  const int base = p - 63 + 2 * emax - 299;      // acc = t * 2^(p-63), one unit = 2^(2 emax - 299)
   const float fh = static_cast<float>(static_cast<unsigned>(t >> 40));                  // exact (< 2^24)
   const float fl = static_cast<float>(static_cast<unsigned>((t >> 16) & 0xffffffull));  // exact (< 2^24)
   const float h = mul_pow2(fh, base + 40);
@@ -184,12 +121,12 @@ __device__ __forceinline__ DF warp_row_sumsq(const float* __restrict__ xrow, int
     e = max(e, sq_exp4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
                                : *reinterpret_cast<const float4*>(p + 128 * c)));
   const int emax = warp_max_int(e);
-  U128 acc{0ull, 0ull};
+  unsigned long long acc = 0ull;
   for (int c = 0; c < nc; ++c)
-    sq_add4(acc, kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
-                         : *reinterpret_cast<const float4*>(p + 128 * c),
-            emax);
-  return sq_to_df(limb_sums_to_u128(warp_limb_sums(acc)), emax);
+    acc += sq_term4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
+                            : *reinterpret_cast<const float4*>(p + 128 * c),
+                    emax);
+  return sq_to_df(warp_sum_u64(acc), emax);
 }
 
 // rstd = 1 / sqrt(ss/K + eps), rounded once to float.  ss/K + eps is formed as
@@ -224,10 +161,10 @@ __device__ __forceinline__ float act_scale_from_amax(float amax) {
   return __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
 }
 
+// rint then clamp: cvt.rni rounds half to even exactly like rintf, and the
+// product's magnitude never exceeds ~127, far inside the int range.
 __device__ __forceinline__ int quant_elem(float xn, float a_scale) {
-  float v = rintf(__fmul_rn(xn, a_scale));
-  v = fminf(fmaxf(v, -128.0f), 127.0f);
-  return static_cast<int>(v);
+  return min(max(__float2int_rn(__fmul_rn(xn, a_scale)), -128), 127);
 }
 
 // y = ((float)acc * (1/a_scale)) * (1/w_scale): the reciprocals are passed in.
