@@ -11,18 +11,20 @@
 // sum is an integer of magnitude <= 127 * K < 2^24 (K <= 65536), so the fp32
 // TMEM accumulator holds the exact integer.
 //
-// One CTA per SM, persistent over output tiles of 128 weight rows x BN tokens:
-//   warp 8     TMA producer: token codes (fp16, 64-wide K slabs, 128B swizzle)
-//              and the tile's raw I2_S bytes (one 128-value block per row)
-//   warps 0-3  unpack: thread t decodes weight row t of the tile from its 32
-//              packed bytes into fp16 (magic-number conversion: 0x6400|c is
-//              1024+c, minus 1025) straight into the 128B-swizzled K-major
-//              layout the MMA reads; each block feeds two 64-wide stages
-//   warp 9     allocates TMEM (2 x BN columns: two accumulators) and one lane
-//              issues tcgen05.mma (M=128 weights, N=BN tokens, K=16) per slab
-//   warps 4-7  epilogue: tcgen05.ld of their TMEM lane quadrant, rescale,
-//              coalesced fp32 stores (a warp writes 32 consecutive outputs of
-//              one token), overlapping the next tile's MMAs
+// One CTA per SM, persistent over output tiles of 128 tokens x BW weights:
+//   warp 8     TMA producer: token codes (fp16, 64-wide K slabs, 128B swizzle;
+//              the MMA's A operand) and the tile's raw I2_S bytes (one
+//              128-value block per weight row, 32 bytes)
+//   warps 0-3  unpack: decode BW weight rows per slab from their packed bytes
+//              into fp16 (magic-number conversion: 0x6400|c is 1024+c, minus
+//              1025) straight into the 128B-swizzled K-major layout of the
+//              MMA's B operand; each packed block feeds two 64-wide slabs
+//   warp 9     allocates TMEM (2 x BW columns: two accumulators) and one lane
+//              issues tcgen05.mma (M=128 tokens, N=BW weights, K=16)
+//   warps 4-7  epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 tokens; each
+//              thread owns one token (one activation scale per tile) and its
+//              outputs are contiguous, so y is written with 16-byte stores,
+//              overlapping the next tile's MMAs (double-buffered accumulator)
 // Every wait is bounded; an expired wait sets the device error word and the
 // CTA unwinds without trapping.
 #include "common.cuh"
@@ -32,26 +34,25 @@
 namespace bitnet {
 namespace {
 
-constexpr int kBM = 128;                   // weight rows per tile (MMA M)
+constexpr int kBT = 128;                   // tokens per tile (MMA M)
 constexpr int kBK = 64;                    // K per stage: one 128-byte swizzle row of fp16
 constexpr int kStages = 4;                 // operand stages
-constexpr int kPkSlots = 4;                // packed-weight slots (one I2_S block column each)
+constexpr int kPkSlots = 2;                // packed-weight slots (one I2_S block column = two stages each)
 constexpr int kThreads = 320;
-constexpr int kAStageBytes = kBM * kBK * 2;           // 16 KB
-constexpr int kPkSlotBytes = kBM * 32;                // 4 KB
+constexpr int kAStageBytes = kBT * kBK * 2;  // 16 KB of token codes
 
-template <int BN>
+template <int BW>
 struct TcLayout {
-  static constexpr int kBStageBytes = BN * kBK * 2;
+  static constexpr int kBStageBytes = BW * kBK * 2;
+  static constexpr int kPkSlotBytes = BW * 32;
   static constexpr int offA = 0;
   static constexpr int offB = offA + kStages * kAStageBytes;
   static constexpr int offP = offB + kStages * kBStageBytes;
-  static constexpr int offInv = offP + kPkSlots * kPkSlotBytes;     // [4 warps][BN] float
-  static constexpr int offBar = offInv + 4 * BN * 4;
+  static constexpr int offBar = offP + kPkSlots * kPkSlotBytes;
   static constexpr int kNumBars = 3 * kStages + 2 * kPkSlots + 4;
-  static constexpr int offMisc = offBar + kNumBars * 8;             // tmem base, abort flag
+  static constexpr int offMisc = offBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kBytes = offMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;                      // room to align the base to 1 KB
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -72,12 +73,30 @@ __device__ __forceinline__ void codes_to_h2(uint32_t v, uint32_t& lo, uint32_t& 
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-template <int BN>
+// One weight row's 64-value slab (slots 2*hf and 2*hf+1 of its I2_S block) as
+// fp16 into the swizzled K-major row `dst` (row r of an 8-row atom: sw = r & 7).
+__device__ __forceinline__ void unpack_row_slab(const uint32_t (&wd)[8], int hf, uint8_t* dst, int sw) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int sl = 2 * hf + (c >> 2);  // slot of the block: elements 32*sl + j
+    const int jw = 2 * (c & 3);        // words jw, jw+1 = bytes j = 8*(c&3) .. +7
+    const int sh = 6 - 2 * sl;
+    const uint32_t v0 = (wd[jw] >> sh) & 0x03030303u;
+    const uint32_t v1 = (wd[jw + 1] >> sh) & 0x03030303u;
+    uint4 out;
+    codes_to_h2(v0, out.x, out.y);
+    codes_to_h2(v1, out.z, out.w);
+    *reinterpret_cast<uint4*>(dst + ((c ^ sw) << 4)) = out;
+  }
+}
+
+template <int BW>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
               const float* __restrict__ a_scale, float inv_w, int M, int N, int K, float* __restrict__ y,
               int32_t* __restrict__ acc_out, unsigned* err) {
-  using L = TcLayout<BN>;
+  using L = TcLayout<BW>;
+  constexpr int kRowsPerThread = BW >= 128 ? BW / 128 : 1;  // unpack rows per thread
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -85,10 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem + L::offA;
   uint8_t* sB = smem + L::offB;
   uint8_t* sP = smem + L::offP;
-  float* sInv = reinterpret_cast<float*>(smem + L::offInv);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
   uint64_t* tok_full = bars;
-  uint64_t* a_full = bars + kStages;
+  uint64_t* b_full = bars + kStages;
   uint64_t* st_empty = bars + 2 * kStages;
   uint64_t* pk_full = bars + 3 * kStages;
   uint64_t* pk_empty = pk_full + kPkSlots;
@@ -99,15 +117,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_wt = (N + kBM - 1) / kBM;
-  const int n_mt = (M + BN - 1) / BN;
+  const int n_wt = (N + BW - 1) / BW;
+  const int n_mt = (M + kBT - 1) / kBT;
   const int num_tiles = n_wt * n_mt;
   const int nkb = K >> 7;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&tok_full[i], 1);
-      mbar_init(&a_full[i], 4);
+      mbar_init(&b_full[i], 4);
       mbar_init(&st_empty[i], 1);
     }
     for (int i = 0; i < kPkSlots; ++i) {
@@ -122,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 9) {
-    tmem_alloc(tmem_slot, 2 * BN);
+    tmem_alloc(tmem_slot, 2 * BW);
     tmem_relinquish();
   }
   if (warp == 8 && lane == 0) {
@@ -142,18 +160,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int s = 0, sph = 0, p = 0, pph = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        const int n0 = (tile % n_wt) * kBM;
-        const int m0 = (tile / n_wt) * BN;
+        const int n0 = (tile % n_wt) * BW;
+        const int m0 = (tile / n_wt) * kBT;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&pk_empty[p], pph ^ 1, err, abort_flag)) goto producer_done;
-          mbar_arrive_expect_tx(&pk_full[p], kPkSlotBytes);
-          tma_load_2d(sP + p * kPkSlotBytes, &tm_w, kb * 32, n0, &pk_full[p]);
+          mbar_arrive_expect_tx(&pk_full[p], L::kPkSlotBytes);
+          tma_load_2d(sP + p * L::kPkSlotBytes, &tm_w, kb * 32, n0, &pk_full[p]);
           if (++p == kPkSlots) { p = 0; pph ^= 1; }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto producer_done;
-            mbar_arrive_expect_tx(&tok_full[s], L::kBStageBytes);
-            tma_load_2d(sB + s * L::kBStageBytes, &tm_tok, kb * 128 + hf * kBK, m0, &tok_full[s]);
+            mbar_arrive_expect_tx(&tok_full[s], kAStageBytes);
+            tma_load_2d(sA + s * kAStageBytes, &tm_tok, kb * 128 + hf * kBK, m0, &tok_full[s]);
             if (++s == kStages) { s = 0; sph ^= 1; }
           }
         }
@@ -163,16 +181,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+      constexpr uint32_t idesc = idesc_f16_f32(kBT, BW);
       int s = 0, sph = 0, tl = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
         const int a = tl & 1;
         if (!mbar_wait(&acc_empty[a], ((tl >> 1) & 1) ^ 1, err, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BW);
         bool ok = true;
         for (int ks = 0; ks < 2 * nkb; ++ks) {
-          if (!mbar_wait(&tok_full[s], sph, err, abort_flag) || !mbar_wait(&a_full[s], sph, err, abort_flag)) {
+          if (!mbar_wait(&tok_full[s], sph, err, abort_flag) || !mbar_wait(&b_full[s], sph, err, abort_flag)) {
             ok = false;
             break;
           }
@@ -191,83 +209,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 4) {
     // --------------------------------------------------------------- unpack
-    const int t = threadIdx.x;  // weight row of the tile
-    uint8_t* const arow_base = sA + (t >> 3) * 1024 + (t & 7) * 128;
-    const int sw = t & 7;
+    // thread t decodes weight rows t, t+128, ... of the tile (BW = 64: t < 64)
+    const int t = threadIdx.x;
+    const bool active = t < BW;
     int s = 0, sph = 0, p = 0, pph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       for (int kb = 0; kb < nkb; ++kb) {
         if (!mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
-        const uint4* src = reinterpret_cast<const uint4*>(sP + p * kPkSlotBytes + t * 32);
-        const uint4 lo4 = src[0];
-        const uint4 hi4 = src[1];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pk_empty[p]);
-        if (++p == kPkSlots) { p = 0; pph ^= 1; }
-        const uint32_t wd[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+        uint32_t wd[kRowsPerThread][8];
+#pragma unroll
+        for (int r = 0; r < kRowsPerThread; ++r) {
+          if (active) {
+            const uint4* src = reinterpret_cast<const uint4*>(sP + p * L::kPkSlotBytes + (t + 128 * r) * 32);
+            const uint4 lo4 = src[0];
+            const uint4 hi4 = src[1];
+            wd[r][0] = lo4.x; wd[r][1] = lo4.y; wd[r][2] = lo4.z; wd[r][3] = lo4.w;
+            wd[r][4] = hi4.x; wd[r][5] = hi4.y; wd[r][6] = hi4.z; wd[r][7] = hi4.w;
+          }
+        }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto unpack_done;
-          uint8_t* arow = arow_base + s * kAStageBytes;
+          if (active) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int sl = 2 * hf + (c >> 2);   // slot of the block: elements 32*sl + j
-            const int jw = 2 * (c & 3);         // words jw, jw+1 = bytes j = 8*(c&3) .. +7
-            const int sh = 6 - 2 * sl;
-            const uint32_t v0 = (wd[jw] >> sh) & 0x03030303u;
-            const uint32_t v1 = (wd[jw + 1] >> sh) & 0x03030303u;
-            uint4 out;
-            codes_to_h2(v0, out.x, out.y);
-            codes_to_h2(v1, out.z, out.w);
-            *reinterpret_cast<uint4*>(arow + ((c ^ sw) << 4)) = out;
+            for (int r = 0; r < kRowsPerThread; ++r) {
+              const int row = t + 128 * r;
+              unpack_row_slab(wd[r], hf, sB + s * L::kBStageBytes + (row >> 3) * 1024 + (row & 7) * 128, row & 7);
+            }
           }
+          // orders this thread's shared-memory accesses (the packed-slot reads
+          // and the slab writes) before later async-proxy accesses: the MMA
+          // reading the slab, the next TMA overwriting the packed slot
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[s]);
+          if (lane == 0) {
+            mbar_arrive(&b_full[s]);
+            // the slot's words have been used by now (the first slab needs all
+            // eight), so its loads are complete: it may be refilled
+            if (hf == 0) mbar_arrive(&pk_empty[p]);
+          }
           if (++s == kStages) { s = 0; sph ^= 1; }
         }
+        if (++p == kPkSlots) { p = 0; pph ^= 1; }
       }
     }
   unpack_done:;
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    float* inv = sInv + (warp - 4) * BN;
     int tl = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
       const int a = tl & 1;
-      const int n0 = (tile % n_wt) * kBM;
-      const int m0 = (tile / n_wt) * BN;
-      // the tile's activation scales: all loads in flight at once, then the
-      // correctly rounded reciprocals (rcp.rn == 1.0f / a in IEEE arithmetic)
-      float av[BN / 32];
-#pragma unroll
-      for (int i = 0; i < BN / 32; ++i) {
-        const int m = m0 + lane + 32 * i;
-        av[i] = m < M ? __ldg(a_scale + m) : 1.0f;
-      }
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < BN / 32; ++i) inv[lane + 32 * i] = __frcp_rn(av[i]);
-      __syncwarp();
+      const int n0 = (tile % n_wt) * BW;
+      const int m0 = (tile / n_wt) * kBT;
+      const int m = m0 + q * 32 + lane;  // this thread's token
+      const bool m_ok = m < M;
+      // rcp.rn == 1.0f / a_scale in IEEE arithmetic
+      const float inv_a = m_ok ? __frcp_rn(__ldg(a_scale + m)) : 0.0f;
       if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
       tc_fence_after();
-      const int n = n0 + q * 32 + lane;
-      const bool n_ok = n < N;
+      float* yrow = y + static_cast<int64_t>(m) * N;
+      const bool vec = (N & 3) == 0 && acc_out == nullptr;
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN; j0 += 32) {
+      for (int j0 = 0; j0 < BW; j0 += 32) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN + j0),
-                           r);
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BW + j0), r);
         tmem_ld_wait();
-        const int mlim = M - (m0 + j0);
+        const int nb = n0 + j0;
+        if (!m_ok || nb >= N) continue;
+        if (vec && nb + 32 <= N) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          if (jj < mlim && n_ok) {
-            const int64_t off = static_cast<int64_t>(m0 + j0 + jj) * N + n;
-            const float accf = __uint_as_float(r[jj]);
-            y[off] = rescale_elem(accf, inv[j0 + jj], inv_w);
-            if (acc_out) acc_out[off] = __float2int_rn(accf);
+          for (int v = 0; v < 8; ++v) {
+            float4 o;
+            o.x = rescale_elem(__uint_as_float(r[4 * v + 0]), inv_a, inv_w);
+            o.y = rescale_elem(__uint_as_float(r[4 * v + 1]), inv_a, inv_w);
+            o.z = rescale_elem(__uint_as_float(r[4 * v + 2]), inv_a, inv_w);
+            o.w = rescale_elem(__uint_as_float(r[4 * v + 3]), inv_a, inv_w);
+            *reinterpret_cast<float4*>(yrow + nb + 4 * v) = o;
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            if (nb + jj < N) {
+              const float accf = __uint_as_float(r[jj]);
+              yrow[nb + jj] = rescale_elem(accf, inv_a, inv_w);
+              if (acc_out) acc_out[static_cast<int64_t>(m) * N + nb + jj] = __float2int_rn(accf);
+            }
           }
         }
       }
@@ -281,19 +308,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * BN);
+    tmem_dealloc(tmem_base, 2 * BW);
   }
 }
 
-template <int BN>
-cudaError_t launch_bn(const DeviceContext* ctx, const CUtensorMap& tm_tok, const CUtensorMap& tm_w,
-                      const float* a_scale, float inv_w, int M, int N, int K, float* y, int32_t* acc_out, bool pdl,
-                      cudaStream_t s) {
-  using L = TcLayout<BN>;
-  auto kern = k_gemm_tc<BN>;
+template <int BW>
+cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __half* codes_f16, const float* a_scale,
+                      const uint8_t* packed_w, float inv_w, int M, int N, int K, float* y, int32_t* acc_out, bool pdl,
+                      cudaStream_t s, int* status) {
+  using L = TcLayout<BW>;
+  CUtensorMap tm_tok, tm_w;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBT)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_tok, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(codes_f16), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
+    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(BW)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed_w), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  auto kern = k_gemm_tc<BW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int tiles = ((N + BW - 1) / BW) * ((M + kBT - 1) / kBT);
   const int grid = tiles < ctx->num_sms ? tiles : ctx->num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -319,40 +373,19 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
     *status = BITNET_ERR_CUDA;
     return cudaErrorNotSupported;
   }
-  const int BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
-  CUtensorMap tm_tok, tm_w;
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(BN)};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = encode(&tm_tok, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(codes_f16), dims, strides,
-                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      *status = BITNET_ERR_CUDA;
-      return cudaErrorInvalidValue;
-    }
-  }
-  {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
-    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kBM)};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed_w), dims, strides, box,
-                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      *status = BITNET_ERR_CUDA;
-      return cudaErrorInvalidValue;
-    }
-  }
   const float inv_w = 1.0f / w_scale;  // IEEE division, as in the oracle
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  switch (BN) {
-    case 64: return launch_bn<64>(ctx, tm_tok, tm_w, a_scale, inv_w, m, n, k, y, acc_out, pdl, s);
-    case 128: return launch_bn<128>(ctx, tm_tok, tm_w, a_scale, inv_w, m, n, k, y, acc_out, pdl, s);
-    default: return launch_bn<256>(ctx, tm_tok, tm_w, a_scale, inv_w, m, n, k, y, acc_out, pdl, s);
+  // widest weight tile that still gives every SM a tile
+  const int64_t m_tiles = (M + kBT - 1) / kBT;
+  int bw = 256;
+  while (bw > 64 && m_tiles * ((N + bw - 1) / bw) < ctx->num_sms) bw >>= 1;
+  switch (bw) {
+    case 64:
+      return launch_bw<64>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, y, acc_out, pdl, s, status);
+    case 128:
+      return launch_bw<128>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, y, acc_out, pdl, s, status);
+    default:
+      return launch_bw<256>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, y, acc_out, pdl, s, status);
   }
 }
 

@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
         }
       }
     }
+    // the stage's loads are complete (their values fed the dot products);
+    // order them before the producer's next bulk copy into the stage
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&tail->empty[s]);
   }

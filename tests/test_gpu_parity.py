@@ -152,6 +152,30 @@ def test_gemm_matches_oracle(oracle_mod, M, K, N):
     assert np.array_equal(host(y), oracle_mod.rescale(acc_o, a_scale, ws))
 
 
+# Shapes whose tile counts make the tensor-core kernel pick 256-, 128- and
+# 64-wide weight tiles with several tiles per CTA and K spanning several packed
+# blocks (the ring of packed slots and operand stages wraps across tiles).
+MULTI_TILE_CASES = [(4096, 640, 2048), (2048, 640, 2048), (4096, 1024, 2048), (1024, 1152, 4096), (300, 640, 1000)]
+
+
+@pytest.mark.parametrize("M,K,N", MULTI_TILE_CASES)
+def test_gemm_multi_tile_ctas(oracle_mod, M, K, N):
+    rng = np.random.default_rng(M + K + N)
+    codes = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    a_scale = rng.uniform(0.5, 300.0, size=M).astype(np.float32)
+    w = wl.gen_latent_w(N, K, seed=N + K)
+    packed, ws = oracle_mod.pack_i2s(w)
+    acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    cd, sd, pd = dev(codes), dev(a_scale), dev(packed)
+    y_acc = bn.i2s_gemm(cd, sd, pd, ws, N, acc_out=acc)   # per-element stores
+    y_vec = bn.i2s_gemm(cd, sd, pd, ws, N)                # vector-store epilogue
+    acc_o = oracle_mod.i2s_matmul(codes, packed, N)
+    assert np.array_equal(host(acc).astype(np.int64), acc_o)
+    y_o = oracle_mod.rescale(acc_o, a_scale, ws)
+    assert np.array_equal(host(y_acc), y_o)
+    assert np.array_equal(host(y_vec), y_o)
+
+
 @pytest.mark.parametrize("path_m", [4, 32])
 def test_gemm_special_weights(oracle_mod, path_m):
     M, K, N = path_m, 128, 128
