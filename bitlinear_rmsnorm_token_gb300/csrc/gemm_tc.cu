@@ -12,16 +12,16 @@
 // TMEM accumulator holds the exact integer.
 //
 // One CTA per SM, persistent over output tiles of 128 tokens x BW weights:
-//   warp 8     TMA producer: token codes (fp16, 64-wide K slabs, 128B swizzle;
+//   warp 12    TMA producer: token codes (fp16, 64-wide K slabs, 128B swizzle;
 //              the MMA's A operand) and the tile's raw I2_S bytes (one
 //              128-value block per weight row, 32 bytes)
-//   warps 0-3  unpack: decode BW weight rows per slab from their packed bytes
-//              into fp16 (magic-number conversion: 0x6400|c is 1024+c, minus
-//              1025) straight into the 128B-swizzled K-major layout of the
-//              MMA's B operand; each packed block feeds two 64-wide slabs
-//   warp 9     allocates TMEM (2 x BW columns: two accumulators) and one lane
+//   warps 0-7  unpack: decode the BW weight rows of each slab from their packed
+//              bytes into fp16 (magic-number conversion: 0x6400|c is 1024+c,
+//              minus 1025) straight into the 128B-swizzled K-major layout of
+//              the MMA's B operand; each packed block feeds two 64-wide slabs
+//   warp 13    allocates TMEM (2 x BW columns: two accumulators) and one lane
 //              issues tcgen05.mma (M=128 tokens, N=BW weights, K=16)
-//   warps 4-7  epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 tokens; each
+//   warps 8-11 epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 tokens; each
 //              thread owns one token (one activation scale per tile) and its
 //              outputs are contiguous, so y is written with 16-byte stores,
 //              overlapping the next tile's MMAs (double-buffered accumulator)
@@ -38,7 +38,8 @@ constexpr int kBT = 128;                   // tokens per tile (MMA M)
 constexpr int kBK = 64;                    // K per stage: one 128-byte swizzle row of fp16
 constexpr int kStages = 4;                 // operand stages
 constexpr int kPkSlots = 2;                // packed-weight slots (one I2_S block column = two stages each)
-constexpr int kThreads = 320;
+constexpr int kUnpackWarps = 8;
+constexpr int kThreads = 448;  // warps 0-7 unpack, 8-11 epilogue, 12 producer, 13 MMA
 constexpr int kAStageBytes = kBT * kBK * 2;  // 16 KB of token codes
 
 template <int BW>
@@ -73,11 +74,14 @@ __device__ __forceinline__ void codes_to_h2(uint32_t v, uint32_t& lo, uint32_t& 
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-// One weight row's 64-value slab (slots 2*hf and 2*hf+1 of its I2_S block) as
-// fp16 into the swizzled K-major row `dst` (row r of an 8-row atom: sw = r & 7).
-__device__ __forceinline__ void unpack_row_slab(const uint32_t (&wd)[8], int hf, uint8_t* dst, int sw) {
+// Chunks c0 .. c0+kChunks-1 (16 bytes = 8 values each) of one weight row's
+// 64-value slab (slots 2*hf and 2*hf+1 of its I2_S block) as fp16 into the
+// swizzled K-major row `dst` (row r of an 8-row atom: sw = r & 7).
+template <int kChunks>
+__device__ __forceinline__ void unpack_row_slab(const uint32_t (&wd)[8], int hf, int c0, uint8_t* dst, int sw) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int ci = 0; ci < kChunks; ++ci) {
+    const int c = c0 + ci;
     const int sl = 2 * hf + (c >> 2);  // slot of the block: elements 32*sl + j
     const int jw = 2 * (c & 3);        // words jw, jw+1 = bytes j = 8*(c&3) .. +7
     const int sh = 6 - 2 * sl;
@@ -96,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float* __restrict__ a_scale, float inv_w, int M, int N, int K, float* __restrict__ y,
               int32_t* __restrict__ acc_out, unsigned* err) {
   using L = TcLayout<BW>;
-  constexpr int kRowsPerThread = BW >= 128 ? BW / 128 : 1;  // unpack rows per thread
+  constexpr int kTpr = kUnpackWarps * 32 / BW;  // unpack threads per weight row (1, 2 or 4)
+  constexpr int kCpt = 8 / kTpr;                 // 16-byte chunks of a slab row per thread
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -125,12 +130,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&tok_full[i], 1);
-      mbar_init(&b_full[i], 4);
+      mbar_init(&b_full[i], kUnpackWarps);
       mbar_init(&st_empty[i], 1);
     }
     for (int i = 0; i < kPkSlots; ++i) {
       mbar_init(&pk_full[i], 1);
-      mbar_init(&pk_empty[i], 4);
+      mbar_init(&pk_empty[i], kUnpackWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -139,11 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 2 * BW);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     prefetch_tensormap(&tm_tok);
     prefetch_tensormap(&tm_w);
   }
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // everything below reads what the previous kernel on the stream produced
   pdl_wait();
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int s = 0, sph = 0, p = 0, pph = 0;
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     producer_done:;
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kBT, BW);
@@ -207,36 +212,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&acc_full[a]);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < kUnpackWarps) {
     // --------------------------------------------------------------- unpack
-    // thread t decodes weight rows t, t+128, ... of the tile (BW = 64: t < 64)
+    // kTpr threads share a weight row of the tile; each writes kCpt of its 8
+    // chunks per slab (all of them need the row's 8 packed words)
     const int t = threadIdx.x;
-    const bool active = t < BW;
+    const int row = t / kTpr;
+    const int c0 = (t % kTpr) * kCpt;
+    uint8_t* const brow = sB + (row >> 3) * 1024 + (row & 7) * 128;
     int s = 0, sph = 0, p = 0, pph = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       for (int kb = 0; kb < nkb; ++kb) {
         if (!mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
-        uint32_t wd[kRowsPerThread][8];
-#pragma unroll
-        for (int r = 0; r < kRowsPerThread; ++r) {
-          if (active) {
-            const uint4* src = reinterpret_cast<const uint4*>(sP + p * L::kPkSlotBytes + (t + 128 * r) * 32);
-            const uint4 lo4 = src[0];
-            const uint4 hi4 = src[1];
-            wd[r][0] = lo4.x; wd[r][1] = lo4.y; wd[r][2] = lo4.z; wd[r][3] = lo4.w;
-            wd[r][4] = hi4.x; wd[r][5] = hi4.y; wd[r][6] = hi4.z; wd[r][7] = hi4.w;
-          }
+        uint32_t wd[8];
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(sP + p * L::kPkSlotBytes + row * 32);
+          const uint4 lo4 = src[0];
+          const uint4 hi4 = src[1];
+          wd[0] = lo4.x; wd[1] = lo4.y; wd[2] = lo4.z; wd[3] = lo4.w;
+          wd[4] = hi4.x; wd[5] = hi4.y; wd[6] = hi4.z; wd[7] = hi4.w;
         }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto unpack_done;
-          if (active) {
-#pragma unroll
-            for (int r = 0; r < kRowsPerThread; ++r) {
-              const int row = t + 128 * r;
-              unpack_row_slab(wd[r], hf, sB + s * L::kBStageBytes + (row >> 3) * 1024 + (row & 7) * 128, row & 7);
-            }
-          }
+          unpack_row_slab<kCpt>(wd, hf, c0, brow + s * L::kBStageBytes, row & 7);
           // orders this thread's shared-memory accesses (the packed-slot reads
           // and the slab writes) before later async-proxy accesses: the MMA
           // reading the slab, the next TMA overwriting the packed slot
@@ -244,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&b_full[s]);
-            // the slot's words have been used by now (the first slab needs all
+            // the slot's words have been used by now (every chunk needs all
             // eight), so its loads are complete: it may be refilled
             if (hf == 0) mbar_arrive(&pk_empty[p]);
           }
@@ -306,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * BW);
   }

@@ -34,7 +34,8 @@ namespace {
 constexpr int kDecWarps = 16;                      // compute warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
 constexpr int kDecStageBytes = 24576;
-constexpr int kDecStages = 3;
+constexpr int kDecMaxStages = 6;  // ring depth is chosen per launch (3 or 6)
+constexpr int kDecRowAcc = 32;  // rows per stage when rows are long enough to need several warps (K >= 4096)
 
 struct DecodeProj {
   const float* x;
@@ -57,11 +58,12 @@ struct DecodeParams {
   int M;
   float eps;
   int weights_static;
+  int stages;  // weight ring depth (<= kDecMaxStages)
 };
 
 struct DecodeSmemTail {
-  uint64_t full[kDecStages];
-  uint64_t empty[kDecStages];
+  uint64_t full[kDecMaxStages];
+  uint64_t empty[kDecMaxStages];
   uint64_t in_full;  // activations (and norm weight) staged
   // per-row reductions, combined across warps with shared-memory atomics
   // (integer or max: the result does not depend on the order)
@@ -69,6 +71,7 @@ struct DecodeSmemTail {
   int emax[kDecodeMaxM];
   unsigned amax_bits[kDecodeMaxM];
   int rowsum[kDecodeMaxM];
+  int row_acc[kDecodeMaxM][kDecRowAcc];  // per-row sums when several warps share a row
   float rstd[kDecodeMaxM];
   float inv_a[kDecodeMaxM];
   int abort_flag;
@@ -85,8 +88,8 @@ struct DecodeSmemTail {
 // read consecutive 16-byte words (no bank conflicts).
 struct DecodeLayout {
   int xs, gs, xq, tail, total;
-  __host__ __device__ DecodeLayout(int M, int K, bool fused) {
-    xs = kDecStages * kDecStageBytes;
+  __host__ __device__ DecodeLayout(int M, int K, bool fused, int stages) {
+    xs = stages * kDecStageBytes;
     gs = xs + (fused ? M * K * 4 : ((M * K + 127) & ~127));
     xq = gs + (fused ? K * 4 : 0);
     tail = xq + ((M * K + 127) & ~127);
@@ -106,7 +109,7 @@ __device__ __forceinline__ void compute_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
 }
 
-template <int MT, bool kFused>
+template <int MT, bool kFused, bool kGrp>
 __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ DecodeParams P, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -129,11 +132,15 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   int lpr = (cpr & 3) ? 2 : 4;
   while (lpr < 32 && cpr % (2 * lpr) == 0 && (r1 - r0) < kDecWarps * (32 / lpr)) lpr *= 2;
   const int rpp = 32 / lpr;  // rows per warp pass
+  // Long rows (cpr a multiple of 32, >= 64) use the row-group mapping of the
+  // main loop; otherwise whole warps take rows and a stage holds whole passes.
+  const bool grp = kGrp && cpr >= 64 && (cpr & 31) == 0;
   int rps = kDecStageBytes / row_bytes;  // rows per stage (K <= 65536 keeps it >= 1)
-  if (rps >= kDecWarps * rpp) rps -= rps % (kDecWarps * rpp);
+  if (!grp && rps >= kDecWarps * rpp) rps -= rps % (kDecWarps * rpp);
   const int nst = (r1 - r0 + rps - 1) / rps;
 
-  const DecodeLayout lay(M, K, kFused);
+  const int kDecStages = P.stages;
+  const DecodeLayout lay(M, K, kFused, kDecStages);
   uint8_t* ring = smem;
   float* xs = reinterpret_cast<float*>(smem + lay.xs);
   float* gs = reinterpret_cast<float*>(smem + lay.gs);
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < kDecMaxStages; ++s) {
       mbar_init(&tail->full[s], 1);
       mbar_init(&tail->empty[s], kDecWarps);
     }
@@ -153,6 +160,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
       tail->emax[m] = 0;
       tail->amax_bits[m] = 0u;
       tail->rowsum[m] = 0;
+      for (int r = 0; r < kDecRowAcc; ++r) tail->row_acc[m][r] = 0;
     }
     tail->abort_flag = 0;
     fence_barrier_init();
@@ -218,56 +226,111 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   // one flat, non-unrolled loop; K/4 is a multiple of 32, so the 32 lanes of a
   // warp always hold groups of the same row and one warp reduction plus one
   // shared atomic per warp combines them (integer sums and maxima: order-free).
+  // Per-row reductions accumulate in registers while a thread's elements stay
+  // in one row and are flushed (one warp reduction, one shared atomic per warp)
+  // when the row changes: a warp's lanes always share the row, so flushes are
+  // warp-uniform.
   if (kFused) {
+    {
+      int e = 0, cur = m_start;
 #pragma unroll 1
-    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
-      while (gi >= G) { gi -= G; ++m; }
-      int e = sq_exp4(*reinterpret_cast<const float4*>(xs + 4 * i));
-      e = warp_max_int(e);
-      if (lane == 0 && e) atomicMax(&tail->emax[m], e);
+      for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+        while (gi >= G) { gi -= G; ++m; }
+        if (m != cur) {
+          const int w = warp_max_int(e);
+          if (lane == 0 && w) atomicMax(&tail->emax[cur], w);
+          e = 0;
+          cur = m;
+        }
+        e = max(e, sq_exp4(*reinterpret_cast<const float4*>(xs + 4 * i)));
+      }
+      if (cur < M) {
+        const int w = warp_max_int(e);
+        if (lane == 0 && w) atomicMax(&tail->emax[cur], w);
+      }
     }
     compute_bar();
+    {
+      unsigned long long acc = 0ull;
+      int cur = m_start;
+      int emax = cur < M ? tail->emax[cur] : 0;
 #pragma unroll 1
-    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
-      while (gi >= G) { gi -= G; ++m; }
-      unsigned long long acc = sq_term4(*reinterpret_cast<const float4*>(xs + 4 * i), tail->emax[m]);
-      acc = warp_sum_u64(acc);
-      if (lane == 0 && acc) atomicAdd(&tail->ss[m], acc);
+      for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+        while (gi >= G) { gi -= G; ++m; }
+        if (m != cur) {
+          const unsigned long long w = warp_sum_u64(acc);
+          if (lane == 0 && w) atomicAdd(&tail->ss[cur], w);
+          acc = 0ull;
+          cur = m;
+          emax = tail->emax[cur];
+        }
+        acc += sq_term4(*reinterpret_cast<const float4*>(xs + 4 * i), emax);
+      }
+      if (cur < M) {
+        const unsigned long long w = warp_sum_u64(acc);
+        if (lane == 0 && w) atomicAdd(&tail->ss[cur], w);
+      }
     }
     compute_bar();
     if (tid < M) tail->rstd[tid] = rstd_from_sumsq(sq_to_df(tail->ss[tid], tail->emax[tid]), K, P.eps);
     compute_bar();
     // normalise in place and take the absmax
+    {
+      float amax = 0.0f;
+      int cur = m_start;
+      float rstd = cur < M ? tail->rstd[cur] : 0.0f;
 #pragma unroll 1
-    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
-      while (gi >= G) { gi -= G; ++m; }
-      const int k = 4 * gi;
-      const float rstd = tail->rstd[m];
-      const float4 v = *reinterpret_cast<const float4*>(xs + 4 * i);
-      const float4 gv = *reinterpret_cast<const float4*>(gs + k);
-      const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
-                                   norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
-      *reinterpret_cast<float4*>(xs + 4 * i) = n;
-      const float amax = warp_max(fmaxf(fmaxf(fabsf(n.x), fabsf(n.y)), fmaxf(fabsf(n.z), fabsf(n.w))));
-      if (lane == 0) atomicMax(&tail->amax_bits[m], __float_as_uint(amax));
+      for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+        while (gi >= G) { gi -= G; ++m; }
+        if (m != cur) {
+          const float w = warp_max(amax);
+          if (lane == 0) atomicMax(&tail->amax_bits[cur], __float_as_uint(w));
+          amax = 0.0f;
+          cur = m;
+          rstd = tail->rstd[cur];
+        }
+        const int k = 4 * gi;
+        const float4 v = *reinterpret_cast<const float4*>(xs + 4 * i);
+        const float4 gv = *reinterpret_cast<const float4*>(gs + k);
+        const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
+                                     norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
+        *reinterpret_cast<float4*>(xs + 4 * i) = n;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(n.x), fabsf(n.y)), fmaxf(fabsf(n.z), fabsf(n.w))));
+      }
+      if (cur < M) {
+        const float w = warp_max(amax);
+        if (lane == 0) atomicMax(&tail->amax_bits[cur], __float_as_uint(w));
+      }
     }
     compute_bar();
     // quantise into the slot-major code layout; lane m of every warp computes
     // row m's scale and passes it round
     const float my_as = act_scale_from_amax(lane < M ? __uint_as_float(tail->amax_bits[lane]) : 1.0f);
+    {
+      int rs = 0, cur = m_start;
 #pragma unroll 1
-    for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
-      while (gi >= G) { gi -= G; ++m; }
-      const int k = 4 * gi;
-      const float as = __shfl_sync(0xffffffffu, my_as, m);
-      const float4 n = *reinterpret_cast<const float4*>(xs + 4 * i);
-      const int q0 = quant_elem(n.x, as), q1 = quant_elem(n.y, as);
-      const int q2 = quant_elem(n.z, as), q3 = quant_elem(n.w, as);
-      *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) =
-          (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-          ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
-      const int rs = warp_sum_int(q0 + q1 + q2 + q3);
-      if (lane == 0 && rs) atomicAdd(&tail->rowsum[m], rs);
+      for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
+        while (gi >= G) { gi -= G; ++m; }
+        if (m != cur) {
+          const int w = warp_sum_int(rs);
+          if (lane == 0 && w) atomicAdd(&tail->rowsum[cur], w);
+          rs = 0;
+          cur = m;
+        }
+        const int k = 4 * gi;
+        const float as = __shfl_sync(0xffffffffu, my_as, m);
+        const float4 n = *reinterpret_cast<const float4*>(xs + 4 * i);
+        const int q0 = quant_elem(n.x, as), q1 = quant_elem(n.y, as);
+        const int q2 = quant_elem(n.z, as), q3 = quant_elem(n.w, as);
+        *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) =
+            (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+            ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+        rs += q0 + q1 + q2 + q3;
+      }
+      if (cur < M) {
+        const int w = warp_sum_int(rs);
+        if (lane == 0 && w) atomicAdd(&tail->rowsum[cur], w);
+      }
     }
     if (tid < M) tail->inv_a[tid] = __frcp_rn(my_as);
   } else {
@@ -317,12 +380,91 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   }
   const float inv_w = pr.inv_w;
   const int slot_stride = cpr << 4;
+  // long-row mapping (see the stage loop): groups of cpr threads, one row each
+  const int n_grp = cpr >= kDecWarps * 32 ? 1 : (kDecWarps * 32) / cpr;
+  const int g_row = cpr >= kDecWarps * 32 ? 0 : tid / cpr;
+  const bool g_on = g_row < n_grp;
+  const int own_c = cpr >= kDecWarps * 32 ? tid : tid % cpr;
+  const int n_own = cpr > kDecWarps * 32 ? cpr / (kDecWarps * 32) : 1;  // <= 2 (K <= 65536)
+  int4 xr1[2][4];  // M == 1: this thread's activation codes, kept in registers
+  if (kGrp && MT == 1 && grp && g_on) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int sl = 0; sl < 4; ++sl)
+        xr1[j][sl] = j < n_own ? *reinterpret_cast<const int4*>(xq + ((own_c + 512 * j) << 4) + sl * slot_stride)
+                               : make_int4(0, 0, 0, 0);
+  }
 
   for (int st = 0; st < nst; ++st) {
     const int s = st % kDecStages;
     if (!mbar_wait(&tail->full[s], (st / kDecStages) & 1, err, &tail->abort_flag)) break;
     const uint8_t* stage = ring + s * kDecStageBytes;
     const int rows = min(rps, r1 - r0 - st * rps);
+    if (kGrp && grp) {
+      // long rows, cpr a multiple of 32: thread t owns chunk positions
+      // t % cpr (+ 512 j when cpr > 512) for the rows r = t / cpr (mod G) of
+      // the stage; warps never straddle rows, one redux + one shared atomic per
+      // warp and row combine the partial sums
+      for (int r = g_on ? g_row : rows; r < rows; r += n_grp) {
+        const uint8_t* wrow = stage + r * row_bytes;
+        int acc[MT][4];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[m][q] = 0;
+        if (g_on) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if (j < n_own) {
+              const int c = own_c + 512 * j;
+              const uint4 wv = *reinterpret_cast<const uint4*>(wrow + c * 16);
+              const unsigned wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+              for (int sl = 0; sl < 4; ++sl) {
+                const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
+                const unsigned m0 = wd[0] & mask, m1 = wd[1] & mask, m2 = wd[2] & mask, m3 = wd[3] & mask;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                  if (m < M) {
+                    const int4 xv = MT == 1 ? xr1[j][sl]
+                                            : *reinterpret_cast<const int4*>(xq + (c << 4) + m * K + sl * slot_stride);
+                    int a = acc[m][sl];
+                    a = dp4a_us(m0, xv.x, a);
+                    a = dp4a_us(m1, xv.y, a);
+                    a = dp4a_us(m2, xv.z, a);
+                    a = dp4a_us(m3, xv.w, a);
+                    acc[m][sl] = a;
+                  }
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < M) {
+            const int t = warp_sum_int((acc[m][0] >> 6) + (acc[m][1] >> 4) + (acc[m][2] >> 2) + acc[m][3]);
+            if (g_on && lane == 0 && t) atomicAdd(&tail->row_acc[m][r], t);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->empty[s]);
+      compute_bar();
+      for (int idx = tid; idx < rows * M; idx += kDecWarps * 32) {
+        const int m = idx / rows;
+        const int r = idx - m * rows;
+        const int a = tail->row_acc[m][r] - tail->rowsum[m];
+        tail->row_acc[m][r] = 0;
+        const int n = r0 + st * rps + r;
+        pr.y[static_cast<int64_t>(m) * N + n] = rescale_elem(__int2float_rn(a), tail->inv_a[m], inv_w);
+        if (pr.acc_out) pr.acc_out[static_cast<int64_t>(m) * N + n] = a;
+      }
+      compute_bar();
+      continue;
+    }
     for (int base = warp * rpp; base < rows; base += kDecWarps * rpp) {
       const int r = base + lane / lpr;
       const bool valid = r < rows;
@@ -381,9 +523,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   }
 }
 
-template <int MT, bool kFused>
+template <int MT, bool kFused, bool kGrp>
 cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err, cudaStream_t s) {
-  auto kern = k_decode<MT, kFused>;
+  auto kern = k_decode<MT, kFused, kGrp>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -399,14 +541,14 @@ cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool p
   return cudaLaunchKernelEx(&cfg, kern, P, err);
 }
 
-template <bool kFused>
+template <bool kFused, bool kGrp>
 cudaError_t dispatch_m(int mt, const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err,
                        cudaStream_t s) {
   switch (mt) {
-    case 1: return launch_decode_t<1, kFused>(P, grid, smem, pdl, err, s);
-    case 2: return launch_decode_t<2, kFused>(P, grid, smem, pdl, err, s);
-    case 4: return launch_decode_t<4, kFused>(P, grid, smem, pdl, err, s);
-    default: return launch_decode_t<8, kFused>(P, grid, smem, pdl, err, s);
+    case 1: return launch_decode_t<1, kFused, kGrp>(P, grid, smem, pdl, err, s);
+    case 2: return launch_decode_t<2, kFused, kGrp>(P, grid, smem, pdl, err, s);
+    case 4: return launch_decode_t<4, kFused, kGrp>(P, grid, smem, pdl, err, s);
+    default: return launch_decode_t<8, kFused, kGrp>(P, grid, smem, pdl, err, s);
   }
 }
 
@@ -478,11 +620,29 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
     cta += n_ctas;
   }
   const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
-  const size_t smem = static_cast<size_t>(DecodeLayout(M, maxK, fused).total);
+  // Ring depth: three stages when no CTA streams more than three of them (the
+  // latency-bound case: small enough for two CTAs per SM, so the next
+  // dependent launch can become resident early), six for long streams (more
+  // bytes in flight per SM) when shared memory allows.
+  bool grp = false;
+  int max_stages = 1;
+  for (int i = 0; i < njobs; ++i) {
+    const int cpr = jobs[i].K / 64;
+    if (cpr >= 64 && cpr % 32 == 0) grp = true;
+    const int rps = kDecStageBytes / (jobs[i].K / 4);
+    const int nst = (P.p[i].rows_per_cta + rps - 1) / rps;
+    max_stages = nst > max_stages ? nst : max_stages;
+  }
+  P.stages = 3;
+  if (max_stages > 3 && DecodeLayout(M, maxK, fused, kDecMaxStages).total <= 227 * 1024) P.stages = kDecMaxStages;
+  const size_t smem = static_cast<size_t>(DecodeLayout(M, maxK, fused, P.stages).total);
   if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;  // unreachable with the dispatch limits
   const bool pdl = true;  // without BITNET_FLAG_WEIGHTS_STATIC every read waits for the previous kernel
-  return fused ? dispatch_m<true>(mt, P, cta, smem, pdl, ctx->err_word, s)
-               : dispatch_m<false>(mt, P, cta, smem, pdl, ctx->err_word, s);
+  if (grp)
+    return fused ? dispatch_m<true, true>(mt, P, cta, smem, pdl, ctx->err_word, s)
+                 : dispatch_m<false, true>(mt, P, cta, smem, pdl, ctx->err_word, s);
+  return fused ? dispatch_m<true, false>(mt, P, cta, smem, pdl, ctx->err_word, s)
+               : dispatch_m<false, false>(mt, P, cta, smem, pdl, ctx->err_word, s);
 }
 
 }  // namespace bitnet

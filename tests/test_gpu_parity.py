@@ -132,6 +132,7 @@ def test_rmsnorm_quant_matches_oracle(oracle_mod, M, K):
 GEMM_CASES = [
     # decode (dp4a) path
     (1, 128, 1), (1, 1024, 2048), (2, 640, 33), (3, 3072, 200), (5, 1024, 129), (8, 1024, 2048), (8, 8192, 64),
+    (1, 16384, 4096), (4, 16384, 2500),
     # tensor-core path: tiles of 128 weight rows x 64/128/256 tokens, ragged tails
     (9, 128, 128), (16, 256, 130), (64, 1024, 256), (100, 640, 1000), (129, 1024, 384), (300, 3072, 257),
     (600, 2048, 1024), (1000, 128, 5),
@@ -217,8 +218,10 @@ def test_accumulator_exactness_extremes(oracle_mod, M, K):
 FWD_CASES = [
     # fused decode launch (M <= 8, 5*M*K + 4*K <= 160 KiB)
     (1, 128, 1), (1, 1024, 2048), (3, 2048, 1024), (8, 1024, 2048), (8, 3072, 100), (1, 16384, 96),
+    # long rows, several warps per row, weight ring wrapping (27 rows per CTA)
+    (1, 16384, 4096), (1, 8192, 3000),
     # norm launch + decode launch on int8 codes (M <= 8, M*K <= 65536)
-    (3, 16384, 300), (8, 8192, 64), (2, 32768, 40),
+    (3, 16384, 300), (8, 8192, 64), (2, 32768, 40), (2, 16384, 4096),
     # norm launch + tensor-core launch
     (16, 640, 256), (64, 1024, 2048), (257, 3072, 1024), (1000, 640, 130), (2048, 2048, 384), (40, 8192, 256)]
 
