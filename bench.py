@@ -182,6 +182,14 @@ def reduce_sum(value, world):
     return float(t.item())
 
 
+def aggregate(ms_local, units_local, world):
+    """Whole-job figures over replicas: the slowest rank's time and the units
+    every rank processed.  Returns (ms_max, units_total, units_total / s)."""
+    ms = reduce_max(float(ms_local), world)
+    units = reduce_sum(float(units_local), world)
+    return ms, units, units / (ms * 1e-3)
+
+
 # --------------------------------------------------------- decode workload
 
 def decode_layer_bytes(layer_shapes, M=1):
@@ -300,9 +308,8 @@ def run_decode(args, rank, world, local):
     barrier(world)
     sampler.stop()
     ms_local = ev0.elapsed_time(ev1)
-    ms = reduce_max(ms_local, world)
-    units = reduce_sum(float(step_bytes) * args.steps, world)
-    value = units / (ms * 1e-3) / 1e9
+    ms, _, value = aggregate(ms_local, float(step_bytes) * args.steps, world)
+    value /= 1e9
     clocks = sampler.summary(t0, t1)
 
     # parity of the timed configuration: every projection of two pool layers
@@ -340,8 +347,7 @@ def run_decode(args, rank, world, local):
             yh[i % n_layers].copy_(L["ybuf"], non_blocking=True)
         e1.record(stream)
     e1.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
-    e2e_units = reduce_sum(float(step_bytes) * e2e_steps, world)
+    _, _, e2e_value = aggregate(e0.elapsed_time(e1), float(step_bytes) * e2e_steps, world)
 
     hbm, _, _, peak_kind = peaks()
     per_launch_ms = ms_local / args.steps
@@ -363,7 +369,7 @@ def run_decode(args, rank, world, local):
                      "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": step_bytes},
-        "e2e": {"value": round(e2e_units / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(e2e_value / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": kx * 4, "d2h_bytes_per_step": ny * 4, "steps": e2e_steps,
                 "api": "bitnet_bitlinear_forward_group from Python, one call per step"},
         "gpu_launches": args.steps,
@@ -375,9 +381,10 @@ def run_decode(args, rank, world, local):
     return out
 
 
-def cpu_baseline_decode(args, budget_s=None):
+def cpu_baseline_decode(args, budget_s=None, max_steps=None, warmup=0):
     """The oracle, as it stands, on the host cores: whole decode layers (7
-    projections at M=1, packed on the host by the oracle) until ~budget_s."""
+    projections at M=1, packed on the host by the oracle).  `warmup` untimed
+    layers, then timed layers until `max_steps` or ~budget_s, whichever first."""
     import oracle
     from bitlinear_rmsnorm_token_gb300 import workloads as wl
 
@@ -392,17 +399,24 @@ def cpu_baseline_decode(args, budget_s=None):
             packed, ws = oracle.pack_i2s(w)
             items.append((x, g, packed, ws, p.N))
         layers.append(items)
-    n = 0
-    t0 = time.perf_counter()
-    while True:
+
+    def one_layer(n):
         for (x, g, packed, ws, N) in layers[n % 2]:
             oracle.bitlinear_forward(x, g, packed, ws, N)
+
+    for n in range(warmup):
+        one_layer(n)
+    n = 0
+    t0 = time.perf_counter()
+    while max_steps is None or n < max_steps:
+        one_layer(n)
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     return {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": f"{n} decode layers (7 projections each, M=1) in {dt:.1f} s"}
+            "kind": "oracle", "steps": n, "seconds": dt,
+            "sample": f"{n} decode layers (7 projections each, M=1) in {dt:.1f} s"}
 
 
 # ----------------------------------------------------- other workloads
@@ -516,8 +530,10 @@ def run_prefill(args, rank, world, local, which):
         ref = oracle.bitlinear_forward(x[rows].cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws, p.N)
         yy = y[rows].cpu().numpy()
         worst = max(worst, float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max()))
-    return {"metric": METRIC, "value": round(flops / (ms * 1e-3) / 1e12, 2), "unit": "TOPS", "n_gpus": world,
-            "ms_per_step": ms, "steps": args.steps, "alg_GBps": alg_bytes / (ms * 1e-3) / 1e9,
+    ms_all, _, ops_per_s = aggregate(ms * args.steps, flops * args.steps, world)
+    ms = ms_all / max(1, args.steps)
+    return {"metric": METRIC, "value": round(ops_per_s / 1e12, 2), "unit": "TOPS", "n_gpus": world,
+            "ms_per_step": ms, "steps": args.steps, "alg_GBps": alg_bytes * world / (ms * 1e-3) / 1e9,
             "config": {"workload": which, "tokens": M, "layers": n_layers,
                        "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
             "parity": {"oracle_worst_row_rel_l2": worst}}
@@ -572,18 +588,21 @@ def run_sweep(args, rank, world, local):
 # ------------------------------------------------------------ reference
 
 def run_reference(args, rank, world):
+    """The oracle on the host cores, rank 0 only (other ranks do no work).  A
+    step is one whole decode layer; W warm-up layers (at most 3: one oracle
+    layer takes milliseconds) then up to K timed ones, bounded by --cpu-seconds."""
     if rank != 0:
         return None
     import oracle
 
     oracle.build()
-    cb = cpu_baseline_decode(args, budget_s=None)
-    steps = args.steps_ref
+    warm = min(args.warmup, 3)
+    cb = cpu_baseline_decode(args, budget_s=None, max_steps=args.steps, warmup=warm)
     shapes = __import__("bitlinear_rmsnorm_token_gb300.workloads", fromlist=["x"]).QWEN3_0P6B_LAYER
-    step_bytes = decode_layer_bytes(shapes, 1)
     value = cb["value"]
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": steps, "warmup": args.warmup, "ms_per_step": step_bytes / (value * 1e9) * 1e3,
+            "steps": cb["steps"], "steps_requested": args.steps, "warmup": warm,
+            "ms_per_step": cb["seconds"] / max(1, cb["steps"]) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary -> int64, fp32",
             "data": "synthetic",
             "config": {"workload": "qwen3_0p6b_decode_layer_M1_7proj", "tokens": 1,
