@@ -18,6 +18,7 @@ __all__ = [
     "BitnetError", "lib", "packed_bytes", "pack_i2s", "unpack_i2s", "rmsnorm_quant_a8", "i2s_gemm",
     "bitlinear_forward", "bitlinear_forward_group", "last_device_status", "status_string",
     "FLAG_WEIGHTS_STATIC", "MAX_GROUP", "EXPORTED_FUNCTIONS", "bitlinear_forward_noalloc",
+    "selftest_bounded_wait",
 ]
 
 OK = 0
@@ -36,6 +37,7 @@ EXPORTED_FUNCTIONS = (
     "bitnet_i2s_packed_bytes", "bitnet_pack_i2s", "bitnet_unpack_i2s", "bitnet_rmsnorm_quant_a8",
     "bitnet_i2s_gemm", "bitnet_bitlinear_forward", "bitnet_bitlinear_forward_group",
     "bitnet_status_string", "bitnet_last_device_status", "bitnet_bitlinear_forward_noalloc",
+    "bitnet_selftest_bounded_wait",
 )
 
 
@@ -86,6 +88,8 @@ def lib(build: bool = False) -> ctypes.CDLL:
     L.bitnet_status_string.argtypes = [ctypes.c_int]
     L.bitnet_last_device_status.restype = ctypes.c_int
     L.bitnet_last_device_status.argtypes = [vp]
+    L.bitnet_selftest_bounded_wait.restype = ctypes.c_int
+    L.bitnet_selftest_bounded_wait.argtypes = [vp]
     _lib = L
     return L
 
@@ -250,3 +254,9 @@ def bitlinear_forward_group(group, M: int, eps: float = 1e-6, flags: int = 0, st
 
 def last_device_status(stream=None) -> int:
     return int(lib().bitnet_last_device_status(_stream(stream)))
+
+
+def selftest_bounded_wait(stream=None) -> None:
+    """Runs the library's bounded wait against a barrier nothing completes (about
+    one second); afterwards last_device_status() reports ERR_TIMEOUT."""
+    _check(lib().bitnet_selftest_bounded_wait(_stream(stream)), "bitnet_selftest_bounded_wait")

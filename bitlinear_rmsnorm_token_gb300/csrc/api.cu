@@ -319,6 +319,40 @@ int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace bitnet {
+namespace {
+
+// One lane per warp waits on a barrier that nothing ever completes, through the
+// same bounded wait as every pipeline of this library; the shared abort flag
+// stops the other waiters as soon as the first one gives up.
+__global__ void k_bounded_wait_selftest(unsigned* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) mbar_wait(&bar, 0, err, &abort_flag);
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace bitnet
+
+extern "C" {
+
+int bitnet_selftest_bounded_wait(bitnet_stream_t stream) {
+  DeviceContext* ctx;
+  int rc = device_context(&ctx);
+  if (rc) return rc;
+  k_bounded_wait_selftest<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ctx->err_word);
+  return cuda_status(cudaGetLastError());
+}
+
 int bitnet_last_device_status(bitnet_stream_t stream) {
   DeviceContext* ctx;
   int rc = device_context(&ctx);

@@ -203,6 +203,16 @@ BITNET_API const char* bitnet_status_string(int status);
  * BITNET_OK otherwise. */
 BITNET_API int bitnet_last_device_status(bitnet_stream_t stream);
 
+/* Diagnostic, with no counterpart in the method: launches one small kernel on
+ * `stream` whose waits target a barrier that nothing ever completes, through
+ * the bounded wait every pipeline of this library uses.  The waits give up
+ * after their time limit (about one second), record the failure in the error
+ * word and return; the kernel exits normally and the context stays usable.
+ * A following bitnet_last_device_status(stream) returns BITNET_ERR_TIMEOUT.
+ * Returns BITNET_OK if the launch succeeded, BITNET_ERR_NO_DEVICE without a
+ * GB300, BITNET_ERR_CUDA on a launch failure. */
+BITNET_API int bitnet_selftest_bounded_wait(bitnet_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
