@@ -22,9 +22,17 @@
 //   warp 13    allocates TMEM (2 x BW columns: two accumulators) and one lane
 //              issues tcgen05.mma (M=128 tokens, N=BW weights, K=16)
 //   warps 8-11 epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 tokens; each
-//              thread owns one token (one activation scale per tile) and its
-//              outputs are contiguous, so y is written with 16-byte stores,
-//              overlapping the next tile's MMAs (double-buffered accumulator)
+//              thread owns one token (one activation scale per tile).  The
+//              warp loads 32 accumulator columns at a time (the next load in
+//              flight while the current columns are written), rescales them
+//              into two 64B-swizzled 32-token x 16-column blocks in shared
+//              memory, and one lane writes each block to y with a TMA store
+//              (whole rows per transaction, no per-thread global stores); the
+//              two blocks alternate so that one store reads shared memory
+//              while the other block is filled.  This overlaps the next
+//              tile's MMAs (double-buffered accumulator).  Without a usable
+//              tensor map for y (N % 4 != 0) or with the accumulator test
+//              output, threads store directly.
 // Every wait is bounded; an expired wait sets the device error word and the
 // CTA unwinds without trapping.
 #include "common.cuh"
@@ -49,11 +57,15 @@ struct TcLayout {
   static constexpr int offA = 0;
   static constexpr int offB = offA + kStages * kAStageBytes;
   static constexpr int offP = offB + kStages * kBStageBytes;
-  static constexpr int offBar = offP + kPkSlots * kPkSlotBytes;
+  static constexpr int offStg = offP + kPkSlots * kPkSlotBytes;  // 1 KB aligned: all sizes above are
+  static constexpr int kStgBytes = 4 * 2 * 32 * 16 * 4;          // two 32 x 16 fp32 blocks per epilogue warp
+  static constexpr int offBar = offStg + kStgBytes;
   static constexpr int kNumBars = 3 * kStages + 2 * kPkSlots + 4;
   static constexpr int offMisc = offBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
+  static_assert(offStg % 1024 == 0, "swizzled staging blocks need 1 KB alignment");
+  static_assert(kAlloc <= 232448, "over the 227 KB of shared memory a CTA may use");
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -97,8 +109,9 @@ __device__ __forceinline__ void unpack_row_slab(const uint32_t (&wd)[8], int hf,
 template <int BW>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
-              const float* __restrict__ a_scale, float inv_w, int M, int N, int K, float* __restrict__ y,
-              int32_t* __restrict__ acc_out, unsigned* err) {
+              const __grid_constant__ CUtensorMap tm_y, int y_by_tma, const float* __restrict__ a_scale,
+              float inv_w, int M, int N, int K, float* __restrict__ y, int32_t* __restrict__ acc_out,
+              unsigned* err) {
   using L = TcLayout<BW>;
   constexpr int kTpr = kUnpackWarps * 32 / BW;  // unpack threads per weight row (1, 2 or 4)
   constexpr int kCpt = 8 / kTpr;                 // 16-byte chunks of a slab row per thread
@@ -151,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 12 && lane == 0) {
     prefetch_tensormap(&tm_tok);
     prefetch_tensormap(&tm_w);
+    if (y_by_tma) prefetch_tensormap(&tm_y);
   }
   tc_fence_before();
   __syncthreads();
@@ -256,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    uint8_t* const stg = smem + L::offStg + q * 4096;  // this warp's two 32 x 16 fp32 staging blocks
+    const int swz = (lane >> 1) & 3;                  // 64B swizzle of this thread's staging row
     int tl = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
       const int a = tl & 1;
@@ -263,30 +279,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = (tile / n_wt) * kBT;
       const int m = m0 + q * 32 + lane;  // this thread's token
       const bool m_ok = m < M;
+      const bool rows_ok = m0 + q * 32 < M;  // warp-uniform: any of the warp's tokens exist
       // rcp.rn == 1.0f / a_scale in IEEE arithmetic
       const float inv_a = m_ok ? __frcp_rn(__ldg(a_scale + m)) : 0.0f;
       if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
       tc_fence_after();
-      float* yrow = y + static_cast<int64_t>(m) * N;
-      const bool vec = (N & 3) == 0 && acc_out == nullptr;
-#pragma unroll 1
-      for (int j0 = 0; j0 < BW; j0 += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BW + j0), r);
-        tmem_ld_wait();
-        const int nb = n0 + j0;
-        if (!m_ok || nb >= N) continue;
-        if (vec && nb + 32 <= N) {
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BW);
+      if (y_by_tma && rows_ok) {
+        const int nch = (min(BW, N - n0) + 31) >> 5;  // 32-column chunks holding outputs
+        // rescale the chunk in r (columns n0 + 32 ch ..) and store it as two blocks
+        auto emit = [&](const uint32_t(&r)[32], int ch) {
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float4 o;
-            o.x = rescale_elem(__uint_as_float(r[4 * v + 0]), inv_a, inv_w);
-            o.y = rescale_elem(__uint_as_float(r[4 * v + 1]), inv_a, inv_w);
-            o.z = rescale_elem(__uint_as_float(r[4 * v + 2]), inv_a, inv_w);
-            o.w = rescale_elem(__uint_as_float(r[4 * v + 3]), inv_a, inv_w);
-            *reinterpret_cast<float4*>(yrow + nb + 4 * v) = o;
+          for (int h = 0; h < 2; ++h) {
+            const int col = n0 + 32 * ch + 16 * h;
+            if (col >= N) break;
+            // the store issued two blocks ago, from this buffer, must have read it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            uint8_t* const buf = stg + h * 2048;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float4 o;
+              o.x = rescale_elem(__uint_as_float(r[16 * h + 4 * v + 0]), inv_a, inv_w);
+              o.y = rescale_elem(__uint_as_float(r[16 * h + 4 * v + 1]), inv_a, inv_w);
+              o.z = rescale_elem(__uint_as_float(r[16 * h + 4 * v + 2]), inv_a, inv_w);
+              o.w = rescale_elem(__uint_as_float(r[16 * h + 4 * v + 3]), inv_a, inv_w);
+              *reinterpret_cast<float4*>(buf + lane * 64 + ((v ^ swz) << 4)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            // rows >= M of the block are clipped by the copy
+            if (lane == 0) {
+              tma_store_2d(&tm_y, buf, col, m0 + q * 32);
+              bulk_commit_group();
+            }
           }
-        } else {
+        };
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(tbase, ra);
+        tmem_ld_wait();
+        tmem_reg_fence(ra);
+        for (int ch = 0;; ch += 2) {
+          const bool more = ch + 1 < nch;
+          if (more) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(32 * (ch + 1)), rb);
+          emit(ra, ch);
+          if (!more) break;
+          tmem_ld_wait();
+          tmem_reg_fence(rb);
+          const bool more2 = ch + 2 < nch;
+          if (more2) tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(32 * (ch + 2)), ra);
+          emit(rb, ch + 1);
+          if (!more2) break;
+          tmem_ld_wait();
+          tmem_reg_fence(ra);
+        }
+      } else if (!y_by_tma && rows_ok) {
+        float* yrow = y + static_cast<int64_t>(m) * N;
+#pragma unroll 1
+        for (int j0 = 0; j0 < BW; j0 += 32) {
+          const int nb = n0 + j0;
+          if (nb >= N) break;
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(j0), r);
+          tmem_ld_wait();
+          tmem_reg_fence(r);
+          if (!m_ok) continue;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             if (nb + jj < N) {
@@ -301,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
     }
+    // stores still in flight read this CTA's shared memory: finish them first
+    if (y_by_tma && lane == 0) bulk_wait_group<0>();
   }
 
   tc_fence_before();
@@ -343,6 +402,23 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
       return cudaErrorInvalidValue;
     }
   }
+  // y through TMA stores: fp32 [M, N], 32-row x 16-column boxes, 64B swizzle (the row
+  // pitch N * 4 must be a multiple of 16 bytes)
+  CUtensorMap tm_y = tm_tok;  // placeholder, never read unless y_by_tma
+  const int y_by_tma = (N % 4 == 0 && acc_out == nullptr) ? 1 : 0;
+  if (y_by_tma) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
   auto kern = k_gemm_tc<BW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
@@ -358,7 +434,8 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, inv_w, M, N, K, y, acc_out, ctx->err_word);
+  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, tm_y, y_by_tma, a_scale, inv_w, M, N, K, y, acc_out,
+                            ctx->err_word);
 }
 
 }  // namespace

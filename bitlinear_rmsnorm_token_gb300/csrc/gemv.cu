@@ -68,7 +68,7 @@ struct DecodeSmemTail {
   // per-row reductions, combined across warps with shared-memory atomics
   // (integer or max: the result does not depend on the order)
   unsigned long long ss[kDecodeMaxM];
-  int emax[kDecodeMaxM];
+  int sq_key[kDecodeMaxM];  // bit pattern of the row's largest |x|
   unsigned amax_bits[kDecodeMaxM];
   int rowsum[kDecodeMaxM];
   int row_acc[kDecodeMaxM][kDecRowAcc];  // per-row sums when several warps share a row
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
     mbar_init(&tail->in_full, 1);
     for (int m = 0; m < kDecodeMaxM; ++m) {
       tail->ss[m] = 0ull;
-      tail->emax[m] = 0;
+      tail->sq_key[m] = 0;
       tail->amax_bits[m] = 0u;
       tail->rowsum[m] = 0;
       for (int r = 0; r < kDecRowAcc; ++r) tail->row_acc[m][r] = 0;
@@ -238,22 +238,22 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
         while (gi >= G) { gi -= G; ++m; }
         if (m != cur) {
           const int w = warp_max_int(e);
-          if (lane == 0 && w) atomicMax(&tail->emax[cur], w);
+          if (lane == 0 && w) atomicMax(&tail->sq_key[cur], w);
           e = 0;
           cur = m;
         }
-        e = max(e, sq_exp4(*reinterpret_cast<const float4*>(xs + 4 * i)));
+        e = max(e, sq_key4(*reinterpret_cast<const float4*>(xs + 4 * i)));
       }
       if (cur < M) {
         const int w = warp_max_int(e);
-        if (lane == 0 && w) atomicMax(&tail->emax[cur], w);
+        if (lane == 0 && w) atomicMax(&tail->sq_key[cur], w);
       }
     }
     compute_bar();
     {
       unsigned long long acc = 0ull;
       int cur = m_start;
-      int emax = cur < M ? tail->emax[cur] : 0;
+      float scale = sq_scale(cur < M ? tail->sq_key[cur] : 0);
 #pragma unroll 1
       for (int i = tid, m = m_start, gi = g_start; i < total; i += kThr, gi += kThr) {
         while (gi >= G) { gi -= G; ++m; }
@@ -262,9 +262,11 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
           if (lane == 0 && w) atomicAdd(&tail->ss[cur], w);
           acc = 0ull;
           cur = m;
-          emax = tail->emax[cur];
+          scale = sq_scale(tail->sq_key[cur]);
         }
-        acc += sq_term4(*reinterpret_cast<const float4*>(xs + 4 * i), emax);
+        SqPartial part = {0ull, 0u};
+        sq_add4(part, *reinterpret_cast<const float4*>(xs + 4 * i), scale);
+        acc += sq_fold(part, 4);
       }
       if (cur < M) {
         const unsigned long long w = warp_sum_u64(acc);
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
       }
     }
     compute_bar();
-    if (tid < M) tail->rstd[tid] = rstd_from_sumsq(sq_to_df(tail->ss[tid], tail->emax[tid]), K, P.eps);
+    if (tid < M) tail->rstd[tid] = rstd_from_fixed(tail->ss[tid], tail->sq_key[tid], K, P.eps);
     compute_bar();
     // normalise in place and take the absmax
     {
@@ -319,13 +321,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
         }
         const int k = 4 * gi;
         const float as = __shfl_sync(0xffffffffu, my_as, m);
-        const float4 n = *reinterpret_cast<const float4*>(xs + 4 * i);
-        const int q0 = quant_elem(n.x, as), q1 = quant_elem(n.y, as);
-        const int q2 = quant_elem(n.z, as), q3 = quant_elem(n.w, as);
-        *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) =
-            (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-            ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
-        rs += q0 + q1 + q2 + q3;
+        const uint32_t pk = quant_pack4_i8(*reinterpret_cast<const float4*>(xs + 4 * i), as);
+        *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(k, cpr)) = pk;
+        rs = __dp4a(static_cast<int>(pk), 0x01010101, rs);
       }
       if (cur < M) {
         const int w = warp_sum_int(rs);

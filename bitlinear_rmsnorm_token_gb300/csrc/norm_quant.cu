@@ -18,30 +18,30 @@ namespace {
 
 constexpr int kNqWarps = 8;
 
+// Quantises four normalised values and stores their codes; the int8 form also
+// adds them to the running row sum (dp4a of the packed bytes with ones).
 template <typename OutT>
-__device__ __forceinline__ void store4(OutT* dst, int q0, int q1, int q2, int q3);
+__device__ __forceinline__ void store_codes4(OutT* dst, float4 n, float a_scale, int& rs);
 
 template <>
-__device__ __forceinline__ void store4<int8_t>(int8_t* dst, int q0, int q1, int q2, int q3) {
-  const uint32_t v = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-                     ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
-  *reinterpret_cast<uint32_t*>(dst) = v;
+__device__ __forceinline__ void store_codes4<int8_t>(int8_t* dst, float4 n, float a_scale, int& rs) {
+  const uint32_t p = quant_pack4_i8(n, a_scale);
+  *reinterpret_cast<uint32_t*>(dst) = p;
+  rs = __dp4a(static_cast<int>(p), 0x01010101, rs);
 }
 
 template <>
-__device__ __forceinline__ void store4<__half>(__half* dst, int q0, int q1, int q2, int q3) {
-  // integers in [-128, 127] are exact in fp16
-  __half2 a = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-  __half2 b = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+__device__ __forceinline__ void store_codes4<__half>(__half* dst, float4 n, float a_scale, int&) {
   uint2 v;
-  v.x = *reinterpret_cast<uint32_t*>(&a);
-  v.y = *reinterpret_cast<uint32_t*>(&b);
+  v.x = quant_pack2_f16(n.x, n.y, a_scale);
+  v.y = quant_pack2_f16(n.z, n.w, a_scale);
   *reinterpret_cast<uint2*>(dst) = v;
 }
 
-// kNC > 0: the row (at most kNC float4 groups per lane) is loaded once into
-// registers; kNC == 0: any K, the row is read three times (L1/L2 after the first).
-template <typename OutT, int kNC>
+// kNC > 0: the row (at most kNC float4 groups per lane; exactly kNC when kExact,
+// which spares the predicated-off groups) is loaded once into registers;
+// kNC == 0: any K, the row is read three times (L1/L2 after the first).
+template <typename OutT, int kNC, bool kExact>
 __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __restrict__ x, const float* __restrict__ g,
                                                                  int64_t M, int K, float eps, OutT* __restrict__ codes,
                                                                  float* __restrict__ a_scale,
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
   if (row >= M) return;
   const float* xr = x + row * K + 4 * lane;
   const float* gr = g + 4 * lane;
-  const int nc = K >> 7;
+  const int nc = kExact ? kNC : (K >> 7);
   OutT* cr = codes + row * K + 4 * lane;
   float* xo = xn_out ? xn_out + row * K + 4 * lane : nullptr;
   float amax = 0.0f;
@@ -65,16 +65,18 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
 #pragma unroll
     for (int c = 0; c < kNC; ++c)
       if (c < nc) v[c] = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
-    int e = 0;
+    int key = 0;
 #pragma unroll
     for (int c = 0; c < kNC; ++c)
-      if (c < nc) e = max(e, sq_exp4(v[c]));
-    const int emax = warp_max_int(e);
-    unsigned long long acc = 0ull;
+      if (c < nc) key = max(key, sq_key4(v[c]));
+    key = warp_max_int(key);
+    const float scale = sq_scale(key);
+    SqPartial part = {0ull, 0u};
 #pragma unroll
     for (int c = 0; c < kNC; ++c)
-      if (c < nc) acc += sq_term4(v[c], emax);
-    const float rstd = rstd_from_sumsq(sq_to_df(warp_sum_u64(acc), emax), K, eps);
+      if (c < nc) sq_add4(part, v[c], scale);
+    const unsigned long long acc = sq_fold(part, 4 * min(nc, kNC));
+    const float rstd = rstd_from_fixed(warp_sum_u64(acc), key, K, eps);
 #pragma unroll
     for (int c = 0; c < kNC; ++c) {
       if (c < nc) {
@@ -88,20 +90,15 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
     const float as = act_scale_from_amax(warp_max(amax));
 #pragma unroll
     for (int c = 0; c < kNC; ++c) {
-      if (c < nc) {
-        const int q0 = quant_elem(v[c].x, as), q1 = quant_elem(v[c].y, as);
-        const int q2 = quant_elem(v[c].z, as), q3 = quant_elem(v[c].w, as);
-        store4<OutT>(cr + 128 * c, q0, q1, q2, q3);
-        rs += q0 + q1 + q2 + q3;
-      }
+      if (c < nc) store_codes4<OutT>(cr + 128 * c, v[c], as, rs);
     }
-    rs = warp_sum_int(rs);
+    if (rowsum) rs = warp_sum_int(rs);
     if (lane == 0) {
       a_scale[row] = as;
       if (rowsum) rowsum[row] = rs;
     }
   } else {
-    const float rstd = rstd_from_sumsq(warp_row_sumsq<true>(x + row * K, K, lane), K, eps);
+    const float rstd = warp_row_rstd<true>(x + row * K, K, lane, eps);
     for (int c = 0; c < nc; ++c) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
       const float4 gv = __ldg(reinterpret_cast<const float4*>(gr + 128 * c));
@@ -114,12 +111,11 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
     for (int c = 0; c < nc; ++c) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
       const float4 gv = __ldg(reinterpret_cast<const float4*>(gr + 128 * c));
-      const int q0 = quant_elem(norm_elem(v.x, rstd, gv.x), as), q1 = quant_elem(norm_elem(v.y, rstd, gv.y), as);
-      const int q2 = quant_elem(norm_elem(v.z, rstd, gv.z), as), q3 = quant_elem(norm_elem(v.w, rstd, gv.w), as);
-      store4<OutT>(cr + 128 * c, q0, q1, q2, q3);
-      rs += q0 + q1 + q2 + q3;
+      const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
+                                   norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
+      store_codes4<OutT>(cr + 128 * c, n, as, rs);
     }
-    rs = warp_sum_int(rs);
+    if (rowsum) rs = warp_sum_int(rs);
     if (lane == 0) {
       a_scale[row] = as;
       if (rowsum) rowsum[row] = rs;
@@ -132,11 +128,18 @@ __global__ void __launch_bounds__(256) k_codes_to_f16(const int8_t* __restrict__
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n4) return;
   const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(in) + t);
-  store4<__half>(out + 4 * t, static_cast<int8_t>(v & 0xFF), static_cast<int8_t>((v >> 8) & 0xFF),
-                 static_cast<int8_t>((v >> 16) & 0xFF), static_cast<int8_t>(v >> 24));
+  // integers in [-128, 127] are exact in fp16
+  const __half2 a = __halves2half2(__int2half_rn(static_cast<int8_t>(v & 0xFFu)),
+                                   __int2half_rn(static_cast<int8_t>((v >> 8) & 0xFFu)));
+  const __half2 b = __halves2half2(__int2half_rn(static_cast<int8_t>((v >> 16) & 0xFFu)),
+                                   __int2half_rn(static_cast<int8_t>(v >> 24)));
+  uint2 o;
+  o.x = *reinterpret_cast<const uint32_t*>(&a);
+  o.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(out + 4 * t) = o;
 }
 
-template <typename OutT, int kNC>
+template <typename OutT, int kNC, bool kExact = false>
 cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
                       int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
@@ -148,13 +151,20 @@ cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float ep
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant<OutT, kNC>, x, g, M, K, eps, codes, a_scale, rowsum, xn_out);
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant<OutT, kNC, kExact>, x, g, M, K, eps, codes, a_scale, rowsum, xn_out);
 }
 
 template <typename OutT>
 cudaError_t launch_nq_k(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
                         int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
   const int nc = K >> 7;
+  switch (nc) {  // the model widths of the prefill shapes: K = 640, 1024, 2048, 3072
+    case 5: return launch_nq<OutT, 5, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 8: return launch_nq<OutT, 8, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 16: return launch_nq<OutT, 16, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 24: return launch_nq<OutT, 24, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    default: break;
+  }
   if (nc <= 8) return launch_nq<OutT, 8>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
   if (nc <= 24) return launch_nq<OutT, 24>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
   return launch_nq<OutT, 0>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
@@ -165,7 +175,10 @@ cudaError_t launch_nq_k(const float* x, const float* g, int64_t M, int K, float 
 cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int K, float eps, int8_t* codes_i8,
                                  __half* codes_f16, float* a_scale, int32_t* rowsum, float* xn_out, bool pdl,
                                  cudaStream_t s) {
-  if (codes_f16) return launch_nq_k<__half>(x, g, M, K, eps, codes_f16, a_scale, rowsum, xn_out, pdl, s);
+  if (codes_f16) {
+    if (rowsum) return cudaErrorInvalidValue;  // row sums are produced with int8 codes only
+    return launch_nq_k<__half>(x, g, M, K, eps, codes_f16, a_scale, nullptr, xn_out, pdl, s);
+  }
   return launch_nq_k<int8_t>(x, g, M, K, eps, codes_i8, a_scale, rowsum, xn_out, pdl, s);
 }
 

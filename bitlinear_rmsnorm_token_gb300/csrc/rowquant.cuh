@@ -10,13 +10,16 @@
 // 1e-5); q = clamp(rint(xn * a_scale), -128, 127); every float operation a
 // single correctly rounded one (no FMA contraction).
 //
-// GB300 has almost no FP64 throughput: the sum of squares is integer arithmetic
-// (below, exact up to a per-term truncation under 2^-46 of the largest square)
-// and rstd is carried in an fp32 pair (hi + lo) to ~2^-44 before its single
-// rounding to float, so it equals the float rounding of the exact value unless
-// that value lies within ~2^-43 (relative) of a float rounding boundary.
+// GB300 has almost no FP64 throughput, and its integer ALU pipe runs at half
+// the rate of the FMA pipe: the sum of squares is a fixed-point integer sum
+// (below) whose per-element work is mostly fp32 multiply/add, accurate to
+// ~2^-43 of the row's largest square per element and independent of summation
+// order, and rstd is carried in an fp32 pair (hi + lo) to ~2^-44 before its
+// single rounding to float, so it equals the float rounding of the exact value
+// unless that value lies within ~2^-40 (relative) of a float rounding boundary.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,37 +40,72 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
   return DF{hi, lo};
 }
 
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that float to
+// an integer (ties to even, like rintf) held in the low mantissa bits.
+constexpr float kRoundMagic = 12582912.0f;
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+
 // ----------------------------------------------------------- sum of squares
-// The sum of squares of a row is an exact integer sum, so it does not depend on
-// how a kernel splits the row over lanes, warps or passes: every launch path
-// gets the same bits.  With x = m * 2^(e-150) (m the 24-bit significand, e the
-// biased exponent, 1 for subnormals) and emax the row's largest e, each square
-// contributes the integer m^2 >> (2(emax - e) + 1), i.e. x^2 in units of
-// 2^(2 emax - 299) truncated to an integer.  The largest term is below 2^47, so
-// 65536 of them fit in 64 bits; each truncation is below 2^-46 of the row's
-// largest square.
-__device__ __forceinline__ int sq_exp(float x) {
-  const unsigned b = __float_as_uint(x) & 0x7fffffffu;
-  const int ef = static_cast<int>(b >> 23);
-  return ef ? ef : (b ? 1 : 0);
+// The sum of squares of a row is an integer sum, so it does not depend on how a
+// kernel splits the row over lanes, warps or passes: every launch path gets the
+// same bits.  The row key is the bit pattern of the row's largest |x|; from its
+// exponent the row scale 2^k puts that largest |x| in [2^20, 2^21).  Each
+// element contributes, with s = |x| 2^k (exact) split as s = S + r (S = rint(s),
+// |r| <= 1/2, both exact):
+//     S^2 + rint(u r),  u = fl(2S + r)          ~= s^2 = S^2 + (2S + r) r,
+// the first term exact in 64-bit integer arithmetic and the second within 5/8
+// of exact (|u r| < 2^21), so the sum is s^2 summed to within
+// 5/8 per element in units where the largest square is ~2^41; it is never
+// negative and stays below 2^58 for K <= 65536.  ss = sum * 2^(-2k).
+__device__ __forceinline__ int sq_key(float x) { return __float_as_int(fabsf(x)); }
+
+__device__ __forceinline__ int sq_key4(float4 v) {
+  return __float_as_int(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
 }
 
-__device__ __forceinline__ int sq_exp4(float4 v) {
-  return max(max(sq_exp(v.x), sq_exp(v.y)), max(sq_exp(v.z), sq_exp(v.w)));
+// k of the row scale.  Rows whose largest |x| is below 2^-106 keep k = 127:
+// their sum of squares (< 2^-196) is far below any eps > 0 at float precision.
+__device__ __forceinline__ int sq_shift(int key) { return min(147 - (key >> 23), 127); }
+
+__device__ __forceinline__ float sq_scale(int key) { return __int_as_float((sq_shift(key) + 127) << 23); }
+
+// One row's partial sum: `sq` holds the S^2 terms; `cb` the raw bit patterns of
+// the rounded sums 1.5 * 2^23 + rint(u r), whose offsets are removed when the
+// partial is folded (each rint(u r) is below 2^21 in magnitude, so up to 1023
+// elements can be folded at once without leaving the int32 range).
+struct SqPartial {
+  unsigned long long sq;
+  uint32_t cb;
+};
+
+__device__ __forceinline__ void sq_add(SqPartial& a, float x, float scale) {
+  const float s = __fmul_rn(fabsf(x), scale);  // exact unless it underflows (then S = 0 and rint(u r) = 0)
+  const float t = __fadd_rn(s, kRoundMagic);
+  const float sf = __fsub_rn(t, kRoundMagic);  // S
+  const uint32_t si = __float_as_uint(t) - kRoundMagicBits;
+  const float r = __fsub_rn(s, sf);
+  const float u = __fmaf_rn(2.0f, sf, r);
+  a.cb += __float_as_uint(__fmaf_rn(u, r, kRoundMagic));
+  asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(a.sq) : "r"(si));
 }
 
-__device__ __forceinline__ unsigned long long sq_term(float x, int emax) {
-  const unsigned b = __float_as_uint(x) & 0x7fffffffu;
-  const int ef = static_cast<int>(b >> 23);
-  const unsigned m = (b & 0x7fffffu) | (ef ? 0x800000u : 0u);
-  const int e = ef ? ef : 1;
-  const int d = max(2 * (emax - e) + 1, 1);  // >= 1; emax == 0 only for an all-zero row
-  const unsigned long long sq = static_cast<unsigned long long>(m) * m;
-  return d < 64 ? (sq >> d) : 0ull;
+__device__ __forceinline__ void sq_add4(SqPartial& a, float4 v, float scale) {
+  sq_add(a, v.x, scale);
+  sq_add(a, v.y, scale);
+  sq_add(a, v.z, scale);
+  sq_add(a, v.w, scale);
 }
 
-__device__ __forceinline__ unsigned long long sq_term4(float4 v, int emax) {
-  return (sq_term(v.x, emax) + sq_term(v.y, emax)) + (sq_term(v.z, emax) + sq_term(v.w, emax));
+// The partial's value after `n` (< 1024) calls of sq_add.
+__device__ __forceinline__ unsigned long long sq_fold(const SqPartial& a, int n) {
+  const int c = static_cast<int>(a.cb - static_cast<uint32_t>(n) * kRoundMagicBits);
+  return a.sq + static_cast<unsigned long long>(static_cast<long long>(c));
 }
 
 // Warp-wide exact sum of per-lane partial sums (the total stays below 2^63):
@@ -97,50 +135,56 @@ __device__ __forceinline__ float mul_pow2(float f, int e) {
   return f;
 }
 
-// The fixed-point sum as an fp32 pair (its top 48 bits).
-__device__ __forceinline__ DF sq_to_df(unsigned long long acc, int emax) {
-  if (acc == 0ull) return DF{0.0f, 0.0f};
-  const int p = 63 - __clzll(static_cast<long long>(acc));
-  const unsigned long long t = acc << (63 - p);  // leading one at bit 63
-  const int base = p - 63 + 2 * emax - 299;      // acc = t * 2^(p-63), one unit = 2^(2 emax - 299)
-  const float fh = static_cast<float>(static_cast<unsigned>(t >> 40));                  // exact (< 2^24)
-  const float fl = static_cast<float>(static_cast<unsigned>((t >> 16) & 0xffffffull));  // exact (< 2^24)
-  const float h = mul_pow2(fh, base + 40);
-  const float l = mul_pow2(fl, base + 16);
-  const float s = __fadd_rn(h, l);
-  return DF{s, __fsub_rn(l, __fsub_rn(s, h))};
-}
-
-// Sum of squares of a row read by one full warp (global or shared memory).
-template <bool kGlobal>
-__device__ __forceinline__ DF warp_row_sumsq(const float* __restrict__ xrow, int K, int lane) {
-  const float* p = xrow + 4 * lane;
-  const int nc = K >> 7;
-  int e = 0;
-  for (int c = 0; c < nc; ++c)
-    e = max(e, sq_exp4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
-                               : *reinterpret_cast<const float4*>(p + 128 * c)));
-  const int emax = warp_max_int(e);
-  unsigned long long acc = 0ull;
-  for (int c = 0; c < nc; ++c)
-    acc += sq_term4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
-                            : *reinterpret_cast<const float4*>(p + 128 * c),
-                    emax);
-  return sq_to_df(warp_sum_u64(acc), emax);
-}
-
-// rstd = 1 / sqrt(ss/K + eps), rounded once to float.  ss/K + eps is formed as
-// an fp32 pair (quotient by the reciprocal of K; the remainder hi - q*K is
-// exact by fma since q is within a few ulp of hi/K and K < 2^23); 1/sqrt by the
-// hardware estimate refined with one Newton step whose residual 1 - v*y0^2 is
-// evaluated to ~2^-47.
-__device__ __forceinline__ float rstd_from_sumsq(DF ss, int K, float eps) {
+// rstd = 1 / sqrt(ss/K + eps), rounded once to float, where ss = acc * 2^(-2k)
+// is the fixed-point sum of squares of a row with key `key`.
+//
+// ss spans ~2^-300 .. 2^272, far outside fp32, so both terms are scaled by
+// 2^(-e2) first, which leaves every intermediate a normal float, and the result
+// by 2^(-e2/2) after (exact for a normal rstd).  e2 is ss's binary exponent
+// rounded down to even, which puts ss * 2^-e2 in [1, 4); when ss/K is below
+// 2^-59 eps it cannot change the result at the accuracy carried here, is
+// dropped, and e2 comes from eps instead.  ss * 2^-e2 is taken as an fp32 pair
+// (the top 48 bits of acc), ss/K + eps as an fp32 pair (quotient by the
+// reciprocal of K; the remainder hi - q*K is exact by fma since q is within a
+// few ulp of hi/K and K < 2^23); 1/sqrt by the hardware estimate refined with
+// one Newton step whose residual 1 - v*y0^2 is evaluated to ~2^-47.
+__device__ __forceinline__ float rstd_from_fixed(unsigned long long acc, int key, int K, float eps) {
+  // eps = em * 2^ee, em in [1, 2)
+  float eps_n = eps;
+  int ee = -127;
+  if ((__float_as_int(eps) >> 23) == 0) {  // subnormal eps
+    eps_n = __fmul_rn(eps, 18446744073709551616.0f);  // * 2^64, exact
+    ee -= 64;
+  }
+  ee += __float_as_int(eps_n) >> 23;
+  const float em = __int_as_float((__float_as_int(eps_n) & 0x7fffff) | 0x3f800000);
+  const int e_eps = ee + (31 - __clz(K)) - 60;
+  DF ss = {0.0f, 0.0f};
+  int e2 = e_eps;
+  if (acc != 0ull) {
+    const int p = 63 - __clzll(static_cast<long long>(acc));
+    const int lv = p - 2 * sq_shift(key);  // ss in [2^lv, 2^(lv+1))
+    if (lv >= e_eps) {
+      e2 = lv;
+      const int base = lv - (lv & ~1) - 63;            // -63 or -62: ss * 2^-e2 = t * 2^base
+      const unsigned long long t = acc << (63 - p);  // leading one at bit 63
+      const float h = __fmul_rn(static_cast<float>(static_cast<unsigned>(t >> 40)),
+                                __int_as_float((base + 40 + 127) << 23));  // exact, in [1, 4)
+      const float l = __fmul_rn(static_cast<float>(static_cast<unsigned>((t >> 16) & 0xffffffull)),
+                                __int_as_float((base + 16 + 127) << 23));  // exact
+      const float sum = __fadd_rn(h, l);
+      ss = DF{sum, __fsub_rn(l, __fsub_rn(sum, h))};
+    }
+  }
+  e2 &= ~1;
+  const int es = ee - e2;  // <= 62
+  const float eps_s = es >= -126 ? __fmul_rn(em, __int_as_float((es + 127) << 23)) : 0.0f;  // else negligible
   const float kf = static_cast<float>(K);  // exact
   const float rk = __frcp_rn(kf);
   const float q = __fmul_rn(ss.hi, rk);
   const float rem = __fmaf_rn(-q, kf, ss.hi);  // exact
   const float ql = __fmul_rn(__fadd_rn(rem, ss.lo), rk);
-  DF v = df_add(DF{q, ql}, DF{eps, 0.0f});
+  DF v = df_add(DF{q, ql}, DF{eps_s, 0.0f});
   const float y0 = rsqrtf(v.hi);
   const float s_hi = __fmul_rn(y0, y0);
   const float s_lo = __fmaf_rn(y0, y0, -s_hi);  // y0^2 = s_hi + s_lo exactly
@@ -150,7 +194,34 @@ __device__ __forceinline__ float rstd_from_sumsq(DF ss, int K, float eps) {
   const float small = __fadd_rn(__fadd_rn(t_err, __fmul_rn(v.hi, s_lo)), __fmul_rn(v.lo, s_hi));
   const float e = __fsub_rn(__fsub_rn(1.0f, t_hi), small);
   const float c = __fmul_rn(__fmul_rn(y0, e), 0.5f);
-  return __fadd_rn(y0, c);
+  const float r = __fadd_rn(y0, c);
+  const int j = -(e2 / 2);
+  return (j >= -126 && j <= 127) ? __fmul_rn(r, __int_as_float((j + 127) << 23)) : mul_pow2(r, j);
+}
+
+// rstd of a row read by one full warp (global or shared memory).
+template <bool kGlobal>
+__device__ __forceinline__ float warp_row_rstd(const float* __restrict__ xrow, int K, int lane, float eps) {
+  const float* p = xrow + 4 * lane;
+  const int nc = K >> 7;
+  int key = 0;
+  for (int c = 0; c < nc; ++c)
+    key = max(key, sq_key4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
+                                   : *reinterpret_cast<const float4*>(p + 128 * c)));
+  key = warp_max_int(key);
+  const float scale = sq_scale(key);
+  unsigned long long acc = 0ull;
+  for (int c0 = 0; c0 < nc; c0 += 128) {  // folds every 512 elements per lane
+    SqPartial part = {0ull, 0u};
+    const int c1 = min(nc, c0 + 128);
+    for (int c = c0; c < c1; ++c)
+      sq_add4(part,
+              kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
+                      : *reinterpret_cast<const float4*>(p + 128 * c),
+              scale);
+    acc += sq_fold(part, 4 * (c1 - c0));
+  }
+  return rstd_from_fixed(warp_sum_u64(acc), key, K, eps);
 }
 
 __device__ __forceinline__ float norm_elem(float x, float rstd, float g) {
@@ -161,10 +232,32 @@ __device__ __forceinline__ float act_scale_from_amax(float amax) {
   return __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
 }
 
-// rint then clamp: cvt.rni rounds half to even exactly like rintf, and the
-// product's magnitude never exceeds ~127, far inside the int range.
-__device__ __forceinline__ int quant_elem(float xn, float a_scale) {
-  return min(max(__float2int_rn(__fmul_rn(xn, a_scale)), -128), 127);
+// q = rint(xn * a_scale).  The definition clamps q to [-128, 127]; for finite
+// inputs that clamp never acts: |xn| <= amax and a_scale = fl(127 / max(amax,
+// 1e-5)), so |fl(xn * a_scale)| <= fl(127 (1 + 2^-24)) and q lies in [-127, 127].
+// Rounding by the 1.5 * 2^23 addition is exact for such products and breaks ties
+// to even like rintf.  (Non-finite inputs give unspecified codes.)
+
+// Four codes as int8 bytes (element 0 in the low byte): the low byte of each
+// rounded sum is the code in two's complement.
+__device__ __forceinline__ uint32_t quant_pack4_i8(float4 n, float a_scale) {
+  const uint32_t t0 = __float_as_uint(__fadd_rn(__fmul_rn(n.x, a_scale), kRoundMagic));
+  const uint32_t t1 = __float_as_uint(__fadd_rn(__fmul_rn(n.y, a_scale), kRoundMagic));
+  const uint32_t t2 = __float_as_uint(__fadd_rn(__fmul_rn(n.z, a_scale), kRoundMagic));
+  const uint32_t t3 = __float_as_uint(__fadd_rn(__fmul_rn(n.w, a_scale), kRoundMagic));
+  return prmt_b32(prmt_b32(t0, t1, 0x0040u), prmt_b32(t2, t3, 0x0040u), 0x5410u);
+}
+
+// Two codes as an fp16 pair (element 0 in the low half).  Adding 1.5 * 2^23 +
+// 0x6600 leaves 0x6600 + q, the fp16 pattern of 1536 + q, in the low 16 bits of
+// the rounded sum; subtracting 1536 in fp16 is exact.
+__device__ __forceinline__ uint32_t quant_pack2_f16(float a, float b, float a_scale) {
+  constexpr float kHalfMagic = 12609024.0f;  // 1.5 * 2^23 + 0x6600
+  const uint32_t t0 = __float_as_uint(__fadd_rn(__fmul_rn(a, a_scale), kHalfMagic));
+  const uint32_t t1 = __float_as_uint(__fadd_rn(__fmul_rn(b, a_scale), kHalfMagic));
+  uint32_t h = prmt_b32(t0, t1, 0x5410u);
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __floats2half2_rn(1536.0f, 1536.0f));
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // y = ((float)acc * (1/a_scale)) * (1/w_scale): the reciprocals are passed in.

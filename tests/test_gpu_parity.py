@@ -100,7 +100,7 @@ def _x_with_edges(M, K, seed):
     return x
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (5, 640), (33, 1024), (17, 3072), (3, 16384), (2, 65536)])
+@pytest.mark.parametrize("M,K", [(1, 128), (5, 640), (33, 1024), (9, 2048), (4, 1152), (17, 3072), (3, 16384), (2, 65536)])
 def test_rmsnorm_quant_matches_oracle(oracle_mod, M, K):
     x = _x_with_edges(M, K, seed=M * 31 + K)
     g = wl.gen_norm_w(K, seed=K)
@@ -127,6 +127,62 @@ def test_rmsnorm_quant_matches_oracle(oracle_mod, M, K):
         assert np.all(host(codes)[1] == 0) and host(rowsum)[1] == 0
 
 
+def _x_extreme_rows(K, seed):
+    """Rows that stress the fixed-point sum of squares and the row scale: huge,
+    tiny and subnormal magnitudes, two magnitudes 40 decades apart, one
+    dominant element over many tiny ones, per-element exponents spread over
+    60 binades, a single non-zero element, values near the float maximum."""
+    rng = np.random.default_rng(seed)
+    b = rng.standard_normal((8, K))
+    x = np.empty((8, K), np.float64)
+    x[0] = b[0] * 1e30
+    x[1] = b[1] * 1e-30
+    x[2] = b[2] * 1e-40
+    x[3] = b[3] * np.where(np.arange(K) % 2 == 1, 1e20, 1e-20)
+    x[4] = b[4] * 1e-7
+    x[4, 0] = 3.0
+    x[5] = b[5] * np.exp2(rng.integers(-30, 30, K).astype(np.float64))
+    x[6] = 0.0
+    x[6, K // 2] = -2.5
+    x[7] = np.where(rng.random(K) < 0.01, 3.0e38, 1.0) * np.sign(b[7])
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("K", [1024, 65536])
+def test_rmsnorm_quant_extreme_rows(oracle_mod, K):
+    x = _x_extreme_rows(K, seed=K)
+    g = wl.gen_norm_w(K, seed=K + 1)
+    M = x.shape[0]
+    codes = torch.empty((M, K), dtype=torch.int8, device="cuda")
+    a_scale = torch.empty(M, dtype=torch.float32, device="cuda")
+    rowsum = torch.empty(M, dtype=torch.int32, device="cuda")
+    xn = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    bn.rmsnorm_quant_a8(dev(x), dev(g), wl.EPS, codes, a_scale, rowsum, xn)
+    xn_gpu = host(xn)
+    q_o, s_o, rs_o = oracle_mod.quant_a8(xn_gpu)
+    assert np.array_equal(host(codes), q_o)
+    assert np.array_equal(host(a_scale), s_o)
+    assert np.array_equal(host(rowsum), rs_o)
+    xn_o = oracle_mod.rmsnorm(x, g, wl.EPS)
+    assert int(np.sum(np.any(xn_gpu != xn_o, axis=1))) <= 1
+
+
+@pytest.mark.parametrize("K", [1024, 4096])
+def test_forward_extreme_rows(oracle_mod, K):
+    """The fused decode path (M = 8) and the prefill path on the same rows."""
+    x = _x_extreme_rows(K, seed=K + 7)
+    g = wl.gen_norm_w(K, seed=K + 8)
+    N = 256
+    w = wl.gen_latent_w(N, K, seed=K + 9)
+    packed, ws = bn.pack_i2s(dev(w))
+    ref = oracle_mod.bitlinear_forward(x, g, host(packed), ws, N, wl.EPS)
+    y_dec = host(bn.bitlinear_forward(dev(x), dev(g), packed, ws, N, wl.EPS))
+    assert_rows_close(y_dec, ref, f"decode K={K}")
+    xx = np.tile(x, (4, 1))  # 32 rows: the tensor-core path
+    y_tc = host(bn.bitlinear_forward(dev(xx), dev(g), packed, ws, N, wl.EPS))
+    assert_rows_close(y_tc, np.tile(ref, (4, 1)), f"prefill K={K}")
+
+
 # ------------------------------------------------------------ contraction
 
 GEMM_CASES = [
@@ -150,7 +206,12 @@ def test_gemm_matches_oracle(oracle_mod, M, K, N):
     y = bn.i2s_gemm(dev(codes), dev(a_scale), dev(packed), ws, N, acc_out=acc)
     acc_o = oracle_mod.i2s_matmul(codes, packed, N)
     assert np.array_equal(host(acc).astype(np.int64), acc_o)
-    assert np.array_equal(host(y), oracle_mod.rescale(acc_o, a_scale, ws))
+    y_o = oracle_mod.rescale(acc_o, a_scale, ws)
+    assert np.array_equal(host(y), y_o)
+    # without the accumulator output the tensor-core path writes y by TMA
+    # stores (N % 4 == 0) that clip the ragged rows and columns of the tiles
+    y2 = bn.i2s_gemm(dev(codes), dev(a_scale), dev(packed), ws, N)
+    assert np.array_equal(host(y2), y_o)
 
 
 # Shapes whose tile counts make the tensor-core kernel pick 256-, 128- and
@@ -169,7 +230,7 @@ def test_gemm_multi_tile_ctas(oracle_mod, M, K, N):
     acc = torch.empty((M, N), dtype=torch.int32, device="cuda")
     cd, sd, pd = dev(codes), dev(a_scale), dev(packed)
     y_acc = bn.i2s_gemm(cd, sd, pd, ws, N, acc_out=acc)   # per-element stores
-    y_vec = bn.i2s_gemm(cd, sd, pd, ws, N)                # vector-store epilogue
+    y_vec = bn.i2s_gemm(cd, sd, pd, ws, N)                # TMA-store epilogue
     acc_o = oracle_mod.i2s_matmul(codes, packed, N)
     assert np.array_equal(host(acc).astype(np.int64), acc_o)
     y_o = oracle_mod.rescale(acc_o, a_scale, ws)
