@@ -540,6 +540,12 @@ def run_prefill(args, rank, world, local, which):
 
 
 def run_sweep(args, rank, world, local):
+    """K, N in {1024, 4096, 8192, 16384} x M in {1, 16, 128, 2048, 16384}.  Each
+    point cycles through enough distinct weight tensors to exceed twice the L2
+    (at most 1024), one projection call per tensor.  Where the temporaries fit
+    the no-alloc entry point's fixed scratch, the whole cycle is one CUDA graph
+    (kernel time, not Python launch time); otherwise calls are issued eagerly
+    (those points run >= 80 us per call)."""
     import torch
 
     import bitlinear_rmsnorm_token_gb300 as bn
@@ -553,8 +559,7 @@ def run_sweep(args, rank, world, local):
     for K in wl.SWEEP_KN:
         for N in wl.SWEEP_KN:
             wb = N * K // 4
-            nw = max(1, int(np.ceil(2.0 * L2_BYTES / wb))) if wb < 2 * L2_BYTES else 1
-            nw = min(nw, 64)
+            nw = min(1024, max(1, int(np.ceil(2.0 * L2_BYTES / wb))))
             ws_list = []
             for i in range(nw):
                 w = wl.gen_device((N, K), wl.seed_for(4, K, N, i), device, std=0.02)
@@ -564,21 +569,33 @@ def run_sweep(args, rank, world, local):
             for M in wl.SWEEP_M:
                 x = wl.gen_device((M, K), wl.seed_for(4, M, K, N), device)
                 y = torch.empty((M, N), dtype=torch.float32, device=device)
-                it = [0]
+                code_bytes = M * K * (1 if M <= 8 else 2)
+                graphed = ((code_bytes + 255) // 256) * 256 + 4 * M <= bn.NOALLOC_SCRATCH_BYTES
+                fwd = bn.bitlinear_forward_noalloc if graphed else bn.bitlinear_forward
 
-                def step():
-                    packed, s = ws_list[it[0] % nw]
-                    it[0] += 1
-                    bn.bitlinear_forward(x, g, packed, s, N, wl.EPS, y, stream=stream)
+                def cycle():
+                    for packed, sc in ws_list:
+                        fwd(x, g, packed, sc, N, wl.EPS, y, stream=stream)
 
                 with torch.cuda.stream(stream):
-                    reps = 20 if M * N * K < 2**36 else 5
-                    ms = time_region(torch, stream, step, reps, 3)
+                    cycle()  # warm-up (also checks every call)
+                stream.synchronize()
+                if graphed:
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph, stream=stream):
+                        cycle()
+                    with torch.cuda.stream(stream):
+                        ms = time_region(torch, stream, graph.replay, 3, 1) / nw
+                    del graph
+                else:
+                    with torch.cuda.stream(stream):
+                        ms = time_region(torch, stream, cycle, 1, 1) / nw
                 b = wb + 4 + M * K * 4 + K * 4 + M * N * 4
                 rows.append({"M": M, "K": K, "N": N, "us": ms * 1e3, "GBps": b / (ms * 1e-3) / 1e9,
                              "TOPS": 2.0 * M * N * K / (ms * 1e-3) / 1e12,
                              "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm,
-                             "tensor_frac": 2.0 * M * N * K / (ms * 1e-3) / 1e12 / bf16})
+                             "tensor_frac": 2.0 * M * N * K / (ms * 1e-3) / 1e12 / bf16,
+                             "weights_cycled": nw, "launch": "cuda graph" if graphed else "eager"})
                 del x, y
             del ws_list
             torch.cuda.empty_cache()

@@ -236,7 +236,7 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
   DeviceContext* ctx;
   if ((rc = device_context(&ctx))) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (decode_fused_supported(M, K)) {
+  if (decode_fused_supported(M, K) && !decode_split_preferred(M, K)) {
     DecodeJob j = {};
     j.x = x;
     j.g = norm_w;
@@ -248,7 +248,11 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
     return cuda_status(launch_decode(ctx, &j, 1, static_cast<int>(M), eps, true, false, s));
   }
   if (decode_supported(M, K)) {
-    // few tokens but long rows: int8 codes through the pool, then the decode kernel
+    // few tokens but long rows: int8 codes through the pool, then the decode
+    // kernel.  The norm kernel lets its dependent start only after the kernels
+    // before it have completed, and it writes no weights, so the decode kernel
+    // may stream its weights before its own dependency wait, overlapping the
+    // norm kernel.
     const size_t code_bytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
     uint8_t* ws = nullptr;
     if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + static_cast<size_t>(M) * 4, s)))
@@ -256,7 +260,7 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
     int8_t* codes = reinterpret_cast<int8_t*>(ws);
     float* as = reinterpret_cast<float*>(ws + code_bytes);
     cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, codes, nullptr, as, nullptr,
-                                         nullptr, false, s);
+                                         nullptr, true, s);
     if (e == cudaSuccess) {
       DecodeJob j = {};
       j.codes = codes;
@@ -266,7 +270,8 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
       j.K = static_cast<int>(K);
       j.N = static_cast<int>(N);
       j.y = y;
-      e = launch_decode(ctx, &j, 1, static_cast<int>(M), eps, false, false, s);
+      e = launch_decode(ctx, &j, 1, static_cast<int>(M), eps, false, true, s,
+                        static_cast<int>(rmsnorm_quant_ctas(M, static_cast<int>(K))));
     }
     pool_free(ws, s);
     return cuda_status(e);

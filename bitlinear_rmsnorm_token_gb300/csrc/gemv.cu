@@ -31,11 +31,18 @@
 namespace bitnet {
 namespace {
 
-constexpr int kDecWarps = 16;                      // compute warps
+constexpr int kDecWarps = 15;                      // compute warps (16 warps in all: 128 registers per thread)
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
 constexpr int kDecStageBytes = 24576;
 constexpr int kDecMaxStages = 6;  // ring depth is chosen per launch (3 or 6)
-constexpr int kDecRowAcc = 32;  // rows per stage when rows are long enough to need several warps (K >= 4096)
+// Long rows (K >= 4096, K a multiple of 2048): small stages of whole rows, each
+// consumed by one warp, up to kDecMaxSlots of them in the ring, filled by bulk
+// copies of about kDecLongCopyBytes (one copy per group of consecutive slots:
+// a bulk copy carries a fixed cost, and 4 KB copies reach only about half the
+// streaming rate of 16 KB ones).
+constexpr int kDecLongStageBytes = 8192;
+constexpr int kDecLongCopyBytes = 16384;
+constexpr int kDecMaxSlots = 64;
 
 struct DecodeProj {
   const float* x;
@@ -58,12 +65,13 @@ struct DecodeParams {
   int M;
   float eps;
   int weights_static;
-  int stages;  // weight ring depth (<= kDecMaxStages)
+  int stages;      // weight ring depth in 24 KB stages (short rows, <= kDecMaxStages)
+  int ring_bytes;  // weight ring size (long rows use it as kDecLongStageBytes-sized slots)
 };
 
 struct DecodeSmemTail {
-  uint64_t full[kDecMaxStages];
-  uint64_t empty[kDecMaxStages];
+  uint64_t full[kDecMaxSlots];
+  uint64_t empty[kDecMaxSlots];
   uint64_t in_full;  // activations (and norm weight) staged
   // per-row reductions, combined across warps with shared-memory atomics
   // (integer or max: the result does not depend on the order)
@@ -71,15 +79,22 @@ struct DecodeSmemTail {
   int sq_key[kDecodeMaxM];  // bit pattern of the row's largest |x|
   unsigned amax_bits[kDecodeMaxM];
   int rowsum[kDecodeMaxM];
-  int row_acc[kDecodeMaxM][kDecRowAcc];  // per-row sums when several warps share a row
   float rstd[kDecodeMaxM];
   float inv_a[kDecodeMaxM];
   int abort_flag;
 };
 
-// Shared-memory carve-up for one CTA: weight ring | x fp32 [M,K] (fused) or
-// the incoming int8 codes [M,K] (unfused) | g fp32 [K] (fused) | codes int8
-// [M,K] in slot-major order | tail.
+// Long rows up to K = 16384 with the norm fused in: every compute thread holds
+// its (at most 9) float4 groups of x and of the norm weight in registers, so
+// neither is staged in shared memory.
+__host__ __device__ inline bool register_prologue(bool fused, int K) {
+  return fused && K >= 4096 && K % 2048 == 0 && K <= 16384;
+}
+constexpr int kDecRegGroups = 9;  // float4 groups per thread: 16384 / 4 <= 9 * 480
+
+// Shared-memory carve-up for one CTA: weight ring | x fp32 [M,K] (fused and
+// staged) or the incoming int8 codes [M,K] (unfused) | g fp32 [K] (fused and
+// staged) | codes int8 [M,K] in slot-major order | tail.
 //
 // Slot-major codes: the 16-byte chunk c of a weight row (block c/2, bytes
 // 16(c&1)..+15) pairs, for slot s, with activation elements
@@ -88,10 +103,11 @@ struct DecodeSmemTail {
 // read consecutive 16-byte words (no bank conflicts).
 struct DecodeLayout {
   int xs, gs, xq, tail, total;
-  __host__ __device__ DecodeLayout(int M, int K, bool fused, int stages) {
-    xs = stages * kDecStageBytes;
-    gs = xs + (fused ? M * K * 4 : ((M * K + 127) & ~127));
-    xq = gs + (fused ? K * 4 : 0);
+  __host__ __device__ DecodeLayout(int M, int K, bool fused, int ring_bytes) {
+    const bool staged = fused && !register_prologue(fused, K);
+    xs = ring_bytes;
+    gs = xs + (staged ? M * K * 4 : (fused ? 0 : ((M * K + 127) & ~127)));
+    xq = gs + (staged ? K * 4 : 0);
     tail = xq + ((M * K + 127) & ~127);
     total = tail + static_cast<int>(sizeof(DecodeSmemTail));
   }
@@ -109,8 +125,11 @@ __device__ __forceinline__ void compute_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
 }
 
-template <int MT, bool kFused, bool kGrp>
-__global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ DecodeParams P, unsigned* err) {
+// Short rows and few tokens: registers for two CTAs per SM, so that the next
+// dependent launch can become resident while this one drains.  Long rows and
+// more tokens: one CTA per SM with up to 128 registers per thread.
+template <int MT, bool kFused, bool kLong>
+__global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_decode(const __grid_constant__ DecodeParams P, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
 
   // which projection this CTA serves
@@ -132,15 +151,29 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   int lpr = (cpr & 3) ? 2 : 4;
   while (lpr < 32 && cpr % (2 * lpr) == 0 && (r1 - r0) < kDecWarps * (32 / lpr)) lpr *= 2;
   const int rpp = 32 / lpr;  // rows per warp pass
-  // Long rows (cpr a multiple of 32, >= 64) use the row-group mapping of the
-  // main loop; otherwise whole warps take rows and a stage holds whole passes.
-  const bool grp = kGrp && cpr >= 64 && (cpr & 31) == 0;
-  int rps = kDecStageBytes / row_bytes;  // rows per stage (K <= 65536 keeps it >= 1)
-  if (!grp && rps >= kDecWarps * rpp) rps -= rps % (kDecWarps * rpp);
+  // Long rows (cpr a multiple of 32, >= 64): stages of whole rows, about 4 KB,
+  // one warp per stage.  Otherwise whole warps take rows and a 24 KB stage
+  // holds whole passes of all warps.
+  const bool lng = kLong && cpr >= 64 && (cpr & 31) == 0;
+  int rps, sbytes, nslots, grp;  // grp: consecutive slots filled by one copy
+  if (lng) {
+    rps = max(1, kDecLongStageBytes / row_bytes);
+    sbytes = rps * row_bytes;
+    grp = max(1, kDecLongCopyBytes / sbytes);
+    nslots = min(kDecMaxSlots, P.ring_bytes / sbytes);
+    grp = min(grp, nslots);
+    nslots -= nslots % grp;
+  } else {
+    rps = kDecStageBytes / row_bytes;  // rows per stage (K <= 65536 keeps it >= 1)
+    if (rps >= kDecWarps * rpp) rps -= rps % (kDecWarps * rpp);
+    sbytes = kDecStageBytes;
+    nslots = P.stages;
+    grp = 1;
+  }
   const int nst = (r1 - r0 + rps - 1) / rps;
+  const bool regp = kLong && register_prologue(kFused, K);  // implies lng
 
-  const int kDecStages = P.stages;
-  const DecodeLayout lay(M, K, kFused, kDecStages);
+  const DecodeLayout lay(M, K, kFused, P.ring_bytes);
   uint8_t* ring = smem;
   float* xs = reinterpret_cast<float*>(smem + lay.xs);
   float* gs = reinterpret_cast<float*>(smem + lay.gs);
@@ -150,9 +183,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kDecMaxStages; ++s) {
+    for (int s = 0; s < nslots; ++s) {
       mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], kDecWarps);
+      mbar_init(&tail->empty[s], lng ? 1 : kDecWarps);
     }
     mbar_init(&tail->in_full, 1);
     for (int m = 0; m < kDecodeMaxM; ++m) {
@@ -160,7 +193,6 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
       tail->sq_key[m] = 0;
       tail->amax_bits[m] = 0u;
       tail->rowsum[m] = 0;
-      for (int r = 0; r < kDecRowAcc; ++r) tail->row_acc[m][r] = 0;
     }
     tail->abort_flag = 0;
     fence_barrier_init();
@@ -173,41 +205,54 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
     if (lane == 0) {
       const uint8_t* src = pr.w + static_cast<int64_t>(r0) * row_bytes;
       const unsigned in_bytes = kFused ? static_cast<unsigned>((M + 1) * K * 4) : static_cast<unsigned>(M * K);
-      mbar_arrive_expect_tx(&tail->in_full, in_bytes);
-      const int first = min(nst, kDecStages);
-      auto issue = [&](int st) {
-        const int s = st % kDecStages;
-        const int rows = min(rps, r1 - r0 - st * rps);
+      if (!regp) mbar_arrive_expect_tx(&tail->in_full, in_bytes);
+      // Copy c fills stages c*grp .. c*grp + grp - 1 (slots of one group of the
+      // ring, completion counted on the group's first full barrier); it is
+      // issued once every slot of the group is free again.
+      const int ncopy = (nst + grp - 1) / grp;
+      const int first = min(ncopy, nslots / grp);
+      auto issue = [&](int c) {
+        const int st0 = c * grp;
+        const int s = st0 % nslots;
+        const int rows = min(grp * rps, r1 - r0 - st0 * rps);
         const unsigned bytes = static_cast<unsigned>(rows * row_bytes);
         mbar_arrive_expect_tx(&tail->full[s], bytes);
-        bulk_load(ring + s * kDecStageBytes, src + static_cast<int64_t>(st) * rps * row_bytes, bytes,
-                  &tail->full[s]);
+        bulk_load(ring + s * sbytes, src + static_cast<int64_t>(st0) * rps * row_bytes, bytes, &tail->full[s]);
       };
       // parameters (packed weights, norm weight) may be requested before the
-      // previous kernel has finished when the caller declared them static
+      // previous kernel has finished when they are known not to be written by
+      // it; the activations always after the wait, and ahead of the weights
+      // when those wait too, so that the prologue starts as early as possible
       if (P.weights_static) {
-        if (kFused) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
-        for (int st = 0; st < first; ++st) issue(st);
+        if (kFused && !regp) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
+        for (int c = 0; c < first; ++c) issue(c);
       }
       pdl_wait();
-      if (!P.weights_static) {
-        if (kFused) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
-        for (int st = 0; st < first; ++st) issue(st);
-      }
-      if (kFused)
-        bulk_load(xs, pr.x, static_cast<unsigned>(M * K * 4), &tail->in_full);
-      else
+      if (kFused) {
+        if (!regp) {
+          if (!P.weights_static) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
+          bulk_load(xs, pr.x, static_cast<unsigned>(M * K * 4), &tail->in_full);
+        }
+      } else {
         bulk_load(xs, pr.codes, static_cast<unsigned>(M * K), &tail->in_full);
+      }
+      if (!P.weights_static)
+        for (int c = 0; c < first; ++c) issue(c);
       int issued = first;
-      for (int st = first; st < nst; ++st) {
-        if (!mbar_wait(&tail->empty[st % kDecStages], ((st / kDecStages) - 1) & 1, err, &tail->abort_flag)) break;
-        issue(st);
-        issued = st + 1;
+      for (int c = first; c < ncopy; ++c) {
+        bool ok = true;
+        for (int j = 0; j < grp && ok; ++j) {
+          const int st = c * grp + j - nslots;  // the stage this slot held one lap earlier
+          ok = mbar_wait(&tail->empty[st % nslots], (st / nslots) & 1, err, &tail->abort_flag);
+        }
+        if (!ok) break;
+        issue(c);
+        issued = c + 1;
       }
       // leave no copy in flight when the CTA retires
-      mbar_wait(&tail->in_full, 0, err, nullptr);
-      for (int st = max(0, issued - kDecStages); st < issued; ++st)
-        mbar_wait(&tail->full[st % kDecStages], (st / kDecStages) & 1, err, nullptr);
+      if (!regp) mbar_wait(&tail->in_full, 0, err, nullptr);
+      for (int c = max(0, issued - nslots / grp); c < issued; ++c)
+        mbar_wait(&tail->full[(c * grp) % nslots], ((c * grp) / nslots) & 1, err, nullptr);
     }
     return;
   }
@@ -221,6 +266,79 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   const int total = M * G;
   const int m_start = tid / G;
   const int g_start = tid - m_start * G;
+  if (kFused && kLong && regp) {
+    // register prologue: row by row, x and the norm weight straight from
+    // global memory into registers, the same order-free reductions as below
+    // through shared-memory atomics.  Thread tid holds the float4 groups
+    // (tid + 480 i + rot) mod G: every CTA reads the same x and norm weight,
+    // and the CTA-dependent rotation spreads their simultaneous requests over
+    // the L2 instead of sending all of them to the same lines at once.
+    const float4* g4 = reinterpret_cast<const float4*>(pr.g);
+    const int rot = (static_cast<int>(blockIdx.x) * 32) % G;
+    auto gidx = [&](int i) {
+      const int j = tid + kThr * i + rot;
+      return j < G ? j : j - G;  // valid when tid + 480 i < G
+    };
+    const int nv = (G - tid + kThr - 1) / kThr;  // groups of this thread (>= 2)
+    float4 gv[kDecRegGroups];
+    auto load_g = [&]() {
+#pragma unroll
+      for (int i = 0; i < kDecRegGroups; ++i)
+        gv[i] = i < nv ? __ldg(g4 + gidx(i)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    };
+    if (P.weights_static) load_g();
+    pdl_wait();  // x (and y) belong to the previous kernel's stream order
+    if (!P.weights_static) load_g();
+#pragma unroll 1
+    for (int m = 0; m < M; ++m) {
+      const float4* x4 = reinterpret_cast<const float4*>(pr.x) + static_cast<int64_t>(m) * G;
+      float4 v[kDecRegGroups];
+      int key = 0;
+#pragma unroll
+      for (int i = 0; i < kDecRegGroups; ++i) {
+        v[i] = i < nv ? __ldg(x4 + gidx(i)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        key = max(key, sq_key4(v[i]));
+      }
+      key = warp_max_int(key);
+      if (lane == 0 && key) atomicMax(&tail->sq_key[m], key);
+      compute_bar();
+      key = tail->sq_key[m];
+      const float scale = sq_scale(key);
+      SqPartial part = {0ull, 0u};
+#pragma unroll
+      for (int i = 0; i < kDecRegGroups; ++i)
+        if (i < nv) sq_add4(part, v[i], scale);
+      const unsigned long long w = warp_sum_u64(sq_fold(part, 4 * nv));
+      if (lane == 0 && w) atomicAdd(&tail->ss[m], w);
+      compute_bar();
+      const float rstd = rstd_from_fixed(tail->ss[m], key, K, P.eps);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kDecRegGroups; ++i) {
+        if (i < nv) {
+          v[i] = make_float4(norm_elem(v[i].x, rstd, gv[i].x), norm_elem(v[i].y, rstd, gv[i].y),
+                             norm_elem(v[i].z, rstd, gv[i].z), norm_elem(v[i].w, rstd, gv[i].w));
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+        }
+      }
+      amax = warp_max(amax);
+      if (lane == 0) atomicMax(&tail->amax_bits[m], __float_as_uint(amax));
+      compute_bar();
+      const float as = act_scale_from_amax(__uint_as_float(tail->amax_bits[m]));
+      int rs = 0;
+#pragma unroll
+      for (int i = 0; i < kDecRegGroups; ++i) {
+        if (i < nv) {
+          const uint32_t pk = quant_pack4_i8(v[i], as);
+          *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(4 * gidx(i), cpr)) = pk;
+          rs = __dp4a(static_cast<int>(pk), 0x01010101, rs);
+        }
+      }
+      rs = warp_sum_int(rs);
+      if (lane == 0 && rs) atomicAdd(&tail->rowsum[m], rs);
+      if (tid == 0) tail->inv_a[m] = __frcp_rn(as);
+    }
+  } else {
   if (!mbar_wait(&tail->in_full, 0, err, &tail->abort_flag)) return;
   // Prologue loops run over all (row, float4 group) pairs of the M x K block in
   // one flat, non-unrolled loop; K/4 is a multiple of 32, so the 32 lanes of a
@@ -357,6 +475,7 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
     }
     if (tid < M) tail->inv_a[tid] = __frcp_rn(__ldg(pr.a_scale + tid));
   }
+  }
   compute_bar();
   // Writing y needs the previous kernel finished: on the unfused path this
   // thread waited above; on the fused path the activations arrived by a copy the
@@ -378,91 +497,98 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   }
   const float inv_w = pr.inv_w;
   const int slot_stride = cpr << 4;
-  // long-row mapping (see the stage loop): groups of cpr threads, one row each
-  const int n_grp = cpr >= kDecWarps * 32 ? 1 : (kDecWarps * 32) / cpr;
-  const int g_row = cpr >= kDecWarps * 32 ? 0 : tid / cpr;
-  const bool g_on = g_row < n_grp;
-  const int own_c = cpr >= kDecWarps * 32 ? tid : tid % cpr;
-  const int n_own = cpr > kDecWarps * 32 ? cpr / (kDecWarps * 32) : 1;  // <= 2 (K <= 65536)
-  int4 xr1[2][4];  // M == 1: this thread's activation codes, kept in registers
-  if (kGrp && MT == 1 && grp && g_on) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int sl = 0; sl < 4; ++sl)
-        xr1[j][sl] = j < n_own ? *reinterpret_cast<const int4*>(xq + ((own_c + 512 * j) << 4) + sl * slot_stride)
-                               : make_int4(0, 0, 0, 0);
-  }
 
-  for (int st = 0; st < nst; ++st) {
-    const int s = st % kDecStages;
-    if (!mbar_wait(&tail->full[s], (st / kDecStages) & 1, err, &tail->abort_flag)) break;
-    const uint8_t* stage = ring + s * kDecStageBytes;
-    const int rows = min(rps, r1 - r0 - st * rps);
-    if (kGrp && grp) {
-      // long rows, cpr a multiple of 32: thread t owns chunk positions
-      // t % cpr (+ 512 j when cpr > 512) for the rows r = t / cpr (mod G) of
-      // the stage; warps never straddle rows, one redux + one shared atomic per
-      // warp and row combine the partial sums
-      for (int r = g_on ? g_row : rows; r < rows; r += n_grp) {
+  if (kLong && lng) {
+    // Long rows: warp w takes the stages in ring slots w, w + 15, ...; lane l takes the 16-byte
+    // chunks l, l + 32, ... of each row, so a warp reads 512 consecutive bytes
+    // of weights and of each slot's activation codes per step (no bank
+    // conflicts), and one redux per row and token finishes the dot product.
+    // With one token the codes of the first 128 chunk positions stay in
+    // registers for the whole stream.
+    const int npos = cpr >> 5;
+    int4 xr[4][4];
+    if (MT == 1) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl)
+          xr[i][sl] = i < npos ? *reinterpret_cast<const int4*>(xq + ((lane + 32 * i) << 4) + sl * slot_stride)
+                               : make_int4(0, 0, 0, 0);
+    }
+    // Slot s belongs to warp s % 15, which consumes every use of it in order:
+    // a parity wait must never be posted for a phase two ahead of the slot's.
+    for (int st = warp < nslots ? warp : nst; st < nst; st += (st % nslots) + kDecWarps < nslots ? kDecWarps
+                                                                           : nslots - (st % nslots) + warp) {
+      const int s = st % nslots;
+      if (!mbar_wait(&tail->full[s - s % grp], (st / nslots) & 1, err, &tail->abort_flag)) break;
+      const uint8_t* stage = ring + s * sbytes;
+      const int rows = min(rps, r1 - r0 - st * rps);
+      for (int r = 0; r < rows; ++r) {
         const uint8_t* wrow = stage + r * row_bytes;
         int acc[MT][4];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc[m][q] = 0;
-        if (g_on) {
+        auto chunk = [&](int c, const int4(&xreg)[4], bool from_regs) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(wrow + c * 16);
+          const unsigned wd[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (j < n_own) {
-              const int c = own_c + 512 * j;
-              const uint4 wv = *reinterpret_cast<const uint4*>(wrow + c * 16);
-              const unsigned wd[4] = {wv.x, wv.y, wv.z, wv.w};
+          for (int sl = 0; sl < 4; ++sl) {
+            const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
+            const unsigned m0 = wd[0] & mask, m1 = wd[1] & mask, m2 = wd[2] & mask, m3 = wd[3] & mask;
 #pragma unroll
-              for (int sl = 0; sl < 4; ++sl) {
-                const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
-                const unsigned m0 = wd[0] & mask, m1 = wd[1] & mask, m2 = wd[2] & mask, m3 = wd[3] & mask;
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                  if (m < M) {
-                    const int4 xv = MT == 1 ? xr1[j][sl]
-                                            : *reinterpret_cast<const int4*>(xq + (c << 4) + m * K + sl * slot_stride);
-                    int a = acc[m][sl];
-                    a = dp4a_us(m0, xv.x, a);
-                    a = dp4a_us(m1, xv.y, a);
-                    a = dp4a_us(m2, xv.z, a);
-                    a = dp4a_us(m3, xv.w, a);
-                    acc[m][sl] = a;
-                  }
-                }
+            for (int m = 0; m < MT; ++m) {
+              if (m < M) {
+                const int4 xv =
+                    from_regs ? xreg[sl] : *reinterpret_cast<const int4*>(xq + (c << 4) + m * K + sl * slot_stride);
+                int a = acc[m][sl];
+                a = dp4a_us(m0, xv.x, a);
+                a = dp4a_us(m1, xv.y, a);
+                a = dp4a_us(m2, xv.z, a);
+                a = dp4a_us(m3, xv.w, a);
+                acc[m][sl] = a;
               }
             }
           }
+        };
+        if (MT == 1) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < npos) chunk(lane + 32 * i, xr[i], true);
+#pragma unroll 1
+          for (int i = 4; i < npos; ++i) chunk(lane + 32 * i, xr[0], false);
+        } else {
+#pragma unroll 1
+          for (int i = 0; i < npos; ++i) chunk(lane + 32 * i, xr[0], false);
         }
+        const int n = r0 + st * rps + r;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           if (m < M) {
             const int t = warp_sum_int((acc[m][0] >> 6) + (acc[m][1] >> 4) + (acc[m][2] >> 2) + acc[m][3]);
-            if (g_on && lane == 0 && t) atomicAdd(&tail->row_acc[m][r], t);
+            if (lane == 0) {
+              const int a = t - rowsum[m];
+              pr.y[static_cast<int64_t>(m) * N + n] = rescale_elem(__int2float_rn(a), inv_a[m], inv_w);
+              if (pr.acc_out) pr.acc_out[static_cast<int64_t>(m) * N + n] = a;
+            }
           }
         }
       }
+      // the stage's loads are complete (their values fed the dot products);
+      // order them before the producer's next bulk copy into the slot
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->empty[s]);
-      compute_bar();
-      for (int idx = tid; idx < rows * M; idx += kDecWarps * 32) {
-        const int m = idx / rows;
-        const int r = idx - m * rows;
-        const int a = tail->row_acc[m][r] - tail->rowsum[m];
-        tail->row_acc[m][r] = 0;
-        const int n = r0 + st * rps + r;
-        pr.y[static_cast<int64_t>(m) * N + n] = rescale_elem(__int2float_rn(a), tail->inv_a[m], inv_w);
-        if (pr.acc_out) pr.acc_out[static_cast<int64_t>(m) * N + n] = a;
-      }
-      compute_bar();
-      continue;
     }
+    return;
+  }
+
+  for (int st = 0; st < nst; ++st) {
+    const int s = st % nslots;
+    if (!mbar_wait(&tail->full[s], (st / nslots) & 1, err, &tail->abort_flag)) break;
+    const uint8_t* stage = ring + s * sbytes;
+    const int rows = min(rps, r1 - r0 - st * rps);
     for (int base = warp * rpp; base < rows; base += kDecWarps * rpp) {
       const int r = base + lane / lpr;
       const bool valid = r < rows;
@@ -521,9 +647,9 @@ __global__ void __launch_bounds__(kDecThreads) k_decode(const __grid_constant__ 
   }
 }
 
-template <int MT, bool kFused, bool kGrp>
+template <int MT, bool kFused, bool kLong>
 cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err, cudaStream_t s) {
-  auto kern = k_decode<MT, kFused, kGrp>;
+  auto kern = k_decode<MT, kFused, kLong>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -539,14 +665,14 @@ cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool p
   return cudaLaunchKernelEx(&cfg, kern, P, err);
 }
 
-template <bool kFused, bool kGrp>
+template <bool kFused, bool kLong>
 cudaError_t dispatch_m(int mt, const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err,
                        cudaStream_t s) {
   switch (mt) {
-    case 1: return launch_decode_t<1, kFused, kGrp>(P, grid, smem, pdl, err, s);
-    case 2: return launch_decode_t<2, kFused, kGrp>(P, grid, smem, pdl, err, s);
-    case 4: return launch_decode_t<4, kFused, kGrp>(P, grid, smem, pdl, err, s);
-    default: return launch_decode_t<8, kFused, kGrp>(P, grid, smem, pdl, err, s);
+    case 1: return launch_decode_t<1, kFused, kLong>(P, grid, smem, pdl, err, s);
+    case 2: return launch_decode_t<2, kFused, kLong>(P, grid, smem, pdl, err, s);
+    case 4: return launch_decode_t<4, kFused, kLong>(P, grid, smem, pdl, err, s);
+    default: return launch_decode_t<8, kFused, kLong>(P, grid, smem, pdl, err, s);
   }
 }
 
@@ -556,12 +682,18 @@ bool decode_supported(int64_t M, int64_t K) {
   return M >= 1 && M <= kDecodeMaxM && M * K <= kDecodeMaxCodeBytes;
 }
 
+bool decode_split_preferred(int64_t M, int64_t K) {
+  return decode_supported(M, K) && K > 16384 && K % 2048 == 0;
+}
+
 bool decode_fused_supported(int64_t M, int64_t K) {
-  return M >= 1 && M <= kDecodeMaxM && 5 * M * K + 4 * K <= kDecodeFusedMaxStageBytes;
+  if (M < 1 || M > kDecodeMaxM) return false;
+  if (K <= 16384 && register_prologue(true, static_cast<int>(K))) return decode_supported(M, K);
+  return 5 * M * K + 4 * K <= kDecodeFusedMaxStageBytes;
 }
 
 cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
-                          bool weights_static, cudaStream_t s) {
+                          bool weights_static, cudaStream_t s, int reserve_sms) {
   DecodeParams P = {};
   P.nproj = njobs;
   P.M = M;
@@ -576,7 +708,8 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
   // One CTA per SM in total (never a second wave, and room for the next
   // dependent launch to become resident early), apportioned to the
   // projections by weight bytes with the largest-remainder rule.
-  int target = ctx->num_sms > njobs ? ctx->num_sms : njobs;
+  const int avail = ctx->num_sms - reserve_sms;
+  int target = avail > njobs ? avail : njobs;
   int want[BITNET_MAX_GROUP];
   double frac[BITNET_MAX_GROUP];
   int used = 0;
@@ -618,25 +751,46 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
     cta += n_ctas;
   }
   const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
-  // Ring depth: three stages when no CTA streams more than three of them (the
-  // latency-bound case: small enough for two CTAs per SM, so the next
+  // Short rows: three 24 KB stages when no CTA streams more than three of them
+  // (the latency-bound case: small enough for two CTAs per SM, so the next
   // dependent launch can become resident early), six for long streams (more
-  // bytes in flight per SM) when shared memory allows.
-  bool grp = false;
+  // bytes in flight per SM) when shared memory allows.  Long rows: all the
+  // shared memory left after the activations, as 4 KB (or one-row) slots.
+  bool lng = false;
   int max_stages = 1;
   for (int i = 0; i < njobs; ++i) {
     const int cpr = jobs[i].K / 64;
-    if (cpr >= 64 && cpr % 32 == 0) grp = true;
+    if (cpr >= 64 && cpr % 32 == 0) lng = true;
     const int rps = kDecStageBytes / (jobs[i].K / 4);
     const int nst = (P.p[i].rows_per_cta + rps - 1) / rps;
     max_stages = nst > max_stages ? nst : max_stages;
   }
+  constexpr int kSmemMax = 227 * 1024;
+  // the projections' layouts differ (staged or register prologue): size for the largest
+  auto layout_total = [&](int ring) {
+    int t = 0;
+    for (int i = 0; i < njobs; ++i) {
+      const int v = DecodeLayout(M, jobs[i].K, fused, ring).total;
+      t = v > t ? v : t;
+    }
+    return t;
+  };
   P.stages = 3;
-  if (max_stages > 3 && DecodeLayout(M, maxK, fused, kDecMaxStages).total <= 227 * 1024) P.stages = kDecMaxStages;
-  const size_t smem = static_cast<size_t>(DecodeLayout(M, maxK, fused, P.stages).total);
-  if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;  // unreachable with the dispatch limits
-  const bool pdl = true;  // without BITNET_FLAG_WEIGHTS_STATIC every read waits for the previous kernel
-  if (grp)
+  if (max_stages > 3 && layout_total(kDecMaxStages * kDecStageBytes) <= kSmemMax) P.stages = kDecMaxStages;
+  P.ring_bytes = P.stages * kDecStageBytes;
+  if (lng) {
+    const int other = layout_total(0);
+    int ring = (kSmemMax - other) & ~1023;
+    ring = ring < kDecMaxSlots * kDecLongStageBytes ? ring : kDecMaxSlots * kDecLongStageBytes;
+    // never smaller than the short-row ring of the same launch, and room for
+    // at least two slots of the longest row
+    const int min_ring = maxK / 4 * 2 > P.ring_bytes ? maxK / 4 * 2 : P.ring_bytes;
+    P.ring_bytes = ring > min_ring ? ring : min_ring;
+  }
+  const size_t smem = static_cast<size_t>(layout_total(P.ring_bytes));
+  if (smem > static_cast<size_t>(kSmemMax)) return cudaErrorInvalidConfiguration;  // unreachable with the dispatch limits
+  const bool pdl = true;  // without prefetch permission every read waits for the previous kernel
+  if (lng)
     return fused ? dispatch_m<true, true>(mt, P, cta, smem, pdl, ctx->err_word, s)
                  : dispatch_m<false, true>(mt, P, cta, smem, pdl, ctx->err_word, s);
   return fused ? dispatch_m<true, false>(mt, P, cta, smem, pdl, ctx->err_word, s)

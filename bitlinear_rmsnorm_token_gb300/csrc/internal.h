@@ -47,6 +47,8 @@ cudaError_t launch_unpack_i2s(const uint8_t* packed, int64_t N, int64_t K, int8_
 
 // RMSNorm + absmax int8 quantisation, one warp per row.  Exactly one of
 // codes_i8 / codes_f16 is non-null.
+// CTAs of the norm + quant launch for M rows of K.
+int64_t rmsnorm_quant_ctas(int64_t M, int K);
 cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int K, float eps, int8_t* codes_i8,
                                  __half* codes_f16, float* a_scale, int32_t* rowsum, float* xn_out,
                                  bool pdl, cudaStream_t s);
@@ -75,8 +77,15 @@ struct DecodeJob {
 };
 bool decode_supported(int64_t M, int64_t K);        // codes given (int8 in global memory)
 bool decode_fused_supported(int64_t M, int64_t K);  // norm + quant in the same launch
+// Few tokens with long rows (K >= 8192, a multiple of 2048): a separate norm
+// kernel with one CTA per row, then the decode kernel streaming weights
+// during it, beats every CTA normalising the whole row in its prologue.
+bool decode_split_preferred(int64_t M, int64_t K);
+// reserve_sms: SMs left to the kernel this launch follows (its CTAs still
+// running when the decode CTAs start), so that every decode CTA is resident at
+// once.
 cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
-                          bool weights_static, cudaStream_t s);
+                          bool weights_static, cudaStream_t s, int reserve_sms = 0);
 
 // Tensor-core (tcgen05) contraction on fp16 codes.
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,

@@ -67,7 +67,7 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   if (K < BITNET_I2S_BLOCK || K % BITNET_I2S_BLOCK != 0 || K > BITNET_MAX_K) return BITNET_ERR_UNSUPPORTED_SHAPE;
   if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 31) - 1) return BITNET_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y)) return BITNET_ERR_MISALIGNED;
-  const bool fused = decode_fused_supported(M, K);
+  const bool fused = decode_fused_supported(M, K) && !decode_split_preferred(M, K);
   const bool decode = decode_supported(M, K);
   // scratch layout: codes [M, K] (int8 for the decode kernel, fp16 for the
   // tensor-core kernel), then fp32 scales [M], 256-byte aligned
@@ -99,8 +99,10 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   // before the contraction reads it, so nothing has to be cleared first
   if (decode) {
     int8_t* codes = static_cast<int8_t*>(scratch);
+    // the norm kernel lets the decode kernel start only after the kernels
+    // before it have completed, so the weights may be streamed early
     cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, codes, nullptr, as, nullptr,
-                                         nullptr, false, s);
+                                         nullptr, true, s);
     if (e == cudaSuccess) {
       DecodeJob j = {};
       j.codes = codes;
@@ -110,7 +112,8 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
       j.K = static_cast<int>(K);
       j.N = static_cast<int>(N);
       j.y = y;
-      e = launch_decode(ctx, &j, 1, static_cast<int>(M), eps, false, false, s);
+      e = launch_decode(ctx, &j, 1, static_cast<int>(M), eps, false, true, s,
+                        static_cast<int>(rmsnorm_quant_ctas(M, static_cast<int>(K))));
     }
     return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
   }

@@ -47,8 +47,11 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
                                                                  float* __restrict__ a_scale,
                                                                  int32_t* __restrict__ rowsum,
                                                                  float* __restrict__ xn_out) {
-  pdl_launch_dependents();
+  // dependents may start only once the kernels before this one have completed
+  // (they may then read any input this kernel does not write before their own
+  // wait)
   pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kNqWarps + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -123,6 +126,94 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
   }
 }
 
+// Long rows (K a multiple of 2048 above 3072): one CTA per row, block-wide
+// reductions through shared-memory atomics (integer and max: order-free).
+// kRegs: K <= 16384, K/16 threads each holding 16 elements in registers
+// (float4 groups t, t+T, t+2T, t+3T of the row: every load instruction of a
+// warp is coalesced).  Otherwise 1024 threads loop over the row's float4 groups
+// with the same stride and read the row again from L2 in every pass.
+template <typename OutT, bool kRegs>
+__global__ void __launch_bounds__(1024) k_rmsnorm_quant_rows(const float* __restrict__ x,
+                                                             const float* __restrict__ g, int K, float eps,
+                                                             OutT* __restrict__ codes, float* __restrict__ a_scale,
+                                                             int32_t* __restrict__ rowsum,
+                                                             float* __restrict__ xn_out) {
+  constexpr int kV = 4;  // float4 groups per thread held in registers (kRegs)
+  __shared__ int s_key;
+  __shared__ unsigned long long s_ss;
+  __shared__ unsigned s_amax;
+  __shared__ int s_rs;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int T = blockDim.x;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int64_t row = blockIdx.x;
+  // float4 groups of this thread: tid + T i for i < nv (exactly kV when kRegs)
+  const int nv = kRegs ? kV : ((K >> 2) - tid + T - 1) / T;
+  if (tid == 0) {
+    s_key = 0;
+    s_ss = 0ull;
+    s_amax = 0u;
+    s_rs = 0;
+  }
+  const float4* xr = reinterpret_cast<const float4*>(x + row * K);
+  const float4* gr = reinterpret_cast<const float4*>(g);
+  float4 v[kV];
+  if (kRegs) {
+#pragma unroll
+    for (int i = 0; i < kV; ++i) v[i] = __ldg(xr + tid + T * i);
+  }
+  auto xv = [&](int i) { return kRegs ? v[i] : __ldg(xr + tid + T * i); };
+  __syncthreads();
+  int key = 0;
+#pragma unroll 4
+  for (int i = 0; i < nv; ++i) key = max(key, sq_key4(xv(i)));
+  key = warp_max_int(key);
+  if (lane == 0 && key) atomicMax(&s_key, key);
+  __syncthreads();
+  key = s_key;
+  const float scale = sq_scale(key);
+  SqPartial part = {0ull, 0u};
+#pragma unroll 4
+  for (int i = 0; i < nv; ++i) sq_add4(part, xv(i), scale);
+  const unsigned long long w = warp_sum_u64(sq_fold(part, 4 * nv));
+  if (lane == 0 && w) atomicAdd(&s_ss, w);
+  __syncthreads();
+  const float rstd = rstd_from_fixed(s_ss, key, K, eps);
+  auto norm4 = [&](float4 a, float4 gv) {
+    return make_float4(norm_elem(a.x, rstd, gv.x), norm_elem(a.y, rstd, gv.y), norm_elem(a.z, rstd, gv.z),
+                       norm_elem(a.w, rstd, gv.w));
+  };
+  float amax = 0.0f;
+#pragma unroll 4
+  for (int i = 0; i < nv; ++i) {
+    const float4 n = norm4(xv(i), __ldg(gr + tid + T * i));
+    if (kRegs) v[i] = n;
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(n.x), fabsf(n.y)), fmaxf(fabsf(n.z), fabsf(n.w))));
+    if (xn_out) reinterpret_cast<float4*>(xn_out + row * K)[tid + T * i] = n;
+  }
+  amax = warp_max(amax);
+  if (lane == 0) atomicMax(&s_amax, __float_as_uint(amax));
+  __syncthreads();
+  const float as = act_scale_from_amax(__uint_as_float(s_amax));
+  int rs = 0;
+#pragma unroll 4
+  for (int i = 0; i < nv; ++i) {
+    const float4 n = kRegs ? v[i] : norm4(__ldg(xr + tid + T * i), __ldg(gr + tid + T * i));
+    store_codes4<OutT>(codes + row * K + 4 * (tid + T * i), n, as, rs);
+  }
+  if (rowsum) {
+    rs = warp_sum_int(rs);
+    if (lane == 0 && rs) atomicAdd(&s_rs, rs);
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a_scale[row] = as;
+    if (rowsum) rowsum[row] = s_rs;
+  }
+}
+
 __global__ void __launch_bounds__(256) k_codes_to_f16(const int8_t* __restrict__ in, __half* __restrict__ out,
                                                       int64_t n4) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -155,9 +246,28 @@ cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float ep
 }
 
 template <typename OutT>
+cudaError_t launch_nq_rows(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
+                           int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  const bool regs = K <= 16384;
+  cfg.gridDim = dim3(static_cast<unsigned>(M));
+  cfg.blockDim = dim3(static_cast<unsigned>(regs ? K / 16 : 1024));
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (regs) return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant_rows<OutT, true>, x, g, K, eps, codes, a_scale, rowsum, xn_out);
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant_rows<OutT, false>, x, g, K, eps, codes, a_scale, rowsum, xn_out);
+}
+
+template <typename OutT>
 cudaError_t launch_nq_k(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
                         int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
   const int nc = K >> 7;
+  if (nc > 24 && K % 2048 == 0 && M < (int64_t(1) << 31))  // keep in step with rmsnorm_quant_ctas
+    return launch_nq_rows<OutT>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
   switch (nc) {  // the model widths of the prefill shapes: K = 640, 1024, 2048, 3072
     case 5: return launch_nq<OutT, 5, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
     case 8: return launch_nq<OutT, 8, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
@@ -171,6 +281,12 @@ cudaError_t launch_nq_k(const float* x, const float* g, int64_t M, int K, float 
 }
 
 }  // namespace
+
+int64_t rmsnorm_quant_ctas(int64_t M, int K) {
+  const int nc = K >> 7;
+  if (nc > 24 && K % 2048 == 0) return M;  // one CTA per row
+  return (M + kNqWarps - 1) / kNqWarps;
+}
 
 cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int K, float eps, int8_t* codes_i8,
                                  __half* codes_f16, float* a_scale, int32_t* rowsum, float* xn_out, bool pdl,

@@ -163,8 +163,11 @@ typedef struct {
  * and norm weight).  Each output equals bitnet_bitlinear_forward of that
  * projection, bit for bit.  `projs` is a HOST array of `count` descriptors
  * (1..BITNET_MAX_GROUP), read before the call returns.  Supported for
- * M <= 8 and 5*M*K + 4*K <= 147456 (activations, codes and norm weight staged
- * in shared memory); other shapes return BITNET_ERR_UNSUPPORTED_SHAPE.
+ * M <= 8 with, for every projection, either 5*M*K + 4*K <= 147456
+ * (activations, codes and norm weight staged in shared memory) or K a multiple
+ * of 2048 in [4096, 16384] with M*K <= 65536 (activations and norm weight held
+ * in registers, codes in shared memory); other shapes return
+ * BITNET_ERR_UNSUPPORTED_SHAPE.
  * flags: 0 or BITNET_FLAG_WEIGHTS_STATIC. */
 BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M,
                                    float eps, uint32_t flags, bitnet_stream_t stream);
@@ -180,8 +183,9 @@ BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, in
  *   - Temporary data (fp16 activation codes and per-token scales, 2*M*K + 4*M
  *     bytes, rounded up) lives in one fixed 16 MiB device array that every GPU
  *     using the library keeps until the process exits.  Larger problems return
- *     BITNET_ERR_SCRATCH_LIMIT without launching anything; M <= 8 with
- *     5*M*K + 4*K <= 147456 needs no scratch at all (one fused launch).
+ *     BITNET_ERR_SCRATCH_LIMIT without launching anything; the shapes that
+ *     bitnet_bitlinear_forward_group accepts (M <= 8, see there) need no
+ *     scratch at all (one fused launch).
  *   - The first call on each device does one-time set-up (device properties and
  *     the array's device address); make that first call before any stream
  *     capture.

@@ -100,7 +100,7 @@ def _x_with_edges(M, K, seed):
     return x
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (5, 640), (33, 1024), (9, 2048), (4, 1152), (17, 3072), (3, 16384), (2, 65536)])
+@pytest.mark.parametrize("M,K", [(1, 128), (5, 640), (33, 1024), (9, 2048), (4, 1152), (17, 3072), (7, 4096), (2, 5120), (3, 16384), (2, 18432), (2, 65536)])
 def test_rmsnorm_quant_matches_oracle(oracle_mod, M, K):
     x = _x_with_edges(M, K, seed=M * 31 + K)
     g = wl.gen_norm_w(K, seed=K)
@@ -277,12 +277,18 @@ def test_accumulator_exactness_extremes(oracle_mod, M, K):
 # ---------------------------------------------------------------- forward
 
 FWD_CASES = [
-    # fused decode launch (M <= 8, 5*M*K + 4*K <= 160 KiB)
-    (1, 128, 1), (1, 1024, 2048), (3, 2048, 1024), (8, 1024, 2048), (8, 3072, 100), (1, 16384, 96),
-    # long rows, several warps per row, weight ring wrapping (27 rows per CTA)
-    (1, 16384, 4096), (1, 8192, 3000),
-    # norm launch + decode launch on int8 codes (M <= 8, M*K <= 65536)
-    (3, 16384, 300), (8, 8192, 64), (2, 32768, 40), (2, 16384, 4096),
+    # fused decode launch, activations staged in shared memory (M <= 8, 5*M*K + 4*K <= 144 KiB)
+    (1, 128, 1), (1, 1024, 2048), (3, 2048, 1024), (8, 1024, 2048), (8, 3072, 100), (1, 10240 - 128, 96),
+    # fused decode launch, long rows (K a multiple of 2048 in [4096, 16384]): activations
+    # and norm weight in registers, one warp per 8 KB stage of whole rows
+    (1, 4096, 4096), (5, 4096, 333), (1, 16384, 4096), (1, 8192, 3000), (4, 8192, 777),
+    (3, 16384, 300), (8, 8192, 64), (2, 16384, 4096),
+    # longer rows: row-per-CTA norm launch, then the decode launch streaming its
+    # weight ring during it
+    (1, 65536, 300), (2, 32768, 40),
+    # ring slots reused many times, slot counts not a multiple of the 15 consumer
+    # warps (28 slots of 8 KB at K=4096; 6 slots of one 16 KB row at K=65536)
+    (1, 4096, 65536), (1, 65536, 4096), (2, 8192, 20000),
     # norm launch + tensor-core launch
     (16, 640, 256), (64, 1024, 2048), (257, 3072, 1024), (1000, 640, 130), (2048, 2048, 384), (40, 8192, 256)]
 
