@@ -216,12 +216,19 @@ int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* 
     j.acc_out = acc_out;
     return cuda_status(launch_decode(ctx, &j, 1, static_cast<int>(M), 0.0f, false, false, s));
   }
-  __half* f16 = nullptr;
-  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&f16), static_cast<size_t>(M * K) * 2, s))) return rc;
+  const bool skinny = gemm_skinny_supported(M, K, N);
+  const size_t code_bytes = (static_cast<size_t>(M * K) * 2 + 255) & ~size_t(255);
+  const size_t gws_bytes = skinny ? gemm_skinny_workspace(ctx, M, K, N) : 0;
+  uint8_t* buf = nullptr;
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&buf), code_bytes + gws_bytes, s))) return rc;
+  __half* f16 = reinterpret_cast<__half*>(buf);
   cudaError_t e = launch_codes_to_f16(a_codes, f16, M * K, s);
   int st = BITNET_OK;
-  if (e == cudaSuccess) e = launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, true, s, &st);
-  pool_free(f16, s);
+  if (e == cudaSuccess)
+    e = skinny ? launch_gemm_skinny(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, buf + code_bytes,
+                                    false, true, s, &st)
+               : launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, true, s, &st);
+  pool_free(buf, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);
 }
@@ -276,16 +283,25 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
     pool_free(ws, s);
     return cuda_status(e);
   }
-  // norm + quant to fp16 codes, then the tensor-core contraction
+  // norm + quant to fp16 codes, then the tensor-core contraction (the split-K
+  // form for up to 128 tokens, its workspace zeroed ahead of the norm launch so
+  // that the two kernels stay chained by programmatic dependent launch)
+  const bool skinny = gemm_skinny_supported(M, K, N);
   const size_t code_bytes = (static_cast<size_t>(M * K) * 2 + 255) & ~size_t(255);
+  const size_t scale_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
+  const size_t gws_bytes = skinny ? gemm_skinny_workspace(ctx, M, K, N) : 0;
   uint8_t* ws = nullptr;
-  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + static_cast<size_t>(M) * 4, s))) return rc;
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + scale_bytes + gws_bytes, s))) return rc;
   __half* f16 = reinterpret_cast<__half*>(ws);
   float* as = reinterpret_cast<float*>(ws + code_bytes);
-  cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr,
-                                       false, s);
+  uint8_t* gws = ws + code_bytes + scale_bytes;
+  cudaError_t e = gws_bytes ? cudaMemsetAsync(gws, 0, gws_bytes, s) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr, true, s);
   int st = BITNET_OK;
-  if (e == cudaSuccess) e = launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, true, s, &st);
+  if (e == cudaSuccess)
+    e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
+               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, true, s, &st);
   pool_free(ws, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);

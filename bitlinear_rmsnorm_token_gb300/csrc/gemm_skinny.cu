@@ -1,0 +1,483 @@
+// gemm_skinny.cu -- BitLinear contraction for a few tens of tokens (9..64) on
+// the 5th-generation tensor cores, with the K dimension split across CTAs.
+//
+// acc[m, n] = sum_k q[m, k] * (code(n, k) - 1) (int8 activations x ternary
+// weights, the product of ggml_vec_dot_i2_i8_s named in section 6.4 of "BitNet
+// Embeddings GGUF Conversion Implementation"), then y = (acc / a_scale[m]) /
+// w_scale in fp32 ("BitNet Inference Framework", "Quantization (W1.58A8)").
+//
+// With few tokens the weight stream is the cost, so the weights are the MMA's
+// M side (128 rows per tile) and the tokens its N side (BN = 16, 32 or 64
+// columns, all tokens in one tile): the MMA work is proportional to the real
+// token count.  A weight matrix has only N/128 tiles, so the K dimension of
+// each tile is split into S ranges of whole I2_S blocks; (tile, range) units
+// are spread over one persistent CTA per SM.
+//
+// Exactness: operands are integers exact in fp16, every partial sum is an
+// integer of magnitude <= 127 * K < 2^24, so the fp32 TMEM accumulator and the
+// fp32 atomic additions that combine the S partial sums of a tile are exact,
+// whatever their order.  The split that completes a tile (a per-tile ticket)
+// rescales it: y = ((float)acc * (1/a_scale)) * (1/w_scale).
+//
+// One stage = one I2_S block column (128 values of K) of the tile:
+//   warp 12    TMA producer: the tokens' fp16 codes of the stage (two 64-wide
+//              slabs, 128-byte swizzle) into a 64 KB ring of their own that
+//              runs up to 16 stages ahead (a token load takes ~1.5 us to land);
+//              the tile's packed bytes arrive in
+//              groups of 4 block columns (128 rows x 128 contiguous bytes,
+//              128-byte swizzle, so that 8 consecutive rows read their columns
+//              from 8 different bank groups) into a ring of 4 slots (the
+//              weight stream needs ~64 KB in flight per SM to cover the HBM
+//              latency); K is split in whole groups
+//   warps 0-7  unpack: warps 0-3 write the first 64-value slab of rows
+//              0..127, warps 4-7 the second, into the MMA's A operand (fp16,
+//              128-byte swizzle, K-major: a warp's stores are conflict-free)
+//   warp 13    TMEM allocation (2 x BN columns: two accumulators); one lane
+//              issues tcgen05.mma (M=128, N=BN, K=16), 8 per stage
+//   warps 8-11 epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 weight rows;
+//              each thread owns one weight row, so for every token the warp
+//              writes (or atomically adds) 32 consecutive outputs
+// Every wait is bounded; an expired wait sets the device error word and the CTA
+// unwinds without trapping.
+#include "common.cuh"
+#include "internal.h"
+#include "rowquant.cuh"
+#include "unpack_f16.cuh"
+
+namespace bitnet {
+namespace {
+
+constexpr int kSkThreads = 448;
+constexpr int kSkUnpackWarps = 8;
+constexpr int kSkBM = 128;  // weight rows per tile (MMA M)
+
+constexpr int kSkPkGroup = 4;  // block columns per packed-weight load: 128 bytes per row
+
+template <int BN>
+struct SkLayout {
+  static constexpr int kPkSlots = 4;
+  static constexpr int kPk = kSkBM * 32 * kSkPkGroup;  // packed bytes of a slot: 128 rows x 128 B
+  static constexpr int kA = 2 * kSkBM * 64 * 2;        // two 64-wide fp16 slabs of the weights
+  static constexpr int kB = 2 * BN * 64 * 2;           // two 64-wide fp16 slabs of the tokens
+  static constexpr int kStages = 3;                    // unpacked weight stages
+  static constexpr int kBSlots = (64 * 1024) / kB;     // token slots
+  static constexpr int offA = 0;                           // [stages][kA]
+  static constexpr int offB = offA + kStages * kA;         // [token slots][kB]
+  static constexpr int offPk = offB + kBSlots * kB;        // [packed slots][kPk]
+  static constexpr int offInv = offPk + kPkSlots * kPk;    // [BN] float: 1 / a_scale
+  static constexpr int kNumBars = 2 * kStages + 2 * kBSlots + 2 * kPkSlots + 4;
+  static constexpr int offBar = offInv + BN * 4;
+  static constexpr int offMisc = offBar + kNumBars * 8;  // tmem base, abort flag, last flag
+  static constexpr int kBytes = offMisc + 32;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kBSlots >= 4, "token ring too shallow");
+  static_assert(kA % 1024 == 0 && kB % 1024 == 0 && kPk % 1024 == 0, "swizzled operands need 1 KB alignment");
+  static_assert(kAlloc <= 232448, "over the 227 KB of shared memory a CTA may use");
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// Unit u = (weight tile, K range): the tile's I2_S blocks [kb0, kb1), whole
+// groups of kSkPkGroup blocks (the last one cut at K).  The i-th block a unit
+// processes is kb0 + (i + rot) mod (kb1 - kb0), rot a whole number of groups
+// that depends on the tile: the CTAs working on one K range at the same time
+// then read its token codes in different orders, instead of all requesting
+// the same L2 lines at once (the sums are order-free integers).
+struct SkUnit {
+  int wt, kb0, kb1, rot;
+  __device__ __forceinline__ int len() const { return kb1 - kb0; }
+  __device__ __forceinline__ int kb(int i) const {
+    const int j = i + rot;
+    return kb0 + (j < len() ? j : j - len());
+  }
+};
+__device__ __forceinline__ SkUnit sk_unit(int u, int S, int nkb) {
+  const int ngrp = (nkb + kSkPkGroup - 1) / kSkPkGroup;
+  SkUnit r;
+  r.wt = u / S;
+  const int ks = u - r.wt * S;
+  r.kb0 = kSkPkGroup * static_cast<int>((static_cast<int64_t>(ngrp) * ks) / S);
+  r.kb1 = min(nkb, kSkPkGroup * static_cast<int>((static_cast<int64_t>(ngrp) * (ks + 1)) / S));
+  const int len = r.kb1 - r.kb0;
+  r.rot = len % kSkPkGroup == 0 ? kSkPkGroup * (r.wt % (len / kSkPkGroup)) : 0;
+  return r;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    k_gemm_skinny(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
+                  const float* __restrict__ a_scale, float inv_w, int M, int N, int K, int S,
+                  float* __restrict__ y, int32_t* __restrict__ acc_out, float* __restrict__ ws,
+                  int* __restrict__ tickets, unsigned* err) {
+  using L = SkLayout<BN>;
+  constexpr int kSt = L::kStages;
+  constexpr int kBS = L::kBSlots;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* sA = smem + L::offA;
+  uint8_t* sB = smem + L::offB;
+  uint8_t* sPk = smem + L::offPk;
+  float* sInv = reinterpret_cast<float*>(smem + L::offInv);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
+  uint64_t* afull = bars;                 // weight slabs unpacked
+  uint64_t* aempty = bars + kSt;          // MMAs reading the weight stage done
+  uint64_t* bfull = bars + 2 * kSt;       // token slabs landed
+  uint64_t* bempty = bfull + kBS;         // MMAs reading the token slot done
+  uint64_t* pk_full = bempty + kBS;       // packed group landed
+  uint64_t* pk_empty = pk_full + L::kPkSlots;
+  uint64_t* acc_full = pk_empty + L::kPkSlots;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nkb = K >> 7;
+  const int n_wt = (N + kSkBM - 1) / kSkBM;
+  const int units = n_wt * S;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSt; ++i) {
+      mbar_init(&afull[i], kSkUnpackWarps);
+      mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < kBS; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], 1);
+    }
+    for (int i = 0; i < L::kPkSlots; ++i) {
+      mbar_init(&pk_full[i], 1);
+      mbar_init(&pk_empty[i], kSkUnpackWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 13) {
+    tmem_alloc(tmem_slot, 2 * BN);
+    tmem_relinquish();
+  }
+  if (warp == 12 && lane == 0) {
+    prefetch_tensormap(&tm_tok);
+    prefetch_tensormap(&tm_w);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // everything below reads what the previous kernel on the stream produced
+  pdl_wait();
+
+  if (warp == 12) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0, ph = 0, p = 0, pph = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const SkUnit w = sk_unit(u, S, nkb);
+        for (int i = 0; i < w.len(); ++i) {
+          const int kb = w.kb(i);
+          if (i % kSkPkGroup == 0) {
+            // the next group of packed block columns (columns past K read as 0)
+            if (!mbar_wait(&pk_empty[p], pph ^ 1, err, abort_flag)) goto producer_done;
+            mbar_arrive_expect_tx(&pk_full[p], static_cast<unsigned>(L::kPk));
+            tma_load_2d(sPk + p * L::kPk, &tm_w, kb * 32, w.wt * kSkBM, &pk_full[p]);
+            if (++p == L::kPkSlots) { p = 0; pph ^= 1; }
+          }
+          if (!mbar_wait(&bempty[s], ph ^ 1, err, abort_flag)) goto producer_done;
+          mbar_arrive_expect_tx(&bfull[s], L::kB);
+          tma_load_2d(sB + s * L::kB, &tm_tok, kb * 128, 0, &bfull[s]);
+          tma_load_2d(sB + s * L::kB + L::kB / 2, &tm_tok, kb * 128 + 64, 0, &bfull[s]);
+          if (++s == kBS) { s = 0; ph ^= 1; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 13) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kSkBM, BN);
+      int s = 0, ph = 0, b = 0, bph = 0, tl = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
+        const SkUnit w = sk_unit(u, S, nkb);
+        const int a = tl & 1;
+        if (!mbar_wait(&acc_empty[a], ((tl >> 1) & 1) ^ 1, err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BN);
+        bool ok = true;
+        for (int i = 0; i < w.len(); ++i) {
+          if (!mbar_wait(&afull[s], ph, err, abort_flag)) {  // also covers the token slot
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * L::kA + h * (L::kA / 2)));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + b * L::kB + h * (L::kB / 2)));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (i || h || kk) ? 1u : 0u);
+          }
+          tc_commit(&aempty[s]);
+          tc_commit(&bempty[b]);
+          if (++s == kSt) { s = 0; ph ^= 1; }
+          if (++b == kBS) { b = 0; bph ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[a]);
+      }
+    }
+  } else if (warp < kSkUnpackWarps) {
+    // --------------------------------------------------------------- unpack
+    const int row = threadIdx.x & 127;  // weight row of the tile
+    const int hf = threadIdx.x >> 7;    // 64-value slab
+    uint8_t* const arow = sA + hf * (L::kA / 2) + (row >> 3) * 1024 + (row & 7) * 128;
+    int s = 0, ph = 0, p = 0, pph = 0, b = 0, bph = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const SkUnit w = sk_unit(u, S, nkb);
+      for (int i = 0; i < w.len(); ++i) {
+        const int gi = i % kSkPkGroup;  // column within the packed group (groups stay whole)
+        if (gi == 0 && !mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
+        // the MMAs of the stage's previous use must have read its A slab
+        if (!mbar_wait(&aempty[s], ph ^ 1, err, abort_flag)) goto unpack_done;
+        uint32_t wd[8];
+        {
+          // 16-byte chunks 2 gi, 2 gi + 1 of the row, stored at chunk c ^ (row & 7)
+          const uint8_t* prow = sPk + p * L::kPk + row * 128;
+          const uint4 lo4 = *reinterpret_cast<const uint4*>(prow + (((2 * gi) ^ (row & 7)) << 4));
+          const uint4 hi4 = *reinterpret_cast<const uint4*>(prow + (((2 * gi + 1) ^ (row & 7)) << 4));
+          wd[0] = lo4.x; wd[1] = lo4.y; wd[2] = lo4.z; wd[3] = lo4.w;
+          wd[4] = hi4.x; wd[5] = hi4.y; wd[6] = hi4.z; wd[7] = hi4.w;
+        }
+        unpack_row_slab<8>(wd, hf, 0, arow + s * L::kA, row & 7);
+        // orders this thread's shared-memory accesses (the packed reads, the
+        // slab writes) before later async-proxy accesses: the MMA reading the
+        // slab, the next TMA overwriting the packed group
+        fence_proxy_async_smem();
+        // afull also tells the MMA thread that the stage's token slabs have
+        // landed: it then waits on one barrier per stage instead of two
+        if (!mbar_wait(&bfull[b], bph, err, abort_flag)) goto unpack_done;
+        if (++b == kBS) { b = 0; bph ^= 1; }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&afull[s]);
+          if (gi == kSkPkGroup - 1 || i == w.len() - 1) mbar_arrive(&pk_empty[p]);
+        }
+        if (gi == kSkPkGroup - 1 || i == w.len() - 1) {
+          if (++p == L::kPkSlots) { p = 0; pph ^= 1; }
+        }
+        if (++s == kSt) { s = 0; ph ^= 1; }
+      }
+    }
+  unpack_done:;
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int et = threadIdx.x - 256;  // 0..127
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    for (int j = et; j < BN; j += 128) sInv[j] = j < M ? __frcp_rn(__ldg(a_scale + j)) : 0.0f;
+    epi_bar();
+    int tl = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
+      const SkUnit w = sk_unit(u, S, nkb);
+      const int a = tl & 1;
+      const int n = w.wt * kSkBM + q * 32 + lane;  // this thread's weight row
+      const bool n_ok = n < N;
+      if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN);
+      // 16 tokens at a time: y (one split) or the partial sum (several splits;
+      // exact fp32 atomic additions)
+#pragma unroll 1
+      for (int j0 = 0; j0 < BN && j0 < M; j0 += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(j0), r);
+        tmem_ld_wait();
+        tmem_reg_fence16(r);
+        if (n_ok) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int j = j0 + i;
+            if (j < M) {
+              const float accf = __uint_as_float(r[i]);
+              if (S == 1) {
+                y[static_cast<int64_t>(j) * N + n] = rescale_elem(accf, sInv[j], inv_w);
+                if (acc_out) acc_out[static_cast<int64_t>(j) * N + n] = __float2int_rn(accf);
+              } else {
+                red_add_f32(ws + static_cast<int64_t>(j) * N + n, accf);
+              }
+            }
+          }
+        }
+      }
+      // the accumulator has been read: release it to the MMAs of a later unit
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+      if (S == 1) continue;
+      // the split that brings the tile's ticket to S writes the tile
+      __threadfence();
+      epi_bar();
+      if (et == 0) *last_flag = atomicAdd(&tickets[w.wt], 1) == S - 1;
+      epi_bar();
+      if (*last_flag) {
+        __threadfence();
+        if (n_ok) {
+          for (int j = 0; j < M && j < BN; ++j) {
+            const float accf = __ldcg(ws + static_cast<int64_t>(j) * N + n);
+            y[static_cast<int64_t>(j) * N + n] = rescale_elem(accf, sInv[j], inv_w);
+            if (acc_out) acc_out[static_cast<int64_t>(j) * N + n] = __float2int_rn(accf);
+          }
+        }
+      }
+      epi_bar();  // last_flag is rewritten by the next unit
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// Number of K splits: the one that minimises the busiest CTA's work, counted in
+// I2_S block columns, with the epilogue of a split unit (its atomic additions
+// and ticket) costed as two more; ties go to fewer splits.
+int choose_splits(int n_wt, int nkb, int ctas) {
+  const int ngrp = (nkb + kSkPkGroup - 1) / kSkPkGroup;
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  const int max_s = ngrp < 64 ? ngrp : 64;
+  for (int S = 1; S <= max_s; ++S) {
+    const int64_t units = static_cast<int64_t>(n_wt) * S;
+    const int64_t per_cta = (units + ctas - 1) / ctas;
+    const int64_t cost = per_cta * (kSkPkGroup * ((ngrp + S - 1) / S) + (S > 1 ? 2 : 0));
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
+template <int BN>
+cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const __half* codes_f16, const float* a_scale,
+                      const uint8_t* packed_w, float inv_w, int M, int K, int N, int S, float* y, int32_t* acc_out,
+                      float* ws, int* tickets, bool pdl, cudaStream_t s, int* status) {
+  using L = SkLayout<BN>;
+  CUtensorMap tm_tok, tm_w;
+  {
+    // tokens: fp16 [M, K]; boxes of 64 values x BN tokens (tokens >= M read as 0)
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BN)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_tok, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(codes_f16), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  {
+    // packed weights: bytes [N, K/4]; boxes of 4 block columns (128 B) x 128 rows
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(32 * kSkPkGroup), static_cast<cuuint32_t>(kSkBM)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(packed_w), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      *status = BITNET_ERR_CUDA;
+      return cudaErrorInvalidValue;
+    }
+  }
+  auto kern = k_gemm_skinny<BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int units = ((N + kSkBM - 1) / kSkBM) * S;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units < ctx->num_sms ? units : ctx->num_sms);
+  cfg.blockDim = dim3(kSkThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, inv_w, M, N, K, S, y, acc_out, ws, tickets,
+                            ctx->err_word);
+}
+
+}  // namespace
+
+// Used for 9..64 tokens when the weight stream is long enough to pay for the
+// split's extra work (zeroing the partial sums, a final pass per tile); below
+// that (K <= 2048 and N <= 8192, a few us) the tokens-as-M kernel is faster.
+bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N) {
+  return M > kDecodeMaxM && M <= 64 && K >= 128 && K % 128 == 0 && N >= 1 && (K >= 4096 || N >= 16384);
+}
+
+size_t gemm_skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N) {
+  const int n_wt = static_cast<int>((N + kSkBM - 1) / kSkBM);
+  const int S = choose_splits(n_wt, static_cast<int>(K >> 7), ctx->num_sms);
+  if (S == 1) return 0;
+  return ((static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255)) +
+         static_cast<size_t>(n_wt) * 4;
+}
+
+cudaError_t launch_gemm_skinny(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
+                               const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
+                               int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
+                               int* status) {
+  *status = BITNET_OK;
+  EncodeTiledFn encode = encode_tiled_fn();
+  if (!encode) {
+    *status = BITNET_ERR_CUDA;
+    return cudaErrorNotSupported;
+  }
+  const float inv_w = 1.0f / w_scale;  // IEEE division, as in the oracle
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const int n_wt = (n + kSkBM - 1) / kSkBM;
+  const int S = choose_splits(n_wt, k >> 7, ctx->num_sms);
+  float* ws = nullptr;
+  int* tickets = nullptr;
+  if (S > 1) {
+    // the partial sums are added into a zeroed fp32 [M, N] array
+    const size_t ws_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255);
+    ws = static_cast<float*>(workspace);
+    tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + ws_bytes);
+    if (!workspace_zeroed) {
+      cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes + static_cast<size_t>(n_wt) * 4, s);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const int bn = m <= 16 ? 16 : m <= 32 ? 32 : 64;
+  switch (bn) {
+    case 16:
+      return launch_bn<16>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, k, n, S, y, acc_out, ws, tickets,
+                           pdl, s, status);
+    case 32:
+      return launch_bn<32>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, k, n, S, y, acc_out, ws, tickets,
+                           pdl, s, status);
+    default:
+      return launch_bn<64>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, k, n, S, y, acc_out, ws, tickets,
+                           pdl, s, status);
+  }
+}
+
+}  // namespace bitnet

@@ -92,4 +92,15 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
                            const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
                            int32_t* acc_out, bool pdl, cudaStream_t s, int* status);
 
+// Tensor-core contraction for 9..128 tokens (weights as the MMA's M side, K
+// split across CTAs).  Needs gemm_skinny_workspace() bytes of device memory
+// (0 when K is not split), zero on entry: zeroed here on the stream unless
+// workspace_zeroed.
+bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N);
+size_t gemm_skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemm_skinny(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
+                               const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
+                               int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
+                               int* status);
+
 }  // namespace bitnet

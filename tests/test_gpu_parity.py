@@ -189,9 +189,14 @@ GEMM_CASES = [
     # decode (dp4a) path
     (1, 128, 1), (1, 1024, 2048), (2, 640, 33), (3, 3072, 200), (5, 1024, 129), (8, 1024, 2048), (8, 8192, 64),
     (1, 16384, 4096), (4, 16384, 2500),
-    # tensor-core path: tiles of 128 weight rows x 64/128/256 tokens, ragged tails
-    (9, 128, 128), (16, 256, 130), (64, 1024, 256), (100, 640, 1000), (129, 1024, 384), (300, 3072, 257),
-    (600, 2048, 1024), (1000, 128, 5),
+    # split-K tensor-core path (9..64 tokens with K >= 4096 or N >= 16384): 128 weight
+    # rows x 16/32/64 tokens, K split into ranges of I2_S blocks combined by atomic fp32
+    # additions, ragged weight tiles
+    (16, 16384, 1024), (64, 4096, 4096), (33, 8192, 130), (9, 65536, 256), (12, 4096, 3000),
+    (48, 6144, 1000), (20, 1024, 16500), (64, 256, 16384),
+    # tensor-core path, tokens as the MMA's M side: 128 tokens x 64/128/256 weights, ragged tails
+    (9, 128, 128), (16, 256, 130), (64, 1024, 256), (100, 640, 1000), (40, 2048, 1000), (64, 128, 5000),
+    (24, 3072, 2049), (17, 1920, 300), (129, 1024, 384), (300, 3072, 257), (600, 2048, 1024), (1000, 128, 5),
 ]
 
 
@@ -290,7 +295,8 @@ FWD_CASES = [
     # warps (28 slots of 8 KB at K=4096; 6 slots of one 16 KB row at K=65536)
     (1, 4096, 65536), (1, 65536, 4096), (2, 8192, 20000),
     # norm launch + tensor-core launch
-    (16, 640, 256), (64, 1024, 2048), (257, 3072, 1024), (1000, 640, 130), (2048, 2048, 384), (40, 8192, 256)]
+    (16, 640, 256), (64, 1024, 2048), (257, 3072, 1024), (1000, 640, 130), (2048, 2048, 384), (40, 8192, 256),
+    (128, 8192, 3000), (12, 16384, 1024)]
 
 
 @pytest.mark.parametrize("M,K,N", FWD_CASES)
