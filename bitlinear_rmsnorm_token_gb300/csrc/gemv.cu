@@ -84,11 +84,14 @@ struct DecodeSmemTail {
   int abort_flag;
 };
 
-// Long rows up to K = 16384 with the norm fused in: every compute thread holds
-// its (at most 9) float4 groups of x and of the norm weight in registers, so
-// neither is staged in shared memory.
-__host__ __device__ inline bool register_prologue(bool fused, int K) {
-  return fused && K >= 4096 && K % 2048 == 0 && K <= 16384;
+// Fused norm with x and the norm weight held in registers (every compute
+// thread holds at most kDecRegGroups float4 groups of each) instead of staged
+// in shared memory: long rows up to K = 16384, and single-token rows up to
+// K = 3840 (two groups per thread, within the register budget of the
+// two-CTAs-per-SM kernels).
+__host__ __device__ inline bool register_prologue_long(int K) { return K >= 4096 && K % 2048 == 0 && K <= 16384; }
+__host__ __device__ inline bool register_prologue(bool fused, int K, int M) {
+  return fused && (register_prologue_long(K) || (M == 1 && K <= 3840));
 }
 constexpr int kDecRegGroups = 9;  // float4 groups per thread: 16384 / 4 <= 9 * 480
 
@@ -104,7 +107,7 @@ constexpr int kDecRegGroups = 9;  // float4 groups per thread: 16384 / 4 <= 9 * 
 struct DecodeLayout {
   int xs, gs, xq, tail, total;
   __host__ __device__ DecodeLayout(int M, int K, bool fused, int ring_bytes) {
-    const bool staged = fused && !register_prologue(fused, K);
+    const bool staged = fused && !register_prologue(fused, K, M);
     xs = ring_bytes;
     gs = xs + (staged ? M * K * 4 : (fused ? 0 : ((M * K + 127) & ~127)));
     xq = gs + (staged ? K * 4 : 0);
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
     grp = 1;
   }
   const int nst = (r1 - r0 + rps - 1) / rps;
-  const bool regp = kLong && register_prologue(kFused, K);  // implies lng
+  const bool regp = register_prologue(kFused, K, M);
 
   const DecodeLayout lay(M, K, kFused, P.ring_bytes);
   uint8_t* ring = smem;
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
   const int total = M * G;
   const int m_start = tid / G;
   const int g_start = tid - m_start * G;
-  if (kFused && kLong && regp) {
+  if (kFused && regp) {
     // register prologue: row by row, x and the norm weight straight from
     // global memory into registers, the same order-free reductions as below
     // through shared-memory atomics.  Thread tid holds the float4 groups
@@ -279,11 +282,13 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       const int j = tid + kThr * i + rot;
       return j < G ? j : j - G;  // valid when tid + 480 i < G
     };
-    const int nv = (G - tid + kThr - 1) / kThr;  // groups of this thread (>= 2)
-    float4 gv[kDecRegGroups];
+    // groups of this thread (at most kRG: 9 for long rows, 2 for one short row)
+    constexpr int kRG = kLong ? kDecRegGroups : 2;
+    const int nv = (G - tid + kThr - 1) / kThr;
+    float4 gv[kRG];
     auto load_g = [&]() {
 #pragma unroll
-      for (int i = 0; i < kDecRegGroups; ++i)
+      for (int i = 0; i < kRG; ++i)
         gv[i] = i < nv ? __ldg(g4 + gidx(i)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     };
     if (P.weights_static) load_g();
@@ -292,10 +297,10 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
 #pragma unroll 1
     for (int m = 0; m < M; ++m) {
       const float4* x4 = reinterpret_cast<const float4*>(pr.x) + static_cast<int64_t>(m) * G;
-      float4 v[kDecRegGroups];
+      float4 v[kRG];
       int key = 0;
 #pragma unroll
-      for (int i = 0; i < kDecRegGroups; ++i) {
+      for (int i = 0; i < kRG; ++i) {
         v[i] = i < nv ? __ldg(x4 + gidx(i)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         key = max(key, sq_key4(v[i]));
       }
@@ -306,7 +311,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       const float scale = sq_scale(key);
       SqPartial part = {0ull, 0u};
 #pragma unroll
-      for (int i = 0; i < kDecRegGroups; ++i)
+      for (int i = 0; i < kRG; ++i)
         if (i < nv) sq_add4(part, v[i], scale);
       const unsigned long long w = warp_sum_u64(sq_fold(part, 4 * nv));
       if (lane == 0 && w) atomicAdd(&tail->ss[m], w);
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       const float rstd = rstd_from_fixed(tail->ss[m], key, K, P.eps);
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < kDecRegGroups; ++i) {
+      for (int i = 0; i < kRG; ++i) {
         if (i < nv) {
           v[i] = make_float4(norm_elem(v[i].x, rstd, gv[i].x), norm_elem(v[i].y, rstd, gv[i].y),
                              norm_elem(v[i].z, rstd, gv[i].z), norm_elem(v[i].w, rstd, gv[i].w));
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       const float as = act_scale_from_amax(__uint_as_float(tail->amax_bits[m]));
       int rs = 0;
 #pragma unroll
-      for (int i = 0; i < kDecRegGroups; ++i) {
+      for (int i = 0; i < kRG; ++i) {
         if (i < nv) {
           const uint32_t pk = quant_pack4_i8(v[i], as);
           *reinterpret_cast<uint32_t*>(xq + m * K + slot_major(4 * gidx(i), cpr)) = pk;
@@ -688,7 +693,7 @@ bool decode_split_preferred(int64_t M, int64_t K) {
 
 bool decode_fused_supported(int64_t M, int64_t K) {
   if (M < 1 || M > kDecodeMaxM) return false;
-  if (K <= 16384 && register_prologue(true, static_cast<int>(K))) return decode_supported(M, K);
+  if (K <= 16384 && register_prologue(true, static_cast<int>(K), static_cast<int>(M))) return decode_supported(M, K);
   return 5 * M * K + 4 * K <= kDecodeFusedMaxStageBytes;
 }
 
