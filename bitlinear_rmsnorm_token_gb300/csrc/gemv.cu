@@ -81,6 +81,12 @@ struct DecodeSmemTail {
   int rowsum[kDecodeMaxM];
   float rstd[kDecodeMaxM];
   float inv_a[kDecodeMaxM];
+  // register prologue: per-warp partials of the current row (written without
+  // atomics, combined by every thread after the barrier) and per-warp row sums
+  int red_key[kDecWarps];
+  unsigned long long red_ss[kDecWarps];
+  unsigned red_amax[kDecWarps];
+  int red_rs[kDecodeMaxM][kDecWarps];
   int abort_flag;
 };
 
@@ -305,18 +311,23 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
         key = max(key, sq_key4(v[i]));
       }
       key = warp_max_int(key);
-      if (lane == 0 && key) atomicMax(&tail->sq_key[m], key);
+      if (lane == 0) tail->red_key[warp] = key;
       compute_bar();
-      key = tail->sq_key[m];
+      key = 0;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) key = max(key, tail->red_key[w]);
       const float scale = sq_scale(key);
       SqPartial part = {0ull, 0u};
 #pragma unroll
       for (int i = 0; i < kRG; ++i)
         if (i < nv) sq_add4(part, v[i], scale);
-      const unsigned long long w = warp_sum_u64(sq_fold(part, 4 * nv));
-      if (lane == 0 && w) atomicAdd(&tail->ss[m], w);
+      const unsigned long long wsum = warp_sum_u64(sq_fold(part, 4 * nv));
+      if (lane == 0) tail->red_ss[warp] = wsum;
       compute_bar();
-      const float rstd = rstd_from_fixed(tail->ss[m], key, K, P.eps);
+      unsigned long long ss = 0ull;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) ss += tail->red_ss[w];
+      const float rstd = rstd_from_fixed(ss, key, K, P.eps);
       float amax = 0.0f;
 #pragma unroll
       for (int i = 0; i < kRG; ++i) {
@@ -327,9 +338,12 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
         }
       }
       amax = warp_max(amax);
-      if (lane == 0) atomicMax(&tail->amax_bits[m], __float_as_uint(amax));
+      if (lane == 0) tail->red_amax[warp] = __float_as_uint(amax);
       compute_bar();
-      const float as = act_scale_from_amax(__uint_as_float(tail->amax_bits[m]));
+      unsigned amax_bits = 0u;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) amax_bits = max(amax_bits, tail->red_amax[w]);
+      const float as = act_scale_from_amax(__uint_as_float(amax_bits));
       int rs = 0;
 #pragma unroll
       for (int i = 0; i < kRG; ++i) {
@@ -340,7 +354,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
         }
       }
       rs = warp_sum_int(rs);
-      if (lane == 0 && rs) atomicAdd(&tail->rowsum[m], rs);
+      if (lane == 0) tail->red_rs[m][warp] = rs;
       if (tid == 0) tail->inv_a[m] = __frcp_rn(as);
     }
   } else {
@@ -497,7 +511,16 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
   float inv_a[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
-    rowsum[m] = m < M ? tail->rowsum[m] : 0;
+    int rsum = 0;
+    if (m < M) {
+      if (kFused && regp) {
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) rsum += tail->red_rs[m][w];
+      } else {
+        rsum = tail->rowsum[m];
+      }
+    }
+    rowsum[m] = rsum;
     inv_a[m] = m < M ? tail->inv_a[m] : 0.0f;
   }
   const float inv_w = pr.inv_w;
