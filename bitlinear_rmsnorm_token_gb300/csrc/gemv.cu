@@ -720,8 +720,20 @@ bool decode_fused_supported(int64_t M, int64_t K) {
   return 5 * M * K + 4 * K <= kDecodeFusedMaxStageBytes;
 }
 
-cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
+cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs_in, int njobs, int M, float eps, bool fused,
                           bool weights_static, cudaStream_t s, int reserve_sms) {
+  if (njobs < 1 || njobs > BITNET_MAX_GROUP) return cudaErrorInvalidValue;
+  // Projections with the longest rows (the longest prologues) take the lowest
+  // CTA indices: the CTAs dispatched last start latest, and the launch ends
+  // with its slowest CTA.  Each projection's outputs do not depend on the order.
+  DecodeJob jobs[BITNET_MAX_GROUP];
+  for (int i = 0; i < njobs; ++i) jobs[i] = jobs_in[i];
+  for (int i = 1; i < njobs; ++i)
+    for (int j = i; j > 0 && jobs[j].K > jobs[j - 1].K; --j) {
+      const DecodeJob t = jobs[j];
+      jobs[j] = jobs[j - 1];
+      jobs[j - 1] = t;
+    }
   DecodeParams P = {};
   P.nproj = njobs;
   P.M = M;
