@@ -10,7 +10,8 @@ layers whose I2_S weights total more than twice the L2 cache, so every step
 streams its weights from HBM.  Metric: weight-stream GB/s = algorithmic bytes
 (packed weights + scale + x + norm weight + y) per step / time.
 
-Other workloads (--workload): q_proj_m8 (M=8, K=1024, N=2048), gemma3_prefill
+Other workloads (--workload): q_proj_m8 (M=8, K=1024, N=2048), proj (one
+projection, --m/--k/--n), gemma3_prefill
 (seven Gemma3-shaped projections at M=32768 with 1% x20 outlier features),
 qwen3_prefill_stack (28 layers x 7 projections at M=32768), sweep (K, N in
 {1024,4096,8192,16384} x M in {1,16,128,2048,16384}).
@@ -477,6 +478,52 @@ def run_q_proj_m8(args, rank, world, local):
             "config": {"workload": "q_proj_M8_K1024_N2048", "launch": "CUDA graph, weight pool > 2x L2"}}
 
 
+def run_proj(args, rank, world, local):
+    """One projection of M tokens, K -> N (--m, --k, --n), through the no-alloc
+    entry point, a CUDA graph cycling through distinct weight tensors totalling
+    more than twice the L2 (kernel time, not launch time)."""
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    M, K, N = args.m, args.k, args.n
+    wb = N * K // 4
+    nw = min(1024, max(2, int(np.ceil(2.0 * L2_BYTES / wb))))
+    ws_list = []
+    for i in range(nw):
+        w = wl.gen_device((N, K), wl.seed_for(5, K, N, i), device, std=0.02)
+        ws_list.append(bn.pack_i2s(w))
+        del w
+    g = torch.from_numpy(wl.gen_norm_w(K, seed=K)).to(device)
+    x = wl.gen_device((M, K), wl.seed_for(5, M, K, N), device)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def cycle():
+        for packed, sc in ws_list:
+            bn.bitlinear_forward_noalloc(x, g, packed, sc, N, wl.EPS, y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        cycle()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        cycle()
+    reps = max(1, args.steps // nw)
+    with torch.cuda.stream(stream):
+        ms = time_region(torch, stream, graph.replay, reps, max(1, min(args.warmup, 3))) / nw
+    b = wb + 4 + M * K * 4 + K * 4 + M * N * 4
+    hbm, bf16, _, _ = peaks()
+    return {"metric": METRIC, "value": round(b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": reps * nw, "ms_per_step": ms, "us_per_projection": ms * 1e3,
+            "tops": 2.0 * M * N * K / (ms * 1e-3) / 1e12, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm,
+            "config": {"workload": f"proj_M{M}_K{K}_N{N}", "weights_cycled": nw,
+                       "launch": "CUDA graph of bitnet_bitlinear_forward_noalloc"}}
+
+
 def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, outlier_frac, stream):
     """Buffers for one layer's projections at M tokens (x drawn on the device)."""
     items = []
@@ -635,7 +682,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=20000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_decode_layer",
-                    choices=["qwen3_decode_layer", "q_proj_m8", "gemma3_prefill", "qwen3_prefill_stack", "sweep"])
+                    choices=["qwen3_decode_layer", "q_proj_m8", "gemma3_prefill", "qwen3_prefill_stack", "sweep",
+                             "proj"])
+    ap.add_argument("--m", type=int, default=16, help="--workload proj: tokens")
+    ap.add_argument("--k", type=int, default=16384, help="--workload proj: input features")
+    ap.add_argument("--n", type=int, default=16384, help="--workload proj: output features")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -651,6 +702,8 @@ def main():
         out = run_q_proj_m8(args, rank, world, local)
     elif args.workload == "sweep":
         out = run_sweep(args, rank, world, local)
+    elif args.workload == "proj":
+        out = run_proj(args, rank, world, local)
     else:
         out = run_prefill(args, rank, world, local, args.workload)
     if rank == 0 and out is not None:

@@ -72,7 +72,7 @@ struct DecodeParams {
 struct DecodeSmemTail {
   uint64_t full[kDecMaxSlots];
   uint64_t empty[kDecMaxSlots];
-  uint64_t in_full;  // activations (and norm weight) staged
+  uint64_t in_full;  // activations (and norm weight) staged; register prologue: loaded into registers
   // per-row reductions, combined across warps with shared-memory atomics
   // (integer or max: the result does not depend on the order)
   unsigned long long ss[kDecodeMaxM];
@@ -181,6 +181,11 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
   }
   const int nst = (r1 - r0 + rps - 1) / rps;
   const bool regp = register_prologue(kFused, K, M);
+  // Long rows, register prologue, weights not requested before the grid
+  // dependency wait: the weight stream starts only once every compute warp
+  // holds its x and norm weight, which otherwise arrive far later (each CTA
+  // brings in the whole row, up to 128 KB, next to its weight ring).
+  const bool gate_weights = regp && lng && !P.weights_static;
 
   const DecodeLayout lay(M, K, kFused, P.ring_bytes);
   uint8_t* ring = smem;
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       mbar_init(&tail->full[s], 1);
       mbar_init(&tail->empty[s], lng ? 1 : kDecWarps);
     }
-    mbar_init(&tail->in_full, 1);
+    mbar_init(&tail->in_full, gate_weights ? kDecWarps : 1);
     for (int m = 0; m < kDecodeMaxM; ++m) {
       tail->ss[m] = 0ull;
       tail->sq_key[m] = 0;
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
         for (int c = 0; c < first; ++c) issue(c);
       }
       pdl_wait();
+      if (gate_weights && !mbar_wait(&tail->in_full, 0, err, &tail->abort_flag)) return;
       if (kFused) {
         if (!regp) {
           if (!P.weights_static) bulk_load(gs, pr.g, static_cast<unsigned>(K * 4), &tail->in_full);
@@ -312,6 +318,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       }
       key = warp_max_int(key);
       if (lane == 0) tail->red_key[warp] = key;
+      if (gate_weights && m == 0 && lane == 0) mbar_arrive(&tail->in_full);  // this warp's x and g are in
       compute_bar();
       key = 0;
 #pragma unroll
