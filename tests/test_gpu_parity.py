@@ -288,6 +288,8 @@ FWD_CASES = [
     # and norm weight in registers, one warp per 8 KB stage of whole rows
     (1, 4096, 4096), (5, 4096, 333), (1, 16384, 4096), (1, 8192, 3000), (4, 8192, 777),
     (3, 16384, 300), (8, 8192, 64), (2, 16384, 4096),
+    # fewer weight rows than CTAs, a single row, K = 12288
+    (1, 16384, 96), (2, 4096, 150), (4, 4096, 5000), (1, 12288, 1),
     # longer rows: row-per-CTA norm launch, then the decode launch streaming its
     # weight ring during it
     (1, 65536, 300), (2, 32768, 40),
@@ -370,6 +372,28 @@ def test_group_matches_oracle_and_single_calls(oracle_mod, M):
     for (xd, gd, packed, ws, N, y), ref, single in zip(items, refs, singles):
         assert torch.equal(y, single)
         assert_rows_close(host(y), ref, "group")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("flags", [0, bn.FLAG_WEIGHTS_STATIC])
+def test_group_long_rows_matches_oracle(oracle_mod, M, flags):
+    """Long-row projections of different widths in one grouped launch, with and
+    without early weight streaming."""
+    shapes = [(4096, 2048), (16384, 1000), (8192, 3000), (4096, 77)]
+    items, refs, singles = [], [], []
+    for i, (K, N) in enumerate(shapes):
+        x = _x_with_edges(M, K, seed=100 + i)
+        g = wl.gen_norm_w(K, seed=200 + i)
+        packed, ws = bn.pack_i2s(dev(wl.gen_latent_w(N, K, seed=300 + i)))
+        xd, gd = dev(x), dev(g)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        items.append((xd, gd, packed, ws, N, y))
+        refs.append(oracle_mod.bitlinear_forward(x, g, host(packed), ws, N, wl.EPS))
+        singles.append(bn.bitlinear_forward(xd, gd, packed, ws, N, wl.EPS))
+    bn.bitlinear_forward_group(items, M, wl.EPS, flags=flags)
+    for (xd, gd, packed, ws, N, y), ref, single in zip(items, refs, singles):
+        assert torch.equal(y, single)
+        assert_rows_close(host(y), ref, "group long rows")
 
 
 def test_group_in_cuda_graph_rotating_layers(oracle_mod):
