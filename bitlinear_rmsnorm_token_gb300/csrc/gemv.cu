@@ -225,13 +225,16 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       // issued once every slot of the group is free again.
       const int ncopy = (nst + grp - 1) / grp;
       const int first = min(ncopy, nslots / grp);
+      // the weights are read once per call: evict them first from the L2
+      const uint64_t wpol = l2_policy_evict_first();
       auto issue = [&](int c) {
         const int st0 = c * grp;
         const int s = st0 % nslots;
         const int rows = min(grp * rps, r1 - r0 - st0 * rps);
         const unsigned bytes = static_cast<unsigned>(rows * row_bytes);
         mbar_arrive_expect_tx(&tail->full[s], bytes);
-        bulk_load(ring + s * sbytes, src + static_cast<int64_t>(st0) * rps * row_bytes, bytes, &tail->full[s]);
+        bulk_load_hint(ring + s * sbytes, src + static_cast<int64_t>(st0) * rps * row_bytes, bytes, &tail->full[s],
+                       wpol);
       };
       // parameters (packed weights, norm weight) may be requested before the
       // previous kernel has finished when they are known not to be written by
