@@ -154,11 +154,25 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
   const int r0 = (static_cast<int>(blockIdx.x) - pr.cta_begin) * pr.rows_per_cta;
   const int r1 = min(N, r0 + pr.rows_per_cta);
   // lpr lanes share a weight row (each taking cpr/lpr of its 16-byte chunks);
-  // start at 4 and widen while the CTA has fewer rows than one pass of all
-  // warps, so every warp gets work.  A stage holds a whole number of passes.
+  // at least 4 where the row allows it (two rows of a shared-memory phase then
+  // touch different banks) and chosen to shorten the busiest warp's chain: each
+  // further pass over rows costs a whole dot-product latency, each chunk of a
+  // lane a few issue cycles and each lane-halving a shuffle.  A stage holds a
+  // whole number of passes.
   const int cpr = K >> 6;
   int lpr = (cpr & 3) ? 2 : 4;
-  while (lpr < 32 && cpr % (2 * lpr) == 0 && (r1 - r0) < kDecWarps * (32 / lpr)) lpr *= 2;
+  {
+    const int R = max(r1 - r0, 1);
+    int best = 1 << 30;
+    for (int l = lpr; l <= 32 && cpr % l == 0; l *= 2) {
+      const int passes = (R + kDecWarps * (32 / l) - 1) / (kDecWarps * (32 / l));
+      const int cost = passes * ((cpr / l) * 40 + (31 - __clz(l)) * 30 + 120);
+      if (cost < best) {
+        best = cost;
+        lpr = l;
+      }
+    }
+  }
   const int rpp = 32 / lpr;  // rows per warp pass
   // Long rows (cpr a multiple of 32, >= 64): stages of whole rows, about 4 KB,
   // one warp per stage.  Otherwise whole warps take rows and a 24 KB stage
@@ -323,9 +337,8 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       if (lane == 0) tail->red_key[warp] = key;
       if (gate_weights && m == 0 && lane == 0) mbar_arrive(&tail->in_full);  // this warp's x and g are in
       compute_bar();
-      key = 0;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) key = max(key, tail->red_key[w]);
+      // cross-warp combines: lane w reads warp w's partial, one warp reduction
+      key = warp_max_int(lane < kDecWarps ? tail->red_key[lane] : 0);
       const float scale = sq_scale(key);
       SqPartial part = {0ull, 0u};
 #pragma unroll
@@ -334,9 +347,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       const unsigned long long wsum = warp_sum_u64(sq_fold(part, 4 * nv));
       if (lane == 0) tail->red_ss[warp] = wsum;
       compute_bar();
-      unsigned long long ss = 0ull;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) ss += tail->red_ss[w];
+      const unsigned long long ss = warp_sum_u64(lane < kDecWarps ? tail->red_ss[lane] : 0ull);
       const float rstd = rstd_from_fixed(ss, key, K, P.eps);
       float amax = 0.0f;
 #pragma unroll
@@ -350,9 +361,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       amax = warp_max(amax);
       if (lane == 0) tail->red_amax[warp] = __float_as_uint(amax);
       compute_bar();
-      unsigned amax_bits = 0u;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) amax_bits = max(amax_bits, tail->red_amax[w]);
+      const unsigned amax_bits = __reduce_max_sync(0xffffffffu, lane < kDecWarps ? tail->red_amax[lane] : 0u);
       const float as = act_scale_from_amax(__uint_as_float(amax_bits));
       int rs = 0;
 #pragma unroll
@@ -524,8 +533,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
     int rsum = 0;
     if (m < M) {
       if (kFused && regp) {
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) rsum += tail->red_rs[m][w];
+        rsum = warp_sum_int(lane < kDecWarps ? tail->red_rs[m][lane] : 0);
       } else {
         rsum = tail->rowsum[m];
       }
@@ -622,6 +630,70 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
     return;
   }
 
+  // One pass of lpr lanes per row over rpp rows: chunk loop, lane reduction,
+  // rescale and store (every lane takes part in the shuffles).
+  auto row_pass = [&](const uint8_t* wrow, bool valid, int n) {
+    int acc[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[m][q] = 0;
+    if (valid) {
+      int c = sub + rot;
+      if (c >= cpr) c -= cpr;
+#pragma unroll 2
+      for (int i = 0; i < cpl; ++i) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(wrow + c * 16);
+        const unsigned wd[4] = {wv.x, wv.y, wv.z, wv.w};
+        const int8_t* xb = xq + (c << 4);
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+          const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
+          const unsigned m0 = wd[0] & mask, m1 = wd[1] & mask, m2 = wd[2] & mask, m3 = wd[3] & mask;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+              const int4 xv = *reinterpret_cast<const int4*>(xb + m * K + sl * slot_stride);
+              int a = acc[m][sl];
+              a = dp4a_us(m0, xv.x, a);
+              a = dp4a_us(m1, xv.y, a);
+              a = dp4a_us(m2, xv.z, a);
+              a = dp4a_us(m3, xv.w, a);
+              acc[m][sl] = a;
+            }
+          }
+        }
+        c += lpr;
+        if (c >= cpr) c -= cpr;
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      int t = (acc[m][0] >> 6) + (acc[m][1] >> 4) + (acc[m][2] >> 2) + acc[m][3];
+      for (int off = lpr >> 1; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (valid && sub == 0 && m < M) {
+        const int a = t - rowsum[m];
+        pr.y[static_cast<int64_t>(m) * N + n] = rescale_elem(__int2float_rn(a), inv_a[m], inv_w);
+        if (pr.acc_out) pr.acc_out[static_cast<int64_t>(m) * N + n] = a;
+      }
+    }
+  };
+
+  if (nst <= nslots) {
+    // Every stage of this CTA is in the ring at once (no slot is reused): wait
+    // for all of them, then share the CTA's rows among the warps as one list,
+    // with no per-stage hand-back.
+    for (int st = 0; st < nst; ++st)
+      if (!mbar_wait(&tail->full[st], 0, err, &tail->abort_flag)) return;
+    const int R = r1 - r0;
+    for (int base = warp * rpp; base < R; base += kDecWarps * rpp) {
+      const int r = base + lane / lpr;
+      const int st = r / rps;
+      row_pass(ring + st * sbytes + (r - st * rps) * row_bytes, r < R, r0 + r);
+    }
+    return;
+  }
+
   for (int st = 0; st < nst; ++st) {
     const int s = st % nslots;
     if (!mbar_wait(&tail->full[s], (st / nslots) & 1, err, &tail->abort_flag)) break;
@@ -629,53 +701,7 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
     const int rows = min(rps, r1 - r0 - st * rps);
     for (int base = warp * rpp; base < rows; base += kDecWarps * rpp) {
       const int r = base + lane / lpr;
-      const bool valid = r < rows;
-      int acc[MT][4];
-#pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[m][q] = 0;
-      if (valid) {
-        const uint8_t* wrow = stage + r * row_bytes;
-        int c = sub + rot;
-        if (c >= cpr) c -= cpr;
-#pragma unroll 2
-        for (int i = 0; i < cpl; ++i) {
-          const uint4 wv = *reinterpret_cast<const uint4*>(wrow + c * 16);
-          const unsigned wd[4] = {wv.x, wv.y, wv.z, wv.w};
-          const int8_t* xb = xq + (c << 4);
-#pragma unroll
-          for (int sl = 0; sl < 4; ++sl) {
-            const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
-            const unsigned m0 = wd[0] & mask, m1 = wd[1] & mask, m2 = wd[2] & mask, m3 = wd[3] & mask;
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              if (m < M) {
-                const int4 xv = *reinterpret_cast<const int4*>(xb + m * K + sl * slot_stride);
-                int a = acc[m][sl];
-                a = dp4a_us(m0, xv.x, a);
-                a = dp4a_us(m1, xv.y, a);
-                a = dp4a_us(m2, xv.z, a);
-                a = dp4a_us(m3, xv.w, a);
-                acc[m][sl] = a;
-              }
-            }
-          }
-          c += lpr;
-          if (c >= cpr) c -= cpr;
-        }
-      }
-      const int n = r0 + st * rps + r;
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        int t = (acc[m][0] >> 6) + (acc[m][1] >> 4) + (acc[m][2] >> 2) + acc[m][3];
-        for (int off = lpr >> 1; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-        if (valid && sub == 0 && m < M) {
-          const int a = t - rowsum[m];
-          pr.y[static_cast<int64_t>(m) * N + n] = rescale_elem(__int2float_rn(a), inv_a[m], inv_w);
-          if (pr.acc_out) pr.acc_out[static_cast<int64_t>(m) * N + n] = a;
-        }
-      }
+      row_pass(stage + r * row_bytes, r < rows, r0 + st * rps + r);
     }
     // the stage's loads are complete (their values fed the dot products);
     // order them before the producer's next bulk copy into the stage
