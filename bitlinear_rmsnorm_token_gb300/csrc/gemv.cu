@@ -569,7 +569,60 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       if (!mbar_wait(&tail->full[s - s % grp], (st / nslots) & 1, err, &tail->abort_flag)) break;
       const uint8_t* stage = ring + s * sbytes;
       const int rows = min(rps, r1 - r0 - st * rps);
-      for (int r = 0; r < rows; ++r) {
+      int r = 0;
+      if (MT == 1) {
+        // One token: two rows per pass.  A chunk position's activation codes
+        // are read (or held) once for both rows, and the two dot products are
+        // independent work for the warp.
+        for (; r + 1 < rows; r += 2) {
+          const uint8_t* w0 = stage + r * row_bytes;
+          const uint8_t* w1 = w0 + row_bytes;
+          int a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
+          auto chunk2 = [&](int c, const int4(&xv)[4]) {
+            const uint4 u = *reinterpret_cast<const uint4*>(w0 + c * 16);
+            const uint4 v = *reinterpret_cast<const uint4*>(w1 + c * 16);
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+              const unsigned mask = 0xC0C0C0C0u >> (2 * sl);
+              int p = a0[sl], q = a1[sl];
+              p = dp4a_us(u.x & mask, xv[sl].x, p);
+              q = dp4a_us(v.x & mask, xv[sl].x, q);
+              p = dp4a_us(u.y & mask, xv[sl].y, p);
+              q = dp4a_us(v.y & mask, xv[sl].y, q);
+              p = dp4a_us(u.z & mask, xv[sl].z, p);
+              q = dp4a_us(v.z & mask, xv[sl].z, q);
+              p = dp4a_us(u.w & mask, xv[sl].w, p);
+              q = dp4a_us(v.w & mask, xv[sl].w, q);
+              a0[sl] = p;
+              a1[sl] = q;
+            }
+          };
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < npos) chunk2(lane + 32 * i, xr[i]);
+#pragma unroll 1
+          for (int i = 4; i < npos; ++i) {
+            const int c = lane + 32 * i;
+            int4 xs[4];
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) xs[sl] = *reinterpret_cast<const int4*>(xq + (c << 4) + sl * slot_stride);
+            chunk2(c, xs);
+          }
+          const int t0 = warp_sum_int((a0[0] >> 6) + (a0[1] >> 4) + (a0[2] >> 2) + a0[3]);
+          const int t1 = warp_sum_int((a1[0] >> 6) + (a1[1] >> 4) + (a1[2] >> 2) + a1[3]);
+          if (lane == 0) {
+            const int n = r0 + st * rps + r;
+            const int e0 = t0 - rowsum[0], e1 = t1 - rowsum[0];
+            pr.y[n] = rescale_elem(__int2float_rn(e0), inv_a[0], inv_w);
+            pr.y[n + 1] = rescale_elem(__int2float_rn(e1), inv_a[0], inv_w);
+            if (pr.acc_out) {
+              pr.acc_out[n] = e0;
+              pr.acc_out[n + 1] = e1;
+            }
+          }
+        }
+      }
+      for (; r < rows; ++r) {
         const uint8_t* wrow = stage + r * row_bytes;
         int acc[MT][4];
 #pragma unroll
