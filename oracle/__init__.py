@@ -77,6 +77,10 @@ def _load():
         ctypes.c_void_p]
     lib.oracle_dequant_dot_f64.restype = None
     lib.oracle_dequant_dot_f64.argtypes = [_i8p, _i8p, _f32p, ctypes.c_float, _i64, _i64, _i64, _f64p]
+    lib.oracle_activation.restype = ctypes.c_double
+    lib.oracle_activation.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.oracle_glu.restype = None
+    lib.oracle_glu.argtypes = [_f32p, _f32p, _i64, ctypes.c_int, _f32p]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -237,3 +241,29 @@ def dequant_dot_f64(q, t, a_scale, w_scale: float) -> np.ndarray:
     y = np.empty((M, N), dtype=np.float64)
     _load().oracle_dequant_dot_f64(q, t, a_scale, ctypes.c_float(w_scale), M, K, N, y)
     return y
+
+
+ACT_SILU = 1
+ACT_GELU_TANH = 2
+
+
+def activation(x: float, act: int) -> float:
+    """The gate activation in double (act 1: SiLU, 2: gelu_pytorch_tanh)."""
+    return float(_load().oracle_activation(float(x), int(act)))
+
+
+def glu(gate, up, act: int) -> np.ndarray:
+    """h = act(gate) * up: the activation rounded once to float, times up in float."""
+    gate = _f32(gate)
+    up = _f32(up)
+    if gate.shape != up.shape:
+        raise ValueError("glu: gate and up differ in shape")
+    h = np.empty(gate.shape, dtype=np.float32)
+    _load().oracle_glu(gate.reshape(-1), up.reshape(-1), gate.size, int(act), h.reshape(-1))
+    return h
+
+
+def bitlinear_forward_glu(gate, up, act: int, g, packed, w_scale: float, N: int, eps: float = 1e-6,
+                          rows=None):
+    """The down projection: y = BitLinear(act(gate) * up)."""
+    return bitlinear_forward(glu(gate, up, act), g, packed, w_scale, N, eps, rows=rows)

@@ -20,6 +20,11 @@
  *           (no bias terms)
  *   [P4-R]  "gguf-gemv", "Requirements" (K a multiple of 128 for I2_S) and its
  *           description of I2_S (codes {0,1,2} -> {-1,0,+1}, one f32 scale)
+ *   [P1-FF] "BitNet Embeddings GGUF Conversion Implementation", section 4.5,
+ *           "FFN per-projection norms" (activation of the gate projection times
+ *           the up projection, then the down projection's own norm and matmul),
+ *           with the activations of section 1's table: SiLU (Qwen3) and
+ *           gelu_pytorch_tanh (Gemma3)
  *
  * Readings where the pages are silent (the same ones the library header states):
  *   - which elements share a byte: byte j of a block holds elements j, 32+j,
@@ -30,6 +35,10 @@
  *   - RMSNorm sum of squares in double in index order, eps added to the mean,
  *     rstd rounded once to float, then (x * rstd) * g in float;
  *   - y = ((float)acc * (1/a_scale)) * (1/w_scale) in float.
+ *   - the down projection's input h = act(gate) * up: the activation evaluated
+ *     in double and rounded once to float, then one float multiply by up;
+ *     SiLU(x) = x / (1 + e^-x), gelu_pytorch_tanh(x) = x/2 (1 + tanh(sqrt(2/pi)
+ *     (x + 0.044715 x^3))).
  * Build with -O2 -ffp-contract=off and no fast-math: every float operation above
  * is a single correctly rounded IEEE operation.
  *
@@ -159,6 +168,25 @@ void oracle_rmsnorm(const float* x, const float* g, int64_t M, int64_t K, float 
       float t = xr[k] * rstd;
       xn[m * K + k] = t * g[k];
     }
+  }
+}
+
+/* [P1-FF]: the gate activation.  act 1: SiLU, act 2: gelu_pytorch_tanh. */
+double oracle_activation(double x, int act) {
+  if (act == 1) return x / (1.0 + exp(-x));
+  if (act == 2) {
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+  }
+  return x;
+}
+
+/* [P1-FF]: h = act(gate) * up elementwise, the input of the down projection. */
+void oracle_glu(const float* gate, const float* up, int64_t count, int act, float* h) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < count; ++i) {
+    float a = (float)oracle_activation((double)gate[i], act);
+    h[i] = a * up[i];
   }
 }
 

@@ -299,3 +299,67 @@ def test_forward_rows_subset(oracle_mod):
     rows = np.array([6, 0, 3])
     part = oracle_mod.bitlinear_forward(x, g, packed, ws, N, rows=rows)
     assert np.array_equal(part, full[rows])
+
+
+# ------------------------------------------- down-projection input (act(gate) * up)
+
+def test_activation_silu_pins(oracle_mod):
+    """SiLU is x times the logistic function (scipy's expit, a library routine);
+    it is 0 at 0, has slope 1/2 there, tends to x for large x and to 0 for very
+    negative x, and silu(x) - silu(-x) = x."""
+    special = pytest.importorskip("scipy.special")
+    act = oracle_mod.ACT_SILU
+    xs = np.linspace(-30.0, 30.0, 1201)
+    for x in xs:
+        ref = x * special.expit(x)
+        assert oracle_mod.activation(x, act) == pytest.approx(ref, rel=1e-14, abs=1e-300)
+    assert oracle_mod.activation(0.0, act) == 0.0
+    assert oracle_mod.activation(1e-8, act) / 1e-8 == pytest.approx(0.5, rel=1e-7)
+    assert oracle_mod.activation(40.0, act) == pytest.approx(40.0, rel=1e-15)
+    assert 0.0 > oracle_mod.activation(-40.0, act) > -1e-15
+    for x in (0.25, 1.0, 3.5, 12.0):
+        assert oracle_mod.activation(x, act) - oracle_mod.activation(-x, act) == pytest.approx(x, rel=1e-14)
+
+
+def test_activation_gelu_tanh_pins(oracle_mod):
+    """gelu_pytorch_tanh approximates x * Phi(x) (Phi from scipy's ndtr) to within
+    5e-4 everywhere (its largest deviation, ~4.7e-4, is near x = -2.7; a wrong or
+    missing cubic term is far outside that); it is 0 at 0 with slope 1/2, tends to
+    x for large x, and gelu(x) - gelu(-x) = x (tanh is odd)."""
+    special = pytest.importorskip("scipy.special")
+    act = oracle_mod.ACT_GELU_TANH
+    xs = np.linspace(-8.0, 8.0, 1601)
+    dev = [abs(oracle_mod.activation(x, act) - x * special.ndtr(x)) for x in xs]
+    assert max(dev) < 5e-4
+    assert max(dev) > 4e-4  # the approximation, not the exact GELU
+    assert oracle_mod.activation(0.0, act) == 0.0
+    assert oracle_mod.activation(1e-8, act) / 1e-8 == pytest.approx(0.5, rel=1e-7)
+    assert oracle_mod.activation(12.0, act) == pytest.approx(12.0, rel=1e-15)
+    assert abs(oracle_mod.activation(-12.0, act)) < 1e-30
+    for x in (0.25, 1.0, 2.7, 6.0):
+        assert oracle_mod.activation(x, act) - oracle_mod.activation(-x, act) == pytest.approx(x, rel=1e-14)
+
+
+@pytest.mark.parametrize("act", [1, 2])
+def test_glu_operation_order(oracle_mod, act):
+    """h = float(act(gate)) * up: with up = 1 it is the activation rounded once to
+    float, with up = 0 it is 0, and otherwise one float multiply of the two."""
+    rng = np.random.default_rng(act)
+    gate = rng.normal(0, 2, (7, 128)).astype(np.float32)
+    up = rng.normal(0, 1, (7, 128)).astype(np.float32)
+    a = np.array([[np.float32(oracle_mod.activation(float(v), act)) for v in r] for r in gate], dtype=np.float32)
+    assert np.array_equal(oracle_mod.glu(gate, np.ones_like(up), act), a)
+    assert not np.any(oracle_mod.glu(gate, np.zeros_like(up), act))
+    assert np.array_equal(oracle_mod.glu(gate, up, act), (a * up).astype(np.float32))
+
+
+def test_glu_forward_is_forward_of_glu(oracle_mod):
+    """The down projection is the plain projection applied to h."""
+    rng = np.random.default_rng(3)
+    M, K, N = 3, 256, 40
+    gate = rng.normal(0, 1, (M, K)).astype(np.float32)
+    up = rng.normal(0, 1, (M, K)).astype(np.float32)
+    g = wl.gen_norm_w(K, seed=4)
+    packed, ws = oracle_mod.pack_i2s(wl.gen_latent_w(N, K, seed=5))
+    y = oracle_mod.bitlinear_forward_glu(gate, up, 1, g, packed, ws, N)
+    assert np.array_equal(y, oracle_mod.bitlinear_forward(oracle_mod.glu(gate, up, 1), g, packed, ws, N))
