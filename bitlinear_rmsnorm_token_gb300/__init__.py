@@ -18,7 +18,7 @@ __all__ = [
     "BitnetError", "lib", "packed_bytes", "pack_i2s", "unpack_i2s", "rmsnorm_quant_a8", "i2s_gemm",
     "bitlinear_forward", "bitlinear_forward_group", "last_device_status", "status_string",
     "FLAG_WEIGHTS_STATIC", "MAX_GROUP", "EXPORTED_FUNCTIONS", "bitlinear_forward_noalloc",
-    "selftest_bounded_wait",
+    "selftest_bounded_wait", "glu", "glu_rmsnorm_quant_a8", "bitlinear_forward_glu", "ACT_SILU", "ACT_GELU_TANH",
 ]
 
 OK = 0
@@ -32,12 +32,14 @@ ERR_SCRATCH_LIMIT = 7
 NOALLOC_SCRATCH_BYTES = 16 << 20
 FLAG_WEIGHTS_STATIC = 1
 MAX_GROUP = 16
+ACT_SILU = 1
+ACT_GELU_TANH = 2
 
 EXPORTED_FUNCTIONS = (
     "bitnet_i2s_packed_bytes", "bitnet_pack_i2s", "bitnet_unpack_i2s", "bitnet_rmsnorm_quant_a8",
     "bitnet_i2s_gemm", "bitnet_bitlinear_forward", "bitnet_bitlinear_forward_group",
     "bitnet_status_string", "bitnet_last_device_status", "bitnet_bitlinear_forward_noalloc",
-    "bitnet_selftest_bounded_wait",
+    "bitnet_selftest_bounded_wait", "bitnet_glu", "bitnet_glu_rmsnorm_quant_a8", "bitnet_bitlinear_forward_glu",
 )
 
 
@@ -90,6 +92,12 @@ def lib(build: bool = False) -> ctypes.CDLL:
     L.bitnet_last_device_status.argtypes = [vp]
     L.bitnet_selftest_bounded_wait.restype = ctypes.c_int
     L.bitnet_selftest_bounded_wait.argtypes = [vp]
+    L.bitnet_glu.restype = ctypes.c_int
+    L.bitnet_glu.argtypes = [vp, vp, ctypes.c_int, i64, vp, vp]
+    L.bitnet_glu_rmsnorm_quant_a8.restype = ctypes.c_int
+    L.bitnet_glu_rmsnorm_quant_a8.argtypes = [vp, vp, ctypes.c_int, vp, i64, i64, f32, vp, vp, vp, vp, vp]
+    L.bitnet_bitlinear_forward_glu.restype = ctypes.c_int
+    L.bitnet_bitlinear_forward_glu.argtypes = [vp, vp, ctypes.c_int, vp, vp, f32, i64, i64, i64, f32, vp, vp]
     _lib = L
     return L
 
@@ -206,6 +214,57 @@ def bitlinear_forward(x, norm_w, packed_w, w_scale: float, N: int, eps: float = 
         _dev(packed_w, torch.uint8, "packed_w"), float(w_scale), M, K, N, float(eps),
         _dev(y, torch.float32, "y"), _stream(stream))
     _check(rc, "bitnet_bitlinear_forward")
+    return y
+
+
+def glu(gate, up, act: int, h=None, stream=None):
+    """h = act(gate) * up elementwise (the down projection's input)."""
+    import torch
+
+    if gate.shape != up.shape:
+        raise ValueError("glu: gate and up differ in shape")
+    if h is None:
+        h = torch.empty_like(gate)
+    rc = lib().bitnet_glu(_dev(gate, torch.float32, "gate"), _dev(up, torch.float32, "up"), int(act), gate.numel(),
+                          _dev(h, torch.float32, "h"), _stream(stream))
+    _check(rc, "bitnet_glu")
+    return h
+
+
+def glu_rmsnorm_quant_a8(gate, up, act: int, norm_w, eps: float = 1e-6, codes=None, a_scale=None, rowsum=None,
+                         xn_out=None, stream=None):
+    """rmsnorm_quant_a8 of act(gate) * up (K <= 3072).  Returns (codes, a_scale, rowsum)."""
+    import torch
+
+    M, K = gate.shape
+    if codes is None:
+        codes = torch.empty((M, K), dtype=torch.int8, device=gate.device)
+    if a_scale is None:
+        a_scale = torch.empty(M, dtype=torch.float32, device=gate.device)
+    rc = lib().bitnet_glu_rmsnorm_quant_a8(
+        _dev(gate, torch.float32, "gate"), _dev(up, torch.float32, "up"), int(act),
+        _dev(norm_w, torch.float32, "norm_w"), M, K, float(eps), _dev(codes, torch.int8, "codes"),
+        _dev(a_scale, torch.float32, "a_scale"), _opt(rowsum, torch.int32, "rowsum"),
+        _opt(xn_out, torch.float32, "xn_out"), _stream(stream))
+    _check(rc, "bitnet_glu_rmsnorm_quant_a8")
+    return codes, a_scale, rowsum
+
+
+def bitlinear_forward_glu(gate, up, act: int, norm_w, packed_w, w_scale: float, N: int, eps: float = 1e-6, y=None,
+                          stream=None):
+    """The down projection: BitLinear(act(gate) * up)."""
+    import torch
+
+    M, K = gate.shape
+    if up.shape != gate.shape:
+        raise ValueError("bitlinear_forward_glu: gate and up differ in shape")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=gate.device)
+    rc = lib().bitnet_bitlinear_forward_glu(
+        _dev(gate, torch.float32, "gate"), _dev(up, torch.float32, "up"), int(act),
+        _dev(norm_w, torch.float32, "norm_w"), _dev(packed_w, torch.uint8, "packed_w"), float(w_scale), M, K, N,
+        float(eps), _dev(y, torch.float32, "y"), _stream(stream))
+    _check(rc, "bitnet_bitlinear_forward_glu")
     return y
 
 

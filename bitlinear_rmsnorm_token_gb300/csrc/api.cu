@@ -233,19 +233,53 @@ int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* 
   return cuda_status(e);
 }
 
-int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w, float w_scale, int64_t M,
-                             int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream) {
-  if (!x || !norm_w || !packed_w || !y) return BITNET_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// The norm + quant launch of a forward: x directly (act == 0), or the down
+// projection's input act(x) * up -- computed as the rows are loaded when they
+// fit registers (K <= 3072), else written to h_buf (M*K floats) first.
+cudaError_t launch_norm_any(const float* x, const float* up, int act, const float* g, int64_t M, int K, float eps,
+                            int8_t* codes_i8, __half* codes_f16, float* a_scale, float* h_buf, bool pdl,
+                            cudaStream_t s) {
+  if (act == 0)
+    return launch_rmsnorm_quant(x, g, M, K, eps, codes_i8, codes_f16, a_scale, nullptr, nullptr, pdl, s);
+  if (rmsnorm_quant_glu_fused_supported(K))
+    return launch_rmsnorm_quant_glu(x, up, act, g, M, K, eps, codes_i8, codes_f16, a_scale, nullptr, nullptr, pdl,
+                                    s);
+  cudaError_t e = launch_glu(x, up, act, M * K, h_buf, s);
+  if (e != cudaSuccess) return e;
+  return launch_rmsnorm_quant(h_buf, g, M, K, eps, codes_i8, codes_f16, a_scale, nullptr, nullptr, pdl, s);
+}
+
+size_t glu_buffer_bytes(int act, int64_t M, int64_t K) {
+  return (act != 0 && !rmsnorm_quant_glu_fused_supported(static_cast<int>(K)))
+             ? ((static_cast<size_t>(M * K) * 4 + 255) & ~size_t(255))
+             : 0;
+}
+
+// bitnet_bitlinear_forward (act == 0) and bitnet_bitlinear_forward_glu: x is the
+// input, or the gate projection's output when act != 0 (the row is act(x) * up).
+int forward_impl(const float* x, const float* up, int act, const float* norm_w, const uint8_t* packed_w,
+                 float w_scale, int64_t M, int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream) {
+  if (!x || !norm_w || !packed_w || !y || (act != 0 && !up)) return BITNET_ERR_INVALID_ARG;
+  if (act != 0 && act != BITNET_ACT_SILU && act != BITNET_ACT_GELU_TANH) return BITNET_ERR_INVALID_ARG;
   if (!(eps > 0.0f) || !(w_scale > 0.0f) || w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
   int rc = check_shape(M, K, N);
   if (rc) return rc;
-  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y)) return BITNET_ERR_MISALIGNED;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y) || (up && !aligned16(up)))
+    return BITNET_ERR_MISALIGNED;
   DeviceContext* ctx;
   if ((rc = device_context(&ctx))) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (decode_fused_supported(M, K) && !decode_split_preferred(M, K)) {
+  const bool fused = act != 0 ? decode_fused_glu_supported(M, K)
+                              : (decode_fused_supported(M, K) && !decode_split_preferred(M, K));
+  if (fused) {
     DecodeJob j = {};
     j.x = x;
+    j.up = up;
+    j.act = act;
     j.g = norm_w;
     j.w = packed_w;
     j.w_scale = w_scale;
@@ -254,6 +288,7 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
     j.y = y;
     return cuda_status(launch_decode(ctx, &j, 1, static_cast<int>(M), eps, true, false, s));
   }
+  const size_t h_bytes = glu_buffer_bytes(act, M, K);
   if (decode_supported(M, K)) {
     // few tokens but long rows: int8 codes through the pool, then the decode
     // kernel.  The norm kernel lets its dependent start only after the kernels
@@ -261,13 +296,13 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
     // may stream its weights before its own dependency wait, overlapping the
     // norm kernel.
     const size_t code_bytes = (static_cast<size_t>(M * K) + 255) & ~size_t(255);
+    const size_t scale_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
     uint8_t* ws = nullptr;
-    if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + static_cast<size_t>(M) * 4, s)))
-      return rc;
+    if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + scale_bytes + h_bytes, s))) return rc;
     int8_t* codes = reinterpret_cast<int8_t*>(ws);
     float* as = reinterpret_cast<float*>(ws + code_bytes);
-    cudaError_t e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, codes, nullptr, as, nullptr,
-                                         nullptr, true, s);
+    float* h = h_bytes ? reinterpret_cast<float*>(ws + code_bytes + scale_bytes) : nullptr;
+    cudaError_t e = launch_norm_any(x, up, act, norm_w, M, static_cast<int>(K), eps, codes, nullptr, as, h, true, s);
     if (e == cudaSuccess) {
       DecodeJob j = {};
       j.codes = codes;
@@ -289,15 +324,19 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
   const bool skinny = gemm_skinny_supported(M, K, N);
   const size_t code_bytes = (static_cast<size_t>(M * K) * 2 + 255) & ~size_t(255);
   const size_t scale_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
-  const size_t gws_bytes = skinny ? gemm_skinny_workspace(ctx, M, K, N) : 0;
+  // rounded up: the workspace ends with 4-byte tile tickets, and h (16-byte
+  // accesses) follows it
+  const size_t gws_bytes = skinny ? ((gemm_skinny_workspace(ctx, M, K, N) + 255) & ~size_t(255)) : 0;
   uint8_t* ws = nullptr;
-  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + scale_bytes + gws_bytes, s))) return rc;
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + scale_bytes + gws_bytes + h_bytes, s)))
+    return rc;
   __half* f16 = reinterpret_cast<__half*>(ws);
   float* as = reinterpret_cast<float*>(ws + code_bytes);
   uint8_t* gws = ws + code_bytes + scale_bytes;
+  float* h = h_bytes ? reinterpret_cast<float*>(ws + code_bytes + scale_bytes + gws_bytes) : nullptr;
   cudaError_t e = gws_bytes ? cudaMemsetAsync(gws, 0, gws_bytes, s) : cudaSuccess;
   if (e == cudaSuccess)
-    e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr, true, s);
+    e = launch_norm_any(x, up, act, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, h, true, s);
   int st = BITNET_OK;
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
@@ -305,6 +344,51 @@ int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t*
   pool_free(ws, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w, float w_scale, int64_t M,
+                             int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream) {
+  return forward_impl(x, nullptr, 0, norm_w, packed_w, w_scale, M, K, N, eps, y, stream);
+}
+
+int bitnet_bitlinear_forward_glu(const float* gate, const float* up, int act, const float* norm_w,
+                                 const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float eps,
+                                 float* y, bitnet_stream_t stream) {
+  if (act == 0) return BITNET_ERR_INVALID_ARG;
+  return forward_impl(gate, up, act, norm_w, packed_w, w_scale, M, K, N, eps, y, stream);
+}
+
+int bitnet_glu(const float* gate, const float* up, int act, int64_t count, float* h, bitnet_stream_t stream) {
+  if (!gate || !up || !h || count < 4 || count % 4 != 0) return BITNET_ERR_INVALID_ARG;
+  if (act != BITNET_ACT_SILU && act != BITNET_ACT_GELU_TANH) return BITNET_ERR_INVALID_ARG;
+  if (!aligned16(gate) || !aligned16(up) || !aligned16(h)) return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  int rc = device_context(&ctx);
+  if (rc) return rc;
+  return cuda_status(launch_glu(gate, up, act, count, h, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bitnet_glu_rmsnorm_quant_a8(const float* gate, const float* up, int act, const float* norm_w, int64_t M,
+                                int64_t K, float eps, int8_t* a_codes, float* a_scale, int32_t* a_rowsum,
+                                float* xn_out, bitnet_stream_t stream) {
+  if (!gate || !up || !norm_w || !a_codes || !a_scale) return BITNET_ERR_INVALID_ARG;
+  if (act != BITNET_ACT_SILU && act != BITNET_ACT_GELU_TANH) return BITNET_ERR_INVALID_ARG;
+  if (!(eps > 0.0f)) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(M, K, 1);
+  if (rc) return rc;
+  if (!rmsnorm_quant_glu_fused_supported(static_cast<int>(K))) return BITNET_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(gate) || !aligned16(up) || !aligned16(norm_w) || !aligned16(a_codes) || !aligned4(a_scale) ||
+      (a_rowsum && !aligned4(a_rowsum)) || (xn_out && !aligned16(xn_out)))
+    return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  return cuda_status(launch_rmsnorm_quant_glu(gate, up, act, norm_w, M, static_cast<int>(K), eps, a_codes, nullptr,
+                                              a_scale, a_rowsum, xn_out, false,
+                                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int bitnet_bitlinear_forward_group(const bitnet_projection* projs, int32_t count, int64_t M, float eps,

@@ -45,7 +45,9 @@ constexpr int kDecLongCopyBytes = 16384;
 constexpr int kDecMaxSlots = 64;
 
 struct DecodeProj {
-  const float* x;
+  const float* x;   // activations, or the gate projection's output when act != 0
+  const float* up;  // act != 0: the up projection's output (the row is act(x) * up)
+  int act;
   const float* g;
   const int8_t* codes;
   const float* a_scale;
@@ -137,7 +139,9 @@ __device__ __forceinline__ void compute_bar() {
 // Short rows and few tokens: registers for two CTAs per SM, so that the next
 // dependent launch can become resident while this one drains.  Long rows and
 // more tokens: one CTA per SM with up to 128 registers per thread.
-template <int MT, bool kFused, bool kLong>
+// kGlu: some projection's row is act(x) * up (the down projection's input),
+// computed as the rows are loaded (register prologue only).
+template <int MT, bool kFused, bool kLong, bool kGlu>
 __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_decode(const __grid_constant__ DecodeParams P, unsigned* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -328,9 +332,11 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
       const float4* x4 = reinterpret_cast<const float4*>(pr.x) + static_cast<int64_t>(m) * G;
       float4 v[kRG];
       int key = 0;
+      const float4* u4 = reinterpret_cast<const float4*>(pr.up) + static_cast<int64_t>(m) * G;
 #pragma unroll
       for (int i = 0; i < kRG; ++i) {
         v[i] = i < nv ? __ldg(x4 + gidx(i)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (kGlu && pr.act != 0 && i < nv) v[i] = glu4(v[i], __ldg(u4 + gidx(i)), pr.act);  // down projection input
         key = max(key, sq_key4(v[i]));
       }
       key = warp_max_int(key);
@@ -764,9 +770,9 @@ __global__ void __launch_bounds__(kDecThreads, (kLong || MT >= 4) ? 1 : 2) k_dec
   }
 }
 
-template <int MT, bool kFused, bool kLong>
+template <int MT, bool kFused, bool kLong, bool kGlu>
 cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err, cudaStream_t s) {
-  auto kern = k_decode<MT, kFused, kLong>;
+  auto kern = k_decode<MT, kFused, kLong, kGlu>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -782,14 +788,14 @@ cudaError_t launch_decode_t(const DecodeParams& P, int grid, size_t smem, bool p
   return cudaLaunchKernelEx(&cfg, kern, P, err);
 }
 
-template <bool kFused, bool kLong>
+template <bool kFused, bool kLong, bool kGlu = false>
 cudaError_t dispatch_m(int mt, const DecodeParams& P, int grid, size_t smem, bool pdl, unsigned* err,
                        cudaStream_t s) {
   switch (mt) {
-    case 1: return launch_decode_t<1, kFused, kLong>(P, grid, smem, pdl, err, s);
-    case 2: return launch_decode_t<2, kFused, kLong>(P, grid, smem, pdl, err, s);
-    case 4: return launch_decode_t<4, kFused, kLong>(P, grid, smem, pdl, err, s);
-    default: return launch_decode_t<8, kFused, kLong>(P, grid, smem, pdl, err, s);
+    case 1: return launch_decode_t<1, kFused, kLong, kGlu>(P, grid, smem, pdl, err, s);
+    case 2: return launch_decode_t<2, kFused, kLong, kGlu>(P, grid, smem, pdl, err, s);
+    case 4: return launch_decode_t<4, kFused, kLong, kGlu>(P, grid, smem, pdl, err, s);
+    default: return launch_decode_t<8, kFused, kLong, kGlu>(P, grid, smem, pdl, err, s);
   }
 }
 
@@ -801,6 +807,11 @@ bool decode_supported(int64_t M, int64_t K) {
 
 bool decode_split_preferred(int64_t M, int64_t K) {
   return decode_supported(M, K) && K > 16384 && K % 2048 == 0;
+}
+
+bool decode_fused_glu_supported(int64_t M, int64_t K) {
+  return M >= 1 && M <= kDecodeMaxM && K <= 16384 && !decode_split_preferred(M, K) &&
+         register_prologue(true, static_cast<int>(K), static_cast<int>(M)) && decode_supported(M, K);
 }
 
 bool decode_fused_supported(int64_t M, int64_t K) {
@@ -866,6 +877,8 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs_in, in
     const int n_ctas = (j.N + rpc - 1) / rpc;
     DecodeProj& p = P.p[i];
     p.x = j.x;
+    p.up = j.up;
+    p.act = j.act;
     p.g = j.g;
     p.codes = j.codes;
     p.a_scale = j.a_scale;
@@ -919,9 +932,15 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs_in, in
   const size_t smem = static_cast<size_t>(layout_total(P.ring_bytes));
   if (smem > static_cast<size_t>(kSmemMax)) return cudaErrorInvalidConfiguration;  // unreachable with the dispatch limits
   const bool pdl = true;  // without prefetch permission every read waits for the previous kernel
-  if (lng)
+  bool glu = false;
+  for (int i = 0; i < njobs; ++i) glu = glu || jobs[i].act != 0;
+  if (glu && !fused) return cudaErrorInvalidValue;  // the activation runs in the fused prologue only
+  if (lng) {
+    if (glu) return dispatch_m<true, true, true>(mt, P, cta, smem, pdl, ctx->err_word, s);
     return fused ? dispatch_m<true, true>(mt, P, cta, smem, pdl, ctx->err_word, s)
                  : dispatch_m<false, true>(mt, P, cta, smem, pdl, ctx->err_word, s);
+  }
+  if (glu) return dispatch_m<true, false, true>(mt, P, cta, smem, pdl, ctx->err_word, s);
   return fused ? dispatch_m<true, false>(mt, P, cta, smem, pdl, ctx->err_word, s)
                : dispatch_m<false, false>(mt, P, cta, smem, pdl, ctx->err_word, s);
 }

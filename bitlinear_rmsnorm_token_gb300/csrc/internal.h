@@ -53,6 +53,15 @@ cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int 
                                  __half* codes_f16, float* a_scale, int32_t* rowsum, float* xn_out,
                                  bool pdl, cudaStream_t s);
 
+// The down projection's input h = act(gate) * up (act 1: SiLU, 2: tanh GELU):
+// fused into the norm launch for K <= 3072, or elementwise into h (count a
+// multiple of 4).
+bool rmsnorm_quant_glu_fused_supported(int K);
+cudaError_t launch_rmsnorm_quant_glu(const float* gate, const float* up, int act, const float* g, int64_t M, int K,
+                                     float eps, int8_t* codes_i8, __half* codes_f16, float* a_scale, int32_t* rowsum,
+                                     float* xn_out, bool pdl, cudaStream_t s);
+cudaError_t launch_glu(const float* gate, const float* up, int act, int64_t count, float* h, cudaStream_t s);
+
 // int8 codes -> fp16 codes (for the tensor-core path of the int8 API).
 cudaError_t launch_codes_to_f16(const int8_t* codes, __half* out, int64_t count, cudaStream_t s);
 
@@ -64,7 +73,9 @@ constexpr int64_t kDecodeMaxCodeBytes = 65536;  // M * K bytes of codes held in 
 constexpr int64_t kDecodeFusedMaxStageBytes = 144 * 1024;
 
 struct DecodeJob {
-  const float* x;          // fused: activations [M, K]
+  const float* x;          // fused: activations [M, K] (act != 0: the gate projection's output)
+  const float* up;         // fused, act != 0: the up projection's output [M, K]
+  int act;                 // 0, or the activation of the down-projection input act(x) * up
   const float* g;          // fused: norm weight [K]
   const int8_t* codes;     // unfused: int8 codes [M, K]
   const float* a_scale;    // unfused: activation scales [M]
@@ -77,6 +88,7 @@ struct DecodeJob {
 };
 bool decode_supported(int64_t M, int64_t K);        // codes given (int8 in global memory)
 bool decode_fused_supported(int64_t M, int64_t K);  // norm + quant in the same launch
+bool decode_fused_glu_supported(int64_t M, int64_t K);  // the same, with the down-projection input
 // Few tokens with long rows (K >= 8192, a multiple of 2048): a separate norm
 // kernel with one CTA per row, then the decode kernel streaming weights
 // during it, beats every CTA normalising the whole row in its prologue.

@@ -41,12 +41,16 @@ __device__ __forceinline__ void store_codes4<__half>(__half* dst, float4 n, floa
 // kNC > 0: the row (at most kNC float4 groups per lane; exactly kNC when kExact,
 // which spares the predicated-off groups) is loaded once into registers;
 // kNC == 0: any K, the row is read three times (L1/L2 after the first).
-template <typename OutT, int kNC, bool kExact>
+// kGlu (kNC > 0 only): the row is act(x) * up, computed as it is loaded.
+template <typename OutT, int kNC, bool kExact, bool kGlu = false>
 __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __restrict__ x, const float* __restrict__ g,
                                                                  int64_t M, int K, float eps, OutT* __restrict__ codes,
                                                                  float* __restrict__ a_scale,
                                                                  int32_t* __restrict__ rowsum,
-                                                                 float* __restrict__ xn_out) {
+                                                                 float* __restrict__ xn_out,
+                                                                 const float* __restrict__ up = nullptr,
+                                                                 int act = 0) {
+  static_assert(!kGlu || kNC > 0, "the activation is applied to rows held in registers");
   // dependents may start only once the kernels before this one have completed
   // (they may then read any input this kernel does not write before their own
   // wait)
@@ -66,8 +70,12 @@ __global__ void __launch_bounds__(kNqWarps * 32) k_rmsnorm_quant(const float* __
   if constexpr (kNC > 0) {
     float4 v[kNC];
 #pragma unroll
-    for (int c = 0; c < kNC; ++c)
-      if (c < nc) v[c] = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
+    for (int c = 0; c < kNC; ++c) {
+      if (c < nc) {
+        v[c] = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
+        if constexpr (kGlu) v[c] = glu4(v[c], __ldg(reinterpret_cast<const float4*>(up + row * K + 4 * lane + 128 * c)), act);
+      }
+    }
     int key = 0;
 #pragma unroll
     for (int c = 0; c < kNC; ++c)
@@ -230,9 +238,10 @@ __global__ void __launch_bounds__(256) k_codes_to_f16(const int8_t* __restrict__
   *reinterpret_cast<uint2*>(out + 4 * t) = o;
 }
 
-template <typename OutT, int kNC, bool kExact = false>
+template <typename OutT, int kNC, bool kExact = false, bool kGlu = false>
 cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
-                      int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
+                      int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s, const float* up = nullptr,
+                      int act = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((M + kNqWarps - 1) / kNqWarps));
   cfg.blockDim = dim3(kNqWarps * 32);
@@ -242,7 +251,8 @@ cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float ep
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant<OutT, kNC, kExact>, x, g, M, K, eps, codes, a_scale, rowsum, xn_out);
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant<OutT, kNC, kExact, kGlu>, x, g, M, K, eps, codes, a_scale, rowsum,
+                            xn_out, up, act);
 }
 
 template <typename OutT>
@@ -280,7 +290,51 @@ cudaError_t launch_nq_k(const float* x, const float* g, int64_t M, int K, float 
   return launch_nq<OutT, 0>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
 }
 
+template <typename OutT>
+cudaError_t launch_nq_glu_k(const float* gate, const float* up, int act, const float* g, int64_t M, int K, float eps,
+                            OutT* codes, float* a_scale, int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
+  switch (K >> 7) {  // the down-projection widths: 2048 (Gemma3), 3072 (Qwen3)
+    case 16:
+      return launch_nq<OutT, 16, true, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+    case 24:
+      return launch_nq<OutT, 24, true, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+    default:
+      break;
+  }
+  if ((K >> 7) <= 8)
+    return launch_nq<OutT, 8, false, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+  return launch_nq<OutT, 24, false, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+}
+
+__global__ void __launch_bounds__(256) k_glu(const float* __restrict__ gate, const float* __restrict__ up, int act,
+                                             int64_t n4, float* __restrict__ h) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n4) return;
+  reinterpret_cast<float4*>(h)[t] = glu4(__ldg(reinterpret_cast<const float4*>(gate) + t),
+                                         __ldg(reinterpret_cast<const float4*>(up) + t), act);
+}
+
 }  // namespace
+
+bool rmsnorm_quant_glu_fused_supported(int K) { return K >= 128 && K % 128 == 0 && (K >> 7) <= 24; }
+
+cudaError_t launch_rmsnorm_quant_glu(const float* gate, const float* up, int act, const float* g, int64_t M, int K,
+                                     float eps, int8_t* codes_i8, __half* codes_f16, float* a_scale, int32_t* rowsum,
+                                     float* xn_out, bool pdl, cudaStream_t s) {
+  if (!rmsnorm_quant_glu_fused_supported(K)) return cudaErrorInvalidValue;
+  if (codes_f16) {
+    if (rowsum) return cudaErrorInvalidValue;
+    return launch_nq_glu_k<__half>(gate, up, act, g, M, K, eps, codes_f16, a_scale, nullptr, xn_out, pdl, s);
+  }
+  return launch_nq_glu_k<int8_t>(gate, up, act, g, M, K, eps, codes_i8, a_scale, rowsum, xn_out, pdl, s);
+}
+
+cudaError_t launch_glu(const float* gate, const float* up, int act, int64_t count, float* h, cudaStream_t s) {
+  const int64_t n4 = count / 4;
+  if (n4 < 1) return cudaSuccess;
+  k_glu<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(gate, up, act, n4, h);
+  return cudaGetLastError();
+}
 
 int64_t rmsnorm_quant_ctas(int64_t M, int K) {
   const int nc = K >> 7;

@@ -260,6 +260,28 @@ __device__ __forceinline__ uint32_t quant_pack2_f16(float a, float b, float a_sc
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// ------------------------------------------------- down-projection input
+// h = act(gate) * up, the input of the down projection ("BitNet Embeddings GGUF
+// Conversion Implementation", section 4.5, "FFN per-projection norms", with the
+// activations of section 1's table): SiLU(x) = x / (1 + e^-x) (Qwen3) and
+// gelu_pytorch_tanh(x) = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (Gemma3),
+// in float with CUDA's expf / tanhf and every other operation rounded on its own
+// (no contraction), so all launch paths produce the same h.
+constexpr int kActSilu = 1;
+constexpr int kActGeluTanh = 2;
+
+__device__ __forceinline__ float act_elem(float x, int act) {
+  if (act == kActSilu) return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x)));
+  const float x3 = __fmul_rn(__fmul_rn(x, x), x);
+  const float z = __fmul_rn(0.7978845608028654f, __fadd_rn(x, __fmul_rn(0.044715f, x3)));
+  return __fmul_rn(__fmul_rn(0.5f, x), __fadd_rn(1.0f, tanhf(z)));
+}
+
+__device__ __forceinline__ float4 glu4(float4 g, float4 u, int act) {
+  return make_float4(__fmul_rn(act_elem(g.x, act), u.x), __fmul_rn(act_elem(g.y, act), u.y),
+                     __fmul_rn(act_elem(g.z, act), u.z), __fmul_rn(act_elem(g.w, act), u.w));
+}
+
 // y = ((float)acc * (1/a_scale)) * (1/w_scale): the reciprocals are passed in.
 __device__ __forceinline__ float rescale_elem(float acc_f, float inv_a, float inv_w) {
   return __fmul_rn(__fmul_rn(acc_f, inv_a), inv_w);

@@ -198,6 +198,44 @@ BITNET_API int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
                                                 int64_t K, int64_t N, float eps, float* y,
                                                 bitnet_stream_t stream);
 
+/* Activations of the down projection's input (the gate projection's activation;
+ * "BitNet Embeddings GGUF Conversion Implementation", section 1's table). */
+#define BITNET_ACT_SILU 1      /* x / (1 + e^-x)                                  (Qwen3)  */
+#define BITNET_ACT_GELU_TANH 2 /* x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))   (Gemma3) */
+
+/* The down projection's input ("BitNet Embeddings GGUF Conversion
+ * Implementation", section 4.5, "FFN per-projection norms": the gate
+ * projection's output through the activation, times the up projection's):
+ *   h[i] = act(gate[i]) * up[i]   for i < count
+ * in float: CUDA's expf / tanhf and every other operation rounded on its own --
+ * the arithmetic every fused path below uses, so they all see the same h.
+ * gate, up, h: device pointers, 16-byte aligned, count a positive multiple of 4;
+ * h may alias gate or up (elementwise).  act: BITNET_ACT_SILU or
+ * BITNET_ACT_GELU_TANH, else BITNET_ERR_INVALID_ARG. */
+BITNET_API int bitnet_glu(const float* gate, const float* up, int act, int64_t count, float* h,
+                          bitnet_stream_t stream);
+
+/* bitnet_rmsnorm_quant_a8 of the rows h = act(gate) * up (gate, up [M, K] fp32)
+ * without writing h: bit for bit bitnet_rmsnorm_quant_a8 applied to the output
+ * of bitnet_glu.  The rows are held in registers: K <= 3072, else
+ * BITNET_ERR_UNSUPPORTED_SHAPE.  Other arguments as bitnet_rmsnorm_quant_a8. */
+BITNET_API int bitnet_glu_rmsnorm_quant_a8(const float* gate, const float* up, int act, const float* norm_w,
+                                           int64_t M, int64_t K, float eps, int8_t* a_codes, float* a_scale,
+                                           int32_t* a_rowsum, float* xn_out, bitnet_stream_t stream);
+
+/* The down projection y[M, N] = BitLinear(act(gate) * up): bit for bit
+ * bitnet_bitlinear_forward applied to the output of bitnet_glu, without writing
+ * h where it can be avoided -- one fused launch for M <= 8 when the rows fit
+ * registers (M = 1 with K <= 3840, or K a multiple of 2048 in [4096, 16384]
+ * with M*K <= 65536); otherwise the norm launch computes h as it loads the rows
+ * (K <= 3072) or h goes through pool memory first (4*M*K bytes more).  gate
+ * and up are [M, K] fp32, 16-byte aligned; the other arguments as
+ * bitnet_bitlinear_forward.  act must be BITNET_ACT_SILU or
+ * BITNET_ACT_GELU_TANH. */
+BITNET_API int bitnet_bitlinear_forward_glu(const float* gate, const float* up, int act, const float* norm_w,
+                                            const uint8_t* packed_w, float w_scale, int64_t M, int64_t K,
+                                            int64_t N, float eps, float* y, bitnet_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 BITNET_API const char* bitnet_status_string(int status);
 

@@ -97,3 +97,23 @@ def test_group_argument_errors(L):
     arr[1].K = 1024
     arr[1].y = ODD.value
     assert g(arr, 2, 1, 1e-6, 0, None) == bn.ERR_MISALIGNED
+
+
+def test_glu_argument_errors(L):
+    f = L.bitnet_bitlinear_forward_glu
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, None) == bn.ERR_INVALID_ARG  # no activation
+    assert f(FAKE, FAKE, 3, FAKE, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, None) == bn.ERR_INVALID_ARG  # unknown one
+    assert f(FAKE, None, 1, FAKE, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, None) == bn.ERR_INVALID_ARG  # no up
+    assert f(FAKE, ODD, 1, FAKE, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, None) == bn.ERR_MISALIGNED
+    assert f(FAKE, FAKE, 2, FAKE, FAKE, 1.0, 1, 100, 1, 1e-6, FAKE, None) == bn.ERR_UNSUPPORTED_SHAPE
+    g = L.bitnet_glu
+    g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    assert g(FAKE, FAKE, 1, 6, FAKE, None) == bn.ERR_INVALID_ARG     # not a multiple of 4
+    assert g(FAKE, FAKE, 7, 8, FAKE, None) == bn.ERR_INVALID_ARG     # unknown activation
+    assert g(FAKE, ODD, 1, 8, FAKE, None) == bn.ERR_MISALIGNED
+    q = L.bitnet_glu_rmsnorm_quant_a8
+    q.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert q(FAKE, FAKE, 1, FAKE, 4, 4096, 1e-6, FAKE, FAKE, None, None, None) == bn.ERR_UNSUPPORTED_SHAPE

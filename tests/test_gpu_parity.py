@@ -38,6 +38,15 @@ def host(t):
     return t.cpu().numpy()
 
 
+def assert_rows_within_tolerance(y, ref, what=""):
+    """The end-to-end row tolerance alone (inputs that differ in the last bits)."""
+    y = np.asarray(y, np.float64)
+    ref = np.asarray(ref, np.float64)
+    nrm = np.linalg.norm(ref, axis=1)
+    rel = np.linalg.norm(y - ref, axis=1)[nrm > 0] / nrm[nrm > 0]
+    assert rel.size == 0 or rel.max() <= REL_L2_TOL, f"{what}: worst row rel-L2 {rel.max():.3e}"
+
+
 def assert_rows_close(y, ref, what=""):
     """The end-to-end contract, row by row."""
     y = np.asarray(y, np.float64)
@@ -453,3 +462,79 @@ def test_full_size_prefill_sampled_rows(oracle_mod, which):
     yh = host(y)
     assert_rows_close(yh[rows], ref, which)
     assert np.isfinite(yh).all()
+
+
+# ------------------------------------------- down projection: act(gate) * up input
+
+def _gate_up(M, K, seed):
+    rng = np.random.default_rng(seed)
+    gate = rng.normal(0.0, 2.0, (M, K)).astype(np.float32)
+    up = rng.normal(0.0, 1.0, (M, K)).astype(np.float32)
+    # edge values of the activations: far tails, zero, tiny
+    edge = np.array([0.0, -0.0, 1e-30, -1e-30, 30.0, -30.0, 90.0, -90.0, 200.0, -200.0, 4.0, -4.0], np.float32)
+    gate[0, : edge.size] = edge
+    return gate, up
+
+
+@pytest.mark.parametrize("act", [bn.ACT_SILU, bn.ACT_GELU_TANH])
+def test_glu_matches_oracle(oracle_mod, act):
+    """h = act(gate) * up against the oracle (activation in double, rounded once):
+    CUDA's expf / tanhf are within a few ulp; where tanh(z) is near -1 the
+    difference is bounded in absolute terms by a few ulp of |gate|."""
+    gate, up = _gate_up(37, 1024, seed=act)
+    h = host(bn.glu(dev(gate), dev(up), act))
+    ref = oracle_mod.glu(gate, up, act)
+    assert np.all(np.isfinite(h))
+    tol = 2e-6 * np.abs(ref) + 4e-7 * np.abs(gate) * np.abs(up) + 1e-37
+    bad = np.abs(h - ref) > tol
+    assert not bad.any(), (gate[bad][:5], h[bad][:5], ref[bad][:5])
+
+
+@pytest.mark.parametrize("K", [640, 2048, 3072, 1152])
+@pytest.mark.parametrize("act", [bn.ACT_SILU, bn.ACT_GELU_TANH])
+def test_glu_norm_is_composition(K, act):
+    """The norm launch that computes act(gate) * up as it loads the rows gives
+    the same bits as bitnet_glu followed by the plain norm launch."""
+    M = 21
+    gate, up = _gate_up(M, K, seed=K + act)
+    g = dev(wl.gen_norm_w(K, seed=K))
+    gd, ud = dev(gate), dev(up)
+    rs1 = torch.empty(M, dtype=torch.int32, device="cuda")
+    xn1 = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    c1, s1, _ = bn.glu_rmsnorm_quant_a8(gd, ud, act, g, wl.EPS, rowsum=rs1, xn_out=xn1)
+    rs2 = torch.empty(M, dtype=torch.int32, device="cuda")
+    xn2 = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    c2, s2, _ = bn.rmsnorm_quant_a8(bn.glu(gd, ud, act), g, wl.EPS, rowsum=rs2, xn_out=xn2)
+    assert torch.equal(c1, c2) and torch.equal(s1, s2) and torch.equal(rs1, rs2) and torch.equal(xn1, xn2)
+
+
+GLU_CASES = [
+    # fused decode launch (rows in registers): Qwen3 and Gemma3 down projections at M=1, long rows
+    (1, 3072, 1024, bn.ACT_SILU), (1, 2048, 640, bn.ACT_GELU_TANH), (1, 8192, 300, bn.ACT_SILU),
+    (3, 12288, 200, bn.ACT_GELU_TANH),
+    # norm launch with the activation (K <= 3072), then the decode launch on int8 codes
+    (2, 3072, 512, bn.ACT_SILU),
+    # h written first (K > 3072, not a register-prologue shape), then norm and decode
+    (1, 4224, 100, bn.ACT_GELU_TANH),
+    # tensor-core paths: split-K (K >= 4096, h through memory) and tokens-as-M (activation in the norm launch)
+    (40, 6144, 300, bn.ACT_SILU), (16, 2048, 640, bn.ACT_GELU_TANH), (300, 3072, 257, bn.ACT_SILU),
+]
+
+
+@pytest.mark.parametrize("M,K,N,act", GLU_CASES)
+def test_forward_glu_matches_composition_and_oracle(oracle_mod, M, K, N, act):
+    gate, up = _gate_up(M, K, seed=M * K + N)
+    g = wl.gen_norm_w(K, seed=N + act)
+    w = wl.gen_latent_w(N, K, seed=K + N)
+    packed, ws = bn.pack_i2s(dev(w))
+    gd, ud, gw = dev(gate), dev(up), dev(g)
+    y = bn.bitlinear_forward_glu(gd, ud, act, gw, packed, ws, N, wl.EPS)
+    h = bn.glu(gd, ud, act)
+    assert torch.equal(y, bn.bitlinear_forward(h, gw, packed, ws, N, wl.EPS))
+    # the GPU's h through the oracle: the same projection; the oracle's own h (activation
+    # rounded from double, a few ulp away): within the row tolerance
+    assert_rows_close(host(y), oracle_mod.bitlinear_forward(host(h), g, host(packed), ws, N, wl.EPS),
+                      f"glu forward M={M} K={K} N={N} (GPU h)")
+    assert_rows_within_tolerance(
+        host(y), oracle_mod.bitlinear_forward_glu(gate, up, act, g, host(packed), ws, N, wl.EPS),
+        f"glu forward M={M} K={K} N={N}")
