@@ -14,7 +14,8 @@ Other workloads (--workload): q_proj_m8 (M=8, K=1024, N=2048), proj (one
 projection, --m/--k/--n), gemma3_prefill
 (seven Gemma3-shaped projections at M=32768 with 1% x20 outlier features),
 qwen3_prefill_stack (28 layers x 7 projections at M=32768), sweep (K, N in
-{1024,4096,8192,16384} x M in {1,16,128,2048,16384}).
+{1024,4096,8192,16384} x M in {1,16,128,2048,16384}), glu_proj (the down
+projection BitLinear(act(gate) * up), --m/--k/--n/--act).
 
 --impl reference times the CPU oracle (test infrastructure, plain C) on the
 host cores on a bounded sample of the same workload.
@@ -550,6 +551,70 @@ def run_proj(args, rank, world, local):
                        "launch": "CUDA graph of bitnet_bitlinear_forward_noalloc"}}
 
 
+def run_glu_proj(args, rank, world, local):
+    """The down projection y = BitLinear(act(gate) * up) (--m, --k, --n, --act): few
+    tokens as a CUDA graph cycling distinct weight tensors totalling more than twice
+    the L2, many tokens eagerly (the norm launch computes the activation as it loads
+    the rows; pool memory for the intermediates)."""
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    import oracle
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    M, K, N, act = args.m, args.k, args.n, args.act
+    wb = N * K // 4
+    nw = min(1024, max(2, int(np.ceil(2.0 * L2_BYTES / wb)))) if M <= 8 else 1
+    ws_list = []
+    for i in range(nw):
+        w = wl.gen_device((N, K), wl.seed_for(6, K, N, i), device, std=0.02)
+        ws_list.append(bn.pack_i2s(w))
+        del w
+    g = torch.from_numpy(wl.gen_norm_w(K, seed=K)).to(device)
+    gate = wl.gen_device((M, K), wl.seed_for(6, M, K, 1), device) * 2.0
+    up = wl.gen_device((M, K), wl.seed_for(6, M, K, 2), device)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def cycle():
+        for packed, sc in ws_list:
+            bn.bitlinear_forward_glu(gate, up, act, g, packed, sc, N, wl.EPS, y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        cycle()
+    stream.synchronize()
+    if M <= 8:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            cycle()
+        reps = max(1, args.steps // nw)
+        with torch.cuda.stream(stream):
+            ms = time_region(torch, stream, graph.replay, reps, max(1, min(args.warmup, 3))) / nw
+        launch = "CUDA graph of bitnet_bitlinear_forward_glu"
+    else:
+        reps = max(1, args.steps)
+        with torch.cuda.stream(stream):
+            ms = time_region(torch, stream, cycle, reps, max(1, min(args.warmup, 3)))
+        launch = "bitnet_bitlinear_forward_glu, eager"
+    rows = np.arange(M) if M <= 64 else np.random.default_rng(0).choice(M, 32, replace=False)
+    packed, sc = ws_list[-1]
+    ref = oracle.bitlinear_forward_glu(gate[rows].cpu().numpy(), up[rows].cpu().numpy(), act, g.cpu().numpy(),
+                                       packed.cpu().numpy(), sc, N)
+    yy = y[rows].cpu().numpy()
+    worst = float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max())
+    b = wb + 4 + 2 * M * K * 4 + K * 4 + M * N * 4
+    hbm, bf16, _, _ = peaks()
+    return {"metric": METRIC, "value": round(b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": reps * nw, "ms_per_step": ms, "us_per_projection": ms * 1e3,
+            "tops": 2.0 * M * N * K / (ms * 1e-3) / 1e12, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm,
+            "tensor_frac": 2.0 * M * N * K / (ms * 1e-3) / 1e12 / bf16,
+            "config": {"workload": f"down_glu_M{M}_K{K}_N{N}_act{act}", "weights_cycled": nw, "launch": launch,
+                       "bytes_per_step": b},
+            "parity": {"oracle_worst_row_rel_l2": worst}}
+
+
 def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, outlier_frac, stream):
     """Buffers for one layer's projections at M tokens (x drawn on the device)."""
     items = []
@@ -709,10 +774,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_decode_layer",
                     choices=["qwen3_decode_layer", "q_proj_m8", "gemma3_prefill", "qwen3_prefill_stack", "sweep",
-                             "proj"])
+                             "proj", "glu_proj"])
     ap.add_argument("--m", type=int, default=16, help="--workload proj: tokens")
     ap.add_argument("--k", type=int, default=16384, help="--workload proj: input features")
     ap.add_argument("--n", type=int, default=16384, help="--workload proj: output features")
+    ap.add_argument("--act", type=int, default=1, help="--workload glu_proj: 1 SiLU, 2 tanh GELU")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -730,6 +796,8 @@ def main():
         out = run_sweep(args, rank, world, local)
     elif args.workload == "proj":
         out = run_proj(args, rank, world, local)
+    elif args.workload == "glu_proj":
+        out = run_glu_proj(args, rank, world, local)
     else:
         out = run_prefill(args, rank, world, local, args.workload)
     if rank == 0 and out is not None:
