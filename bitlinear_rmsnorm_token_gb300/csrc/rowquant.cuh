@@ -264,17 +264,22 @@ __device__ __forceinline__ uint32_t quant_pack2_f16(float a, float b, float a_sc
 // h = act(gate) * up, the input of the down projection ("BitNet Embeddings GGUF
 // Conversion Implementation", section 4.5, "FFN per-projection norms", with the
 // activations of section 1's table): SiLU(x) = x / (1 + e^-x) (Qwen3) and
-// gelu_pytorch_tanh(x) = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (Gemma3),
-// in float with CUDA's expf / tanhf and every other operation rounded on its own
-// (no contraction), so all launch paths produce the same h.
+// gelu_pytorch_tanh(x) = x/2 (1 + tanh(z)), z = sqrt(2/pi) (x + 0.044715 x^3)
+// (Gemma3).  Since (1 + tanh z) / 2 = 1 / (1 + e^-2z), both are x / (1 + e^-t)
+// with t = x or 2z: evaluated as x * rcp(1 + expf(-t)) (CUDA's expf, a correctly
+// rounded reciprocal, every operation rounded on its own), which needs no divide
+// and, for very negative x, keeps its relative accuracy where 1 + tanh(z) would
+// cancel.  All launch paths use this one function, so they all see the same h.
 constexpr int kActSilu = 1;
 constexpr int kActGeluTanh = 2;
 
 __device__ __forceinline__ float act_elem(float x, int act) {
-  if (act == kActSilu) return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x)));
-  const float x3 = __fmul_rn(__fmul_rn(x, x), x);
-  const float z = __fmul_rn(0.7978845608028654f, __fadd_rn(x, __fmul_rn(0.044715f, x3)));
-  return __fmul_rn(__fmul_rn(0.5f, x), __fadd_rn(1.0f, tanhf(z)));
+  float t = x;
+  if (act == kActGeluTanh) {
+    const float x3 = __fmul_rn(__fmul_rn(x, x), x);
+    t = __fmul_rn(1.5957691216057308f, __fadd_rn(x, __fmul_rn(0.044715f, x3)));  // 2 sqrt(2/pi) (x + 0.044715 x^3)
+  }
+  return __fmul_rn(x, __frcp_rn(__fadd_rn(1.0f, expf(-t))));
 }
 
 __device__ __forceinline__ float4 glu4(float4 g, float4 u, int act) {

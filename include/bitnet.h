@@ -207,8 +207,10 @@ BITNET_API int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
  * Implementation", section 4.5, "FFN per-projection norms": the gate
  * projection's output through the activation, times the up projection's):
  *   h[i] = act(gate[i]) * up[i]   for i < count
- * in float: CUDA's expf / tanhf and every other operation rounded on its own --
- * the arithmetic every fused path below uses, so they all see the same h.
+ * in float, both activations as x * (1 / (1 + e^-t)) with t = x (SiLU) or
+ * t = 2 sqrt(2/pi) (x + 0.044715 x^3) (tanh GELU: (1 + tanh z) / 2 = 1 / (1 + e^-2z)),
+ * CUDA's expf and a correctly rounded reciprocal, every operation rounded on its
+ * own -- the arithmetic every fused path below uses, so they all see the same h.
  * gate, up, h: device pointers, 16-byte aligned, count a positive multiple of 4;
  * h may alias gate or up (elementwise).  act: BITNET_ACT_SILU or
  * BITNET_ACT_GELU_TANH, else BITNET_ERR_INVALID_ARG. */

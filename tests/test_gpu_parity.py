@@ -479,8 +479,8 @@ def _gate_up(M, K, seed):
 @pytest.mark.parametrize("act", [bn.ACT_SILU, bn.ACT_GELU_TANH])
 def test_glu_matches_oracle(oracle_mod, act):
     """h = act(gate) * up against the oracle (activation in double, rounded once):
-    CUDA's expf / tanhf are within a few ulp; where tanh(z) is near -1 the
-    difference is bounded in absolute terms by a few ulp of |gate|."""
+    the GPU's x * 1/(1 + expf(-t)) is within a few ulp of it, in relative terms
+    except where the result underflows."""
     gate, up = _gate_up(37, 1024, seed=act)
     h = host(bn.glu(dev(gate), dev(up), act))
     ref = oracle_mod.glu(gate, up, act)
