@@ -218,16 +218,17 @@ int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* 
   }
   const bool skinny = gemm_skinny_supported(M, K, N);
   const size_t code_bytes = (static_cast<size_t>(M * K) * 2 + 255) & ~size_t(255);
-  const size_t gws_bytes = skinny ? gemm_skinny_workspace(ctx, M, K, N) : 0;
+  const size_t gws_bytes = skinny ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N);
   uint8_t* buf = nullptr;
   if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&buf), code_bytes + gws_bytes, s))) return rc;
   __half* f16 = reinterpret_cast<__half*>(buf);
+  void* gws = gws_bytes ? static_cast<void*>(buf + code_bytes) : nullptr;
   cudaError_t e = launch_codes_to_f16(a_codes, f16, M * K, s);
   int st = BITNET_OK;
   if (e == cudaSuccess)
-    e = skinny ? launch_gemm_skinny(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, buf + code_bytes,
-                                    false, true, s, &st)
-               : launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, true, s, &st);
+    e = skinny ? launch_gemm_skinny(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, gws, false, true, s,
+                                    &st)
+               : launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, gws, false, true, s, &st);
   pool_free(buf, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);
@@ -326,7 +327,8 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
   const size_t scale_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
   // rounded up: the workspace ends with 4-byte tile tickets, and h (16-byte
   // accesses) follows it
-  const size_t gws_bytes = skinny ? ((gemm_skinny_workspace(ctx, M, K, N) + 255) & ~size_t(255)) : 0;
+  const size_t gws_raw = skinny ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N);
+  const size_t gws_bytes = (gws_raw + 255) & ~size_t(255);
   uint8_t* ws = nullptr;
   if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + scale_bytes + gws_bytes + h_bytes, s)))
     return rc;
@@ -340,7 +342,8 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
   int st = BITNET_OK;
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
-               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, true, s, &st);
+               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws_bytes ? gws : nullptr, true,
+                                true, s, &st);
   pool_free(ws, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);

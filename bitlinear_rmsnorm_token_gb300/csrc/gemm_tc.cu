@@ -33,6 +33,13 @@
 //              tile's MMAs (double-buffered accumulator).  Without a usable
 //              tensor map for y (N % 4 != 0) or with the accumulator test
 //              output, threads store directly.
+// Split K: when the output tiles are too few to give every SM work (a few
+// hundred tokens, long rows), the K blocks of each tile are split into S
+// ranges and the CTAs iterate over (tile, range) units.  A unit's epilogue adds
+// its partial sums to a zeroed fp32 workspace with red.global.add (exact: the
+// partial sums are integers below 2^24, so the order of the additions does not
+// matter); a per-tile ticket lets the unit that completes the tile read the
+// sums back, rescale them and write y.
 // Every wait is bounded; an expired wait sets the device error word and the
 // CTA unwinds without trapping.
 #include "common.cuh"
@@ -50,6 +57,12 @@ constexpr int kPkSlots = 2;                // packed-weight slots (one I2_S bloc
 constexpr int kUnpackWarps = 8;
 constexpr int kThreads = 448;  // warps 0-7 unpack, 8-11 epilogue, 12 producer, 13 MMA
 constexpr int kAStageBytes = kBT * kBK * 2;  // 16 KB of token codes
+
+__device__ __forceinline__ void epi_bar_tc() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add_global_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
 
 template <int BW>
 struct TcLayout {
@@ -73,8 +86,8 @@ template <int BW>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_y, int y_by_tma, const float* __restrict__ a_scale,
-              float inv_w, int M, int N, int K, float* __restrict__ y, int32_t* __restrict__ acc_out,
-              unsigned* err) {
+              float inv_w, int M, int N, int K, int S, float* __restrict__ y, int32_t* __restrict__ acc_out,
+              float* __restrict__ ws, int* __restrict__ tickets, unsigned* err) {
   using L = TcLayout<BW>;
   constexpr int kTpr = kUnpackWarps * 32 / BW;  // unpack threads per weight row (1, 2 or 4)
   constexpr int kCpt = 8 / kTpr;                 // 16-byte chunks of a slab row per thread
@@ -95,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -102,6 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_mt = (M + kBT - 1) / kBT;
   const int num_tiles = n_wt * n_mt;
   const int nkb = K >> 7;
+  const int num_units = num_tiles * S;
+  // unit u: tile u / S, I2_S block columns [kb_lo, kb_hi) of range u % S
+  auto kb_lo = [&](int u) { return static_cast<int>((static_cast<int64_t>(nkb) * (u % S)) / S); };
+  auto kb_hi = [&](int u) { return static_cast<int>((static_cast<int64_t>(nkb) * (u % S + 1)) / S); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -141,10 +159,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int s = 0, sph = 0, p = 0, pph = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const int tile = u / S;
         const int n0 = (tile % n_wt) * BW;
         const int m0 = (tile / n_wt) * kBT;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb_lo(u); kb < kb_hi(u); ++kb) {
           if (!mbar_wait(&pk_empty[p], pph ^ 1, err, abort_flag)) goto producer_done;
           mbar_arrive_expect_tx(&pk_full[p], L::kPkSlotBytes);
           tma_load_2d(sP + p * L::kPkSlotBytes, &tm_w, kb * 32, n0, &pk_full[p]);
@@ -165,13 +184,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kBT, BW);
       int s = 0, sph = 0, tl = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
         const int a = tl & 1;
         if (!mbar_wait(&acc_empty[a], ((tl >> 1) & 1) ^ 1, err, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BW);
         bool ok = true;
-        for (int ks = 0; ks < 2 * nkb; ++ks) {
+        const int nstages = 2 * (kb_hi(u) - kb_lo(u));
+        for (int ks = 0; ks < nstages; ++ks) {
           if (!mbar_wait(&tok_full[s], sph, err, abort_flag) || !mbar_wait(&b_full[s], sph, err, abort_flag)) {
             ok = false;
             break;
@@ -198,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = (t % kTpr) * kCpt;
     uint8_t* const brow = sB + (row >> 3) * 1024 + (row & 7) * 128;
     int s = 0, sph = 0, p = 0, pph = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < nkb; ++kb) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      for (int kb = kb_lo(u); kb < kb_hi(u); ++kb) {
         if (!mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
         uint32_t wd[8];
         {
@@ -236,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* const stg = smem + L::offStg + q * 4096;  // this warp's two 32 x 16 fp32 staging blocks
     const int swz = (lane >> 1) & 3;                  // 64B swizzle of this thread's staging row
     int tl = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tl) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++tl) {
+      const int tile = u / S;
       const int a = tl & 1;
       const int n0 = (tile % n_wt) * BW;
       const int m0 = (tile / n_wt) * kBT;
@@ -245,9 +266,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rows_ok = m0 + q * 32 < M;  // warp-uniform: any of the warp's tokens exist
       // rcp.rn == 1.0f / a_scale in IEEE arithmetic
       const float inv_a = m_ok ? __frcp_rn(__ldg(a_scale + m)) : 0.0f;
-      if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
-      tc_fence_after();
+      // with split K the four epilogue warps meet at named barriers for every
+      // unit, so they leave the loop together: a failed wait only skips the
+      // unit's work and the abort flag is read after the unit's last barrier
+      const bool got = mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag);
+      if (!got && S == 1) break;
+      if (got) tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BW);
+      if (S > 1) {
+        // One range of the tile: add the partial sums to the workspace.  Each
+        // 32 x 32 block (this warp's 32 tokens x 32 columns) is transposed
+        // through the warp's staging buffer (XOR-swizzled: conflict-free both
+        // ways) so that every atomic instruction covers 32 consecutive outputs
+        // of one token.
+        float* const blk = reinterpret_cast<float*>(stg);
+        if (got && rows_ok) {
+#pragma unroll 1
+          for (int j0 = 0; j0 < BW; j0 += 32) {
+            const int nb = n0 + j0;
+            if (nb >= N) break;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(j0), r);
+            tmem_ld_wait();
+            tmem_reg_fence(r);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) blk[lane * 32 + (c ^ lane)] = __uint_as_float(r[c]);
+            __syncwarp();
+            const int col = nb + lane;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+              const int mi = m0 + q * 32 + i;
+              if (mi < M && col < N) red_add_global_f32(ws + static_cast<int64_t>(mi) * N + col, blk[i * 32 + (lane ^ i)]);
+            }
+            __syncwarp();
+          }
+        }
+        // the accumulator has been read: release it to the MMAs of a later unit
+        if (got) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[a]);
+        }
+        // the range that brings the tile's ticket to S writes the tile
+        __threadfence();
+        epi_bar_tc();
+        if (warp == 8 && lane == 0) *last_flag = !*abort_flag && atomicAdd(&tickets[tile], 1) == S - 1;
+        epi_bar_tc();
+        if (*last_flag && rows_ok) {
+          __threadfence();
+          // 32 columns at a time: lane i loads its token's 32 sums (32 loads in
+          // flight), the block is transposed through the staging buffer, and
+          // each store instruction writes 32 consecutive outputs of one token
+#pragma unroll 1
+          for (int j0 = 0; j0 < BW; j0 += 32) {
+            const int nb = n0 + j0;
+            if (nb >= N) break;
+            float v[32];
+            const float* wrow = ws + static_cast<int64_t>(m_ok ? m : m0) * N + nb;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = (m_ok && nb + c < N) ? __ldcg(wrow + c) : 0.0f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) blk[lane * 32 + (c ^ lane)] = v[c];
+            __syncwarp();
+            const int col = nb + lane;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+              const int mi = m0 + q * 32 + i;
+              const float inv_ai = __shfl_sync(0xffffffffu, inv_a, i);
+              if (mi < M && col < N) {
+                const float accf = blk[i * 32 + (lane ^ i)];
+                y[static_cast<int64_t>(mi) * N + col] = rescale_elem(accf, inv_ai, inv_w);
+                if (acc_out) acc_out[static_cast<int64_t>(mi) * N + col] = __float2int_rn(accf);
+              }
+            }
+            __syncwarp();
+          }
+        }
+        epi_bar_tc();  // last_flag is rewritten by the next unit
+        if (*abort_flag) break;
+        continue;
+      }
       if (y_by_tma && rows_ok) {
         const int nch = (min(BW, N - n0) + 31) >> 5;  // 32-column chunks holding outputs
         // rescale the chunk in r (columns n0 + 32 ch ..) and store it as two blocks
@@ -335,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BW>
 cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __half* codes_f16, const float* a_scale,
-                      const uint8_t* packed_w, float inv_w, int M, int N, int K, float* y, int32_t* acc_out, bool pdl,
-                      cudaStream_t s, int* status) {
+                      const uint8_t* packed_w, float inv_w, int M, int N, int K, int S, float* y, int32_t* acc_out,
+                      float* ws, int* tickets, bool pdl, cudaStream_t s, int* status) {
   using L = TcLayout<BW>;
   CUtensorMap tm_tok, tm_w;
   {
@@ -368,7 +466,7 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
   // y through TMA stores: fp32 [M, N], 32-row x 16-column boxes, 64B swizzle (the row
   // pitch N * 4 must be a multiple of 16 bytes)
   CUtensorMap tm_y = tm_tok;  // placeholder, never read unless y_by_tma
-  const int y_by_tma = (N % 4 == 0 && acc_out == nullptr) ? 1 : 0;
+  const int y_by_tma = (N % 4 == 0 && acc_out == nullptr && S == 1) ? 1 : 0;
   if (y_by_tma) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
@@ -385,8 +483,8 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
   auto kern = k_gemm_tc<BW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int tiles = ((N + BW - 1) / BW) * ((M + kBT - 1) / kBT);
-  const int grid = tiles < ctx->num_sms ? tiles : ctx->num_sms;
+  const int units = ((N + BW - 1) / BW) * ((M + kBT - 1) / kBT) * S;
+  const int grid = units < ctx->num_sms ? units : ctx->num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -397,15 +495,54 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, tm_y, y_by_tma, a_scale, inv_w, M, N, K, y, acc_out,
-                            ctx->err_word);
+  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, tm_y, y_by_tma, a_scale, inv_w, M, N, K, S, y, acc_out, ws,
+                            tickets, ctx->err_word);
+}
+
+// Weight-tile width and number of K ranges.  Wide tiles re-read the tokens
+// least; when they leave SMs idle, K is split.  The cost of the busiest CTA is
+// counted per I2_S block column (a token slab plus BW weight rows: 2 + BW/64)
+// with a split unit's atomic additions and read-back as 2 BW more (measured: a
+// split pays only when each range still holds long K); the
+// cheapest option wins, ties to wider tiles and fewer ranges.
+struct TcPlan {
+  int bw, S;
+};
+TcPlan tc_plan(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N, bool can_split) {
+  const int64_t m_tiles = (M + kBT - 1) / kBT;
+  const int nkb = static_cast<int>(K >> 7);
+  TcPlan best = {256, 1};
+  int64_t best_cost = INT64_MAX;
+  for (int bw = 256; bw >= 64; bw >>= 1) {
+    const int64_t tiles = m_tiles * ((N + bw - 1) / bw);
+    const int max_s = can_split ? (nkb < 64 ? nkb : 64) : 1;
+    for (int S = 1; S <= max_s; ++S) {
+      const int64_t units = tiles * S;
+      const int64_t per_cta = (units + ctx->num_sms - 1) / ctx->num_sms;
+      const int64_t cost = per_cta * (((nkb + S - 1) / S) * (2 + bw / 64) + (S > 1 ? 2 * bw : 0));
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = {bw, S};
+      }
+    }
+  }
+  return best;
 }
 
 }  // namespace
 
+size_t gemm_tc_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N) {
+  const TcPlan pl = tc_plan(ctx, M, K, N, true);
+  if (pl.S == 1) return 0;
+  const int64_t tiles = ((M + kBT - 1) / kBT) * ((N + pl.bw - 1) / pl.bw);
+  return ((static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255)) +
+         static_cast<size_t>(tiles) * 4;
+}
+
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
                            const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
-                           int32_t* acc_out, bool pdl, cudaStream_t s, int* status) {
+                           int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
+                           int* status) {
   *status = BITNET_OK;
   EncodeTiledFn encode = encode_tiled_fn();
   if (!encode) {
@@ -414,17 +551,30 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
   }
   const float inv_w = 1.0f / w_scale;  // IEEE division, as in the oracle
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  // widest weight tile that still gives every SM a tile
-  const int64_t m_tiles = (M + kBT - 1) / kBT;
-  int bw = 256;
-  while (bw > 64 && m_tiles * ((N + bw - 1) / bw) < ctx->num_sms) bw >>= 1;
-  switch (bw) {
+  // the same plan gemm_tc_workspace sized the workspace for; none: no split
+  const TcPlan pl = tc_plan(ctx, M, K, N, workspace != nullptr);
+  float* ws = nullptr;
+  int* tickets = nullptr;
+  if (pl.S > 1) {
+    const int64_t tiles = ((M + kBT - 1) / kBT) * ((N + pl.bw - 1) / pl.bw);
+    const size_t part = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255);
+    ws = static_cast<float*>(workspace);
+    tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + part);
+    if (!workspace_zeroed) {
+      cudaError_t e = cudaMemsetAsync(workspace, 0, part + static_cast<size_t>(tiles) * 4, s);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  switch (pl.bw) {
     case 64:
-      return launch_bw<64>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, y, acc_out, pdl, s, status);
+      return launch_bw<64>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, y, acc_out, ws, tickets,
+                           pdl, s, status);
     case 128:
-      return launch_bw<128>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, y, acc_out, pdl, s, status);
+      return launch_bw<128>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, y, acc_out, ws,
+                            tickets, pdl, s, status);
     default:
-      return launch_bw<256>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, y, acc_out, pdl, s, status);
+      return launch_bw<256>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, y, acc_out, ws,
+                            tickets, pdl, s, status);
   }
 }
 

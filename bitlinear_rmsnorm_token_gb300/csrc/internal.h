@@ -99,10 +99,15 @@ bool decode_split_preferred(int64_t M, int64_t K);
 cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int njobs, int M, float eps, bool fused,
                           bool weights_static, cudaStream_t s, int reserve_sms = 0);
 
-// Tensor-core (tcgen05) contraction on fp16 codes.
+// Tensor-core (tcgen05) contraction on fp16 codes, tokens as the MMA's M side.
+// When its output tiles would leave SMs idle it splits K: it then needs
+// gemm_tc_workspace() bytes of device memory, zero on entry (zeroed here on the
+// stream unless workspace_zeroed); with a null workspace it does not split.
+size_t gemm_tc_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
                            const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
-                           int32_t* acc_out, bool pdl, cudaStream_t s, int* status);
+                           int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
+                           int* status);
 
 // Tensor-core contraction for 9..128 tokens (weights as the MMA's M side, K
 // split across CTAs).  Needs gemm_skinny_workspace() bytes of device memory

@@ -118,19 +118,22 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
     return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
   }
   __half* f16 = static_cast<__half*>(scratch);
-  // up to 128 tokens: the split-K contraction, when its workspace also fits
+  // up to 128 tokens: the split-K contraction, when its workspace also fits;
+  // the tokens-as-M contraction splits K too when its workspace fits
   const size_t scale_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
-  const size_t gws_bytes = gemm_skinny_supported(M, K, N) ? gemm_skinny_workspace(ctx, M, K, N) : 0;
-  const bool skinny = gemm_skinny_supported(M, K, N) &&
-                      code_bytes + scale_bytes + gws_bytes <= static_cast<size_t>(BITNET_NOALLOC_SCRATCH_BYTES);
+  const bool sk_shape = gemm_skinny_supported(M, K, N);
+  const size_t gws_bytes = sk_shape ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N);
+  const bool fits = code_bytes + scale_bytes + gws_bytes <= static_cast<size_t>(BITNET_NOALLOC_SCRATCH_BYTES);
+  const bool skinny = sk_shape && fits;
   uint8_t* gws = static_cast<uint8_t*>(scratch) + code_bytes + scale_bytes;
-  cudaError_t e = skinny && gws_bytes ? cudaMemsetAsync(gws, 0, gws_bytes, s) : cudaSuccess;
+  void* tc_ws = (!sk_shape && fits && gws_bytes) ? static_cast<void*>(gws) : nullptr;
+  cudaError_t e = (fits && gws_bytes) ? cudaMemsetAsync(gws, 0, gws_bytes, s) : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr, true, s);
   int st = BITNET_OK;
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
-               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, true, s, &st);
+               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, tc_ws, true, true, s, &st);
   if (st != BITNET_OK) return st;
   return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
 }
