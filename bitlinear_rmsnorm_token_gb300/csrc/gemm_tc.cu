@@ -51,9 +51,8 @@ namespace bitnet {
 namespace {
 
 constexpr int kBT = 128;                   // tokens per tile (MMA M)
-constexpr int kBK = 64;                    // K per stage: one 128-byte swizzle row of fp16
-constexpr int kStages = 4;                 // operand stages
-constexpr int kPkSlots = 2;                // packed-weight slots (one I2_S block column = two stages each)
+constexpr int kBK = 64;                    // K per sub-slab: one 128-byte swizzle row of fp16
+constexpr int kPkSlots = 2;                // packed-weight slots (one I2_S block column each)
 constexpr int kUnpackWarps = 8;
 constexpr int kThreads = 448;  // warps 0-7 unpack, 8-11 epilogue, 12 producer, 13 MMA
 constexpr int kAStageBytes = kBT * kBK * 2;  // 16 KB of token codes
@@ -64,17 +63,27 @@ __device__ __forceinline__ void red_add_global_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// A stage holds kSub 64-wide K sub-slabs of both operands, and the MMA thread
+// waits once per stage.  A wait of the issuing thread behind MMAs still in
+// flight costs a few hundred cycles (measured on sm_103a: ~240 cycles, with
+// ~45 more per issued instruction), so a stage must carry enough MMA work to
+// hide it: 4 MMAs of N=256 (512 cycles) do; narrower tiles take 128-wide
+// stages (8 MMAs per wait).
 template <int BW>
 struct TcLayout {
-  static constexpr int kBStageBytes = BW * kBK * 2;
+  static constexpr int kSub = BW == 256 ? 1 : 2;         // 64-wide sub-slabs per stage
+  static constexpr int kStages = BW == 128 ? 3 : 4;      // ~192 KB of operand stages
+  static constexpr int kSubBBytes = BW * kBK * 2;        // one sub-slab of weights (fp16)
+  static constexpr int kAStage = kSub * kAStageBytes;
+  static constexpr int kBStage = kSub * kSubBBytes;
   static constexpr int kPkSlotBytes = BW * 32;
   static constexpr int offA = 0;
-  static constexpr int offB = offA + kStages * kAStageBytes;
-  static constexpr int offP = offB + kStages * kBStageBytes;
+  static constexpr int offB = offA + kStages * kAStage;
+  static constexpr int offP = offB + kStages * kBStage;
   static constexpr int offStg = offP + kPkSlots * kPkSlotBytes;  // 1 KB aligned: all sizes above are
   static constexpr int kStgBytes = 4 * 2 * 32 * 16 * 4;          // two 32 x 16 fp32 blocks per epilogue warp
   static constexpr int offBar = offStg + kStgBytes;
-  static constexpr int kNumBars = 3 * kStages + 2 * kPkSlots + 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kPkSlots + 4;
   static constexpr int offMisc = offBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KB
@@ -99,10 +108,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + L::offB;
   uint8_t* sP = smem + L::offP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
-  uint64_t* tok_full = bars;
-  uint64_t* b_full = bars + kStages;
-  uint64_t* st_empty = bars + 2 * kStages;
-  uint64_t* pk_full = bars + 3 * kStages;
+  // full[s]: the token slabs have landed (producer's expect-tx arrival plus the
+  // bytes) and every unpack warp has written its weight rows; one wait per stage
+  uint64_t* full = bars;
+  uint64_t* st_empty = bars + L::kStages;
+  uint64_t* pk_full = bars + 2 * L::kStages;
   uint64_t* pk_empty = pk_full + kPkSlots;
   uint64_t* acc_full = pk_empty + kPkSlots;
   uint64_t* acc_empty = acc_full + 2;
@@ -122,9 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kb_hi = [&](int u) { return static_cast<int>((static_cast<int64_t>(nkb) * (u % S + 1)) / S); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&tok_full[i], 1);
-      mbar_init(&b_full[i], kUnpackWarps);
+    for (int i = 0; i < L::kStages; ++i) {
+      mbar_init(&full[i], 1 + kUnpackWarps);
       mbar_init(&st_empty[i], 1);
     }
     for (int i = 0; i < kPkSlots; ++i) {
@@ -170,10 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++p == kPkSlots) { p = 0; pph ^= 1; }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto producer_done;
-            mbar_arrive_expect_tx(&tok_full[s], kAStageBytes);
-            tma_load_2d(sA + s * kAStageBytes, &tm_tok, kb * 128 + hf * kBK, m0, &tok_full[s]);
-            if (++s == kStages) { s = 0; sph ^= 1; }
+            const int h = hf % L::kSub;
+            if (h == 0) {
+              if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto producer_done;
+              mbar_arrive_expect_tx(&full[s], L::kAStage);
+            }
+            tma_load_2d(sA + s * L::kAStage + h * kAStageBytes, &tm_tok, kb * 128 + hf * kBK, m0, &full[s]);
+            if (h == L::kSub - 1 && ++s == L::kStages) { s = 0; sph ^= 1; }
           }
         }
       }
@@ -190,20 +202,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * BW);
         bool ok = true;
-        const int nstages = 2 * (kb_hi(u) - kb_lo(u));
+        const int nstages = 2 * (kb_hi(u) - kb_lo(u)) / L::kSub;
         for (int ks = 0; ks < nstages; ++ks) {
-          if (!mbar_wait(&tok_full[s], sph, err, abort_flag) || !mbar_wait(&b_full[s], sph, err, abort_flag)) {
+          if (!mbar_wait(&full[s], sph, err, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * kAStageBytes));
-          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + s * L::kBStageBytes));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | kk) != 0 ? 1u : 0u);
+          for (int h = 0; h < L::kSub; ++h) {
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * L::kAStage + h * kAStageBytes));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + s * L::kBStage + h * L::kSubBBytes));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (ks | h | kk) != 0 ? 1u : 0u);
+          }
           tc_commit(&st_empty[s]);
-          if (++s == kStages) { s = 0; sph ^= 1; }
+          if (++s == L::kStages) { s = 0; sph ^= 1; }
         }
         if (!ok) break;
         tc_commit(&acc_full[a]);
@@ -231,20 +246,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          if (!mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto unpack_done;
-          unpack_row_slab<kCpt>(wd, hf, c0, brow + s * L::kBStageBytes, row & 7);
-          // orders this thread's shared-memory accesses (the packed-slot reads
-          // and the slab writes) before later async-proxy accesses: the MMA
-          // reading the slab, the next TMA overwriting the packed slot
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&b_full[s]);
-            // the slot's words have been used by now (every chunk needs all
-            // eight), so its loads are complete: it may be refilled
-            if (hf == 0) mbar_arrive(&pk_empty[p]);
+          const int h = hf % L::kSub;
+          if (h == 0 && !mbar_wait(&st_empty[s], sph ^ 1, err, abort_flag)) goto unpack_done;
+          unpack_row_slab<kCpt>(wd, hf, c0, brow + s * L::kBStage + h * L::kSubBBytes, row & 7);
+          if (h == L::kSub - 1) {
+            // orders this thread's shared-memory accesses (the packed-slot
+            // reads and the slab writes) before later async-proxy accesses:
+            // the MMA reading the slab, the next TMA overwriting the packed slot
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&full[s]);
+              // the slot's words have been used by now (every chunk needs all
+              // eight), so its loads are complete: it may be refilled
+              if (hf == L::kSub - 1) mbar_arrive(&pk_empty[p]);
+            }
+            if (++s == L::kStages) { s = 0; sph ^= 1; }
           }
-          if (++s == kStages) { s = 0; sph ^= 1; }
         }
         if (++p == kPkSlots) { p = 0; pph ^= 1; }
       }
