@@ -425,11 +425,18 @@ cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
 
 }  // namespace
 
-// Used for 9..64 tokens when the weight stream is long enough to pay for the
+// Used for 9..63 tokens when the weight stream is long enough to pay for the
 // split's extra work (zeroing the partial sums, a final pass per tile); below
 // that (K <= 2048 and N <= 8192, a few us) the tokens-as-M kernel is faster.
+// The tokens-as-M kernel's time hardly depends on the token count (its tiles
+// hold 128), while this one's grows with it: measured on GB300, the
+// tokens-as-M kernel is as fast or faster from 64 tokens on, and beyond 2^31
+// multiply-adds (M K N) at any token count (K = N = 16384: 78 against 82 us at
+// 16 tokens, against 173 us at 64; K = 16384, N = 8192, 16 tokens: 56 against
+// 51 us).
 bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N) {
-  return M > kDecodeMaxM && M <= 64 && K >= 128 && K % 128 == 0 && N >= 1 && (K >= 4096 || N >= 16384);
+  return M > kDecodeMaxM && M < 64 && K >= 128 && K % 128 == 0 && N >= 1 && (K >= 4096 || N >= 16384) &&
+         M * K * N <= (int64_t(1) << 31);
 }
 
 size_t gemm_skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N) {

@@ -332,32 +332,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_bar_tc();
         if (*last_flag && rows_ok) {
           __threadfence();
-          // 32 columns at a time: lane i loads its token's 32 sums (32 loads in
-          // flight), the block is transposed through the staging buffer, and
-          // each store instruction writes 32 consecutive outputs of one token
+          // 32 columns at a time, lane = column: each load and each store
+          // instruction covers 32 consecutive sums or outputs of one token
+          // (32 loads in flight per lane).  Lane = token would make every load
+          // touch 32 rows: ~11k cycles per 32-column block instead of ~1k.
 #pragma unroll 1
           for (int j0 = 0; j0 < BW; j0 += 32) {
             const int nb = n0 + j0;
             if (nb >= N) break;
-            float v[32];
-            const float* wrow = ws + static_cast<int64_t>(m_ok ? m : m0) * N + nb;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = (m_ok && nb + c < N) ? __ldcg(wrow + c) : 0.0f;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) blk[lane * 32 + (c ^ lane)] = v[c];
-            __syncwarp();
             const int col = nb + lane;
-#pragma unroll 4
+            const int nrow = min(32, M - (m0 + q * 32));  // tokens of this warp (>= 1)
+            const int64_t base = static_cast<int64_t>(m0 + q * 32) * N + col;
+            const float* wcol = ws + base;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = (i < nrow && col < N) ? __ldcg(wcol + i * N) : 0.0f;
+            float* ycol = y + base;
+#pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const int mi = m0 + q * 32 + i;
               const float inv_ai = __shfl_sync(0xffffffffu, inv_a, i);
-              if (mi < M && col < N) {
-                const float accf = blk[i * 32 + (lane ^ i)];
-                y[static_cast<int64_t>(mi) * N + col] = rescale_elem(accf, inv_ai, inv_w);
-                if (acc_out) acc_out[static_cast<int64_t>(mi) * N + col] = __float2int_rn(accf);
+              if (i < nrow && col < N) {
+                ycol[i * N] = rescale_elem(v[i], inv_ai, inv_w);
+                if (acc_out) acc_out[base + i * N] = __float2int_rn(v[i]);
               }
             }
-            __syncwarp();
           }
         }
         epi_bar_tc();  // last_flag is rewritten by the next unit
@@ -519,9 +517,9 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
 
 // Weight-tile width and number of K ranges.  Wide tiles re-read the tokens
 // least; when they leave SMs idle, K is split.  The cost of the busiest CTA is
-// counted per I2_S block column (a token slab plus BW weight rows: 2 + BW/64)
-// with a split unit's atomic additions and read-back as 2 BW more (measured: a
-// split pays only when each range still holds long K); the
+// counted in units of 10 ns, measured on GB300 with one unit per CTA: an I2_S
+// block column (128 values of K) costs 48 / 53 / 86 at BW = 64 / 128 / 256,
+// and a split unit's atomic additions, ticket and read-back 250 + 9 BW; the
 // cheapest option wins, ties to wider tiles and fewer ranges.
 struct TcPlan {
   int bw, S;
@@ -537,7 +535,8 @@ TcPlan tc_plan(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N, bool c
     for (int S = 1; S <= max_s; ++S) {
       const int64_t units = tiles * S;
       const int64_t per_cta = (units + ctx->num_sms - 1) / ctx->num_sms;
-      const int64_t cost = per_cta * (((nkb + S - 1) / S) * (2 + bw / 64) + (S > 1 ? 2 * bw : 0));
+      const int64_t per_kb = bw == 256 ? 86 : (bw == 128 ? 53 : 48);
+      const int64_t cost = per_cta * (((nkb + S - 1) / S) * per_kb + (S > 1 ? 250 + 9 * bw : 0));
       if (cost < best_cost) {
         best_cost = cost;
         best = {bw, S};

@@ -109,7 +109,7 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
                            int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
                            int* status);
 
-// Tensor-core contraction for 9..128 tokens (weights as the MMA's M side, K
+// Tensor-core contraction for 9..63 tokens (weights as the MMA's M side, K
 // split across CTAs).  Needs gemm_skinny_workspace() bytes of device memory
 // (0 when K is not split), zero on entry: zeroed here on the stream unless
 // workspace_zeroed.

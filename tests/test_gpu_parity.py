@@ -206,9 +206,10 @@ GEMM_CASES = [
     # tensor-core path, tokens as the MMA's M side: 128 tokens x 64/128/256 weights, ragged tails
     (9, 128, 128), (16, 256, 130), (64, 1024, 256), (100, 640, 1000), (40, 2048, 1000), (64, 128, 5000),
     (24, 3072, 2049), (17, 1920, 300), (129, 1024, 384), (300, 3072, 257), (600, 2048, 1024), (1000, 128, 5),
-    # the same kernel with K split over CTAs (few output tiles): exact fp32 atomic partial sums, the
-    # last range of a tile rescales it; ragged token and weight tails
+    # the same kernel with K split over CTAs (few output tiles; 64- and 128-wide tiles): exact fp32
+    # atomic partial sums, the last range of a tile rescales it; ragged token and weight tails
     (128, 16384, 1024), (128, 4096, 4096), (200, 8192, 300), (65, 2048, 2100), (70, 65536, 256),
+    (128, 16384, 2048),
 ]
 
 
