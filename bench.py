@@ -15,7 +15,8 @@ projection, --m/--k/--n), gemma3_prefill
 (seven Gemma3-shaped projections at M=32768 with 1% x20 outlier features),
 qwen3_prefill_stack (28 layers x 7 projections at M=32768), sweep (K, N in
 {1024,4096,8192,16384} x M in {1,16,128,2048,16384}), glu_proj (the down
-projection BitLinear(act(gate) * up), --m/--k/--n/--act).
+projection BitLinear(act(gate) * up), --m/--k/--n/--act).  --io f16|bf16 runs the
+prefill workloads with 16-bit x and y (bitnet_bitlinear_forward_typed).
 
 --impl reference times the CPU oracle (test infrastructure, plain C) on the
 host cores on a bounded sample of the same workload.
@@ -658,8 +659,10 @@ def run_glu_proj(args, rank, world, local):
             "parity": {"oracle_worst_row_rel_l2": worst}}
 
 
-def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, outlier_frac, stream):
-    """Buffers for one layer's projections at M tokens (x drawn on the device)."""
+def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, outlier_frac, stream,
+                            io_dtype=None):
+    """Buffers for one layer's projections at M tokens (x drawn on the device;
+    with io_dtype, x rounded to that 16-bit type and y allocated in it)."""
     items = []
     for i, p in enumerate(shapes):
         x = wl.gen_device((M, p.K), wl.seed_for(config, layer, i, wl.T_X), device)
@@ -671,7 +674,9 @@ def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, out
         w = wl.gen_device((p.N, p.K), wl.seed_for(config, layer, i, wl.T_W), device, std=0.02)
         packed, ws = bn.pack_i2s(w)
         del w
-        y = torch.empty((M, p.N), dtype=torch.float32, device=device)
+        if io_dtype is not None:
+            x = x.to(io_dtype)
+        y = torch.empty((M, p.N), dtype=io_dtype or torch.float32, device=device)
         items.append((p, x, g, packed, ws, y))
     return items
 
@@ -691,31 +696,37 @@ def run_prefill(args, rank, world, local, which):
     else:
         shapes, n_layers, frac, cfg = wl.QWEN3_0P6B_LAYER, wl.QWEN3_0P6B_LAYERS, 0.0, 3
     stream = torch.cuda.Stream(device)
-    layers = [prefill_projection_step(torch, bn, wl, shapes, M, device, cfg, l, frac, stream)
+    io = {"f32": None, "f16": torch.float16, "bf16": torch.bfloat16}[args.io]
+    io_bytes = 4 if io is None else 2
+    layers = [prefill_projection_step(torch, bn, wl, shapes, M, device, cfg, l, frac, stream, io)
               for l in range(n_layers)]
     torch.cuda.synchronize()
 
     def step():
         for items in layers:
             for (p, x, g, packed, ws, y) in items:
-                bn.bitlinear_forward(x, g, packed, ws, p.N, wl.EPS, y, stream=stream)
+                if io is None:
+                    bn.bitlinear_forward(x, g, packed, ws, p.N, wl.EPS, y, stream=stream)
+                else:
+                    bn.bitlinear_forward_typed(x, g, packed, ws, p.N, wl.EPS, y, stream=stream)
 
     with torch.cuda.stream(stream):
         ms = time_region(torch, stream, step, max(1, args.steps), max(1, min(args.warmup, 3)))
     flops = sum(2.0 * M * p.N * p.K for p in shapes) * n_layers
-    alg_bytes = sum(M * p.K * 4 + p.K * 4 + p.N * p.K / 4 + 4 + M * p.N * 4 for p in shapes) * n_layers
+    alg_bytes = sum(M * p.K * io_bytes + p.K * 4 + p.N * p.K / 4 + 4 + M * p.N * io_bytes for p in shapes) * n_layers
     # sampled-row parity of the first and last projection
     worst = 0.0
     rows = np.random.default_rng(0).choice(M, 32, replace=False)
     for (p, x, g, packed, ws, y) in (layers[0][0], layers[-1][-1]):
-        ref = oracle.bitlinear_forward(x[rows].cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws, p.N)
-        yy = y[rows].cpu().numpy()
+        ref = oracle.bitlinear_forward_typed(x[rows].float().cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws,
+                                             p.N, y_dtype={"f32": 0, "f16": 1, "bf16": 2}[args.io])
+        yy = y[rows].float().cpu().numpy()
         worst = max(worst, float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max()))
     ms_all, _, ops_per_s = aggregate(ms * args.steps, flops * args.steps, world)
     ms = ms_all / max(1, args.steps)
     return {"metric": METRIC, "value": round(ops_per_s / 1e12, 2), "unit": "TOPS", "n_gpus": world,
             "ms_per_step": ms, "steps": args.steps, "alg_GBps": alg_bytes * world / (ms * 1e-3) / 1e9,
-            "config": {"workload": which, "tokens": M, "layers": n_layers,
+            "config": {"workload": which, "tokens": M, "layers": n_layers, "io": args.io,
                        "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
             "parity": {"oracle_worst_row_rel_l2": worst}}
 
@@ -822,6 +833,8 @@ def main():
     ap.add_argument("--k", type=int, default=16384, help="--workload proj: input features")
     ap.add_argument("--n", type=int, default=16384, help="--workload proj: output features")
     ap.add_argument("--act", type=int, default=1, help="--workload glu_proj: 1 SiLU, 2 tanh GELU")
+    ap.add_argument("--io", choices=["f32", "f16", "bf16"], default="f32",
+                    help="prefill workloads: element type of x and y (bitnet_bitlinear_forward_typed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

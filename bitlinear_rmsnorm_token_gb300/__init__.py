@@ -19,6 +19,7 @@ __all__ = [
     "bitlinear_forward", "bitlinear_forward_group", "last_device_status", "status_string",
     "FLAG_WEIGHTS_STATIC", "MAX_GROUP", "EXPORTED_FUNCTIONS", "bitlinear_forward_noalloc",
     "selftest_bounded_wait", "glu", "glu_rmsnorm_quant_a8", "bitlinear_forward_glu", "ACT_SILU", "ACT_GELU_TANH",
+    "bitlinear_forward_typed", "DTYPE_F32", "DTYPE_F16", "DTYPE_BF16",
 ]
 
 OK = 0
@@ -34,12 +35,16 @@ FLAG_WEIGHTS_STATIC = 1
 MAX_GROUP = 16
 ACT_SILU = 1
 ACT_GELU_TANH = 2
+DTYPE_F32 = 0
+DTYPE_F16 = 1
+DTYPE_BF16 = 2
 
 EXPORTED_FUNCTIONS = (
     "bitnet_i2s_packed_bytes", "bitnet_pack_i2s", "bitnet_unpack_i2s", "bitnet_rmsnorm_quant_a8",
     "bitnet_i2s_gemm", "bitnet_bitlinear_forward", "bitnet_bitlinear_forward_group",
     "bitnet_status_string", "bitnet_last_device_status", "bitnet_bitlinear_forward_noalloc",
     "bitnet_selftest_bounded_wait", "bitnet_glu", "bitnet_glu_rmsnorm_quant_a8", "bitnet_bitlinear_forward_glu",
+    "bitnet_bitlinear_forward_typed",
 )
 
 
@@ -98,6 +103,9 @@ def lib(build: bool = False) -> ctypes.CDLL:
     L.bitnet_glu_rmsnorm_quant_a8.argtypes = [vp, vp, ctypes.c_int, vp, i64, i64, f32, vp, vp, vp, vp, vp]
     L.bitnet_bitlinear_forward_glu.restype = ctypes.c_int
     L.bitnet_bitlinear_forward_glu.argtypes = [vp, vp, ctypes.c_int, vp, vp, f32, i64, i64, i64, f32, vp, vp]
+    L.bitnet_bitlinear_forward_typed.restype = ctypes.c_int
+    L.bitnet_bitlinear_forward_typed.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, f32, i64, i64, i64, f32, vp,
+                                                 ctypes.c_int, vp]
     _lib = L
     return L
 
@@ -214,6 +222,35 @@ def bitlinear_forward(x, norm_w, packed_w, w_scale: float, N: int, eps: float = 
         _dev(packed_w, torch.uint8, "packed_w"), float(w_scale), M, K, N, float(eps),
         _dev(y, torch.float32, "y"), _stream(stream))
     _check(rc, "bitnet_bitlinear_forward")
+    return y
+
+
+def _dtype_code(t, name, allowed):
+    import torch
+
+    codes = {torch.float32: DTYPE_F32, torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
+    if t.dtype not in codes or codes[t.dtype] not in allowed:
+        raise TypeError(f"{name}: unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def bitlinear_forward_typed(x, norm_w, packed_w, w_scale: float, N: int, eps: float = 1e-6, y=None,
+                            y_dtype=None, stream=None):
+    """bitlinear_forward with x in float32/float16/bfloat16, norm_w in float32/float16
+    and y in float32/float16/bfloat16 (default: x's dtype).  y is the fp32 result of
+    the widened inputs, rounded once to y's dtype."""
+    import torch
+
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=y_dtype if y_dtype is not None else x.dtype, device=x.device)
+    xt = _dtype_code(x, "x", (DTYPE_F32, DTYPE_F16, DTYPE_BF16))
+    gt = _dtype_code(norm_w, "norm_w", (DTYPE_F32, DTYPE_F16))
+    yt = _dtype_code(y, "y", (DTYPE_F32, DTYPE_F16, DTYPE_BF16))
+    rc = lib().bitnet_bitlinear_forward_typed(
+        _dev(x, x.dtype, "x"), xt, _dev(norm_w, norm_w.dtype, "norm_w"), gt, _dev(packed_w, torch.uint8, "packed_w"),
+        float(w_scale), M, K, N, float(eps), _dev(y, y.dtype, "y"), yt, _stream(stream))
+    _check(rc, "bitnet_bitlinear_forward_typed")
     return y
 
 

@@ -228,7 +228,7 @@ int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* 
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, gws, false, true, s,
                                     &st)
-               : launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, gws, false, true, s, &st);
+               : launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, acc_out, gws, false, true, s, &st);
   pool_free(buf, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);
@@ -342,9 +342,86 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
   int st = BITNET_OK;
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
-               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws_bytes ? gws : nullptr, true,
+               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, nullptr, gws_bytes ? gws : nullptr, true,
                                 true, s, &st);
   pool_free(ws, s);
+  if (st != BITNET_OK) return st;
+  return cuda_status(e);
+}
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// The projection with 16-bit x / y and an fp16 norm weight: inputs widened to
+// fp32 exactly, the fp32 path's arithmetic, y rounded once to its type.
+int forward_typed(const void* x, int x_dtype, const void* norm_w, int g_dtype, const uint8_t* packed_w,
+                  float w_scale, int64_t M, int64_t K, int64_t N, float eps, void* y, int y_dtype,
+                  bitnet_stream_t stream) {
+  auto io_type = [](int t) { return t == BITNET_DTYPE_F32 || t == BITNET_DTYPE_F16 || t == BITNET_DTYPE_BF16; };
+  if (!x || !norm_w || !packed_w || !y) return BITNET_ERR_INVALID_ARG;
+  if (!io_type(x_dtype) || !io_type(y_dtype) || (g_dtype != BITNET_DTYPE_F32 && g_dtype != BITNET_DTYPE_F16))
+    return BITNET_ERR_INVALID_ARG;
+  if (x_dtype == BITNET_DTYPE_F32 && g_dtype == BITNET_DTYPE_F32 && y_dtype == BITNET_DTYPE_F32)
+    return forward_impl(static_cast<const float*>(x), nullptr, 0, static_cast<const float*>(norm_w), packed_w,
+                        w_scale, M, K, N, eps, static_cast<float*>(y), stream);
+  if (!(eps > 0.0f) || !(w_scale > 0.0f) || w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
+  int rc = check_shape(M, K, N);
+  if (rc) return rc;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(packed_w) || !aligned16(y)) return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  if ((rc = device_context(&ctx))) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // few tokens (the weight-streaming kernels read and write fp32): the fp32
+  // path on converted copies; otherwise the norm launch reads x as it is
+  const bool few = M <= kDecodeMaxM;
+  const bool skinny = !few && gemm_skinny_supported(M, K, N);
+  const bool x_copy = few && x_dtype != BITNET_DTYPE_F32;
+  const bool y_copy = (few || skinny) && y_dtype != BITNET_DTYPE_F32;
+  const size_t g_bytes = g_dtype != BITNET_DTYPE_F32 ? round256(static_cast<size_t>(K) * 4) : 0;
+  const size_t x_bytes = x_copy ? round256(static_cast<size_t>(M * K) * 4) : 0;
+  const size_t y_bytes = y_copy ? round256(static_cast<size_t>(M * N) * 4) : 0;
+  const size_t code_bytes = few ? 0 : round256(static_cast<size_t>(M * K) * 2);
+  const size_t scale_bytes = few ? 0 : round256(static_cast<size_t>(M) * 4);
+  const size_t gws_bytes =
+      few ? 0 : round256(skinny ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N));
+  const size_t total = g_bytes + x_bytes + y_bytes + code_bytes + scale_bytes + gws_bytes;
+  uint8_t* pool = nullptr;
+  if (total && (rc = pool_alloc(ctx, reinterpret_cast<void**>(&pool), total, s))) return rc;
+  uint8_t* at = pool;
+  auto take = [&](size_t b) {
+    uint8_t* p = b ? at : nullptr;
+    at += b;
+    return p;
+  };
+  float* g32 = reinterpret_cast<float*>(take(g_bytes));
+  float* x32 = reinterpret_cast<float*>(take(x_bytes));
+  float* y32 = reinterpret_cast<float*>(take(y_bytes));
+  __half* f16 = reinterpret_cast<__half*>(take(code_bytes));
+  float* as = reinterpret_cast<float*>(take(scale_bytes));
+  uint8_t* gws = take(gws_bytes);
+  const float* g = g32 ? g32 : static_cast<const float*>(norm_w);
+  cudaError_t e = cudaSuccess;
+  if (g32) e = launch_convert(norm_w, g_dtype, g32, BITNET_DTYPE_F32, K, s);
+  int st = BITNET_OK;
+  if (few) {
+    if (e == cudaSuccess && x32) e = launch_convert(x, x_dtype, x32, BITNET_DTYPE_F32, M * K, s);
+    if (e == cudaSuccess) {
+      st = forward_impl(x32 ? x32 : static_cast<const float*>(x), nullptr, 0, g, packed_w, w_scale, M, K, N, eps,
+                        y32 ? y32 : static_cast<float*>(y), stream);
+      if (st != BITNET_OK) e = cudaErrorUnknown;
+    }
+  } else {
+    if (e == cudaSuccess && gws_bytes) e = cudaMemsetAsync(gws, 0, gws_bytes, s);
+    if (e == cudaSuccess)
+      e = launch_rmsnorm_quant_f16_in(x, x_dtype, g, M, static_cast<int>(K), eps, f16, as, true, s);
+    if (e == cudaSuccess)
+      e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y32 ? y32 : static_cast<float*>(y),
+                                      nullptr, gws, true, true, s, &st)
+                 : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, y_dtype, nullptr,
+                                  gws_bytes ? gws : nullptr, true, true, s, &st);
+  }
+  if (e == cudaSuccess && st == BITNET_OK && y32) e = launch_convert(y32, BITNET_DTYPE_F32, y, y_dtype, M * N, s);
+  if (pool) pool_free(pool, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);
 }
@@ -352,6 +429,12 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
 }  // namespace
 
 extern "C" {
+
+int bitnet_bitlinear_forward_typed(const void* x, int x_dtype, const void* norm_w, int norm_w_dtype,
+                                   const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float eps,
+                                   void* y, int y_dtype, bitnet_stream_t stream) {
+  return forward_typed(x, x_dtype, norm_w, norm_w_dtype, packed_w, w_scale, M, K, N, eps, y, y_dtype, stream);
+}
 
 int bitnet_bitlinear_forward(const float* x, const float* norm_w, const uint8_t* packed_w, float w_scale, int64_t M,
                              int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream) {

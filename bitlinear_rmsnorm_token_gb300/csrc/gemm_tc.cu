@@ -31,8 +31,10 @@
 //              two blocks alternate so that one store reads shared memory
 //              while the other block is filled.  This overlaps the next
 //              tile's MMAs (double-buffered accumulator).  Without a usable
-//              tensor map for y (N % 4 != 0) or with the accumulator test
-//              output, threads store directly.
+//              tensor map for y (row pitch not a multiple of 16 bytes) or with
+//              the accumulator test output, threads store directly.
+//              y is fp32, or fp16 / bf16 (YT: the fp32 result rounded once;
+//              a 16-bit block holds 32 columns in the same 64-byte rows).
 // Split K: when the output tiles are too few to give every SM work (a few
 // hundred tokens, long rows), the K blocks of each tile are split into S
 // ranges and the CTAs iterate over (tile, range) units.  A unit's epilogue adds
@@ -46,6 +48,8 @@
 #include "internal.h"
 #include "rowquant.cuh"
 #include "unpack_f16.cuh"
+
+#include <type_traits>
 
 namespace bitnet {
 namespace {
@@ -91,11 +95,19 @@ struct TcLayout {
   static_assert(kAlloc <= 232448, "over the 227 KB of shared memory a CTA may use");
 };
 
-template <int BW>
+// Two results rounded to a 16-bit type, packed low half first.
+template <typename YT>
+__device__ __forceinline__ uint32_t pack2_out(float a, float b) {
+  const YT lo = round_out<YT>(a), hi = round_out<YT>(b);
+  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
+         (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+}
+
+template <int BW, typename YT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_y, int y_by_tma, const float* __restrict__ a_scale,
-              float inv_w, int M, int N, int K, int S, float* __restrict__ y, int32_t* __restrict__ acc_out,
+              float inv_w, int M, int N, int K, int S, YT* __restrict__ y, int32_t* __restrict__ acc_out,
               float* __restrict__ ws, int* __restrict__ tickets, unsigned* err) {
   using L = TcLayout<BW>;
   constexpr int kTpr = kUnpackWarps * 32 / BW;  // unpack threads per weight row (1, 2 or 4)
@@ -347,12 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = (i < nrow && col < N) ? __ldcg(wcol + i * N) : 0.0f;
-            float* ycol = y + base;
+            YT* ycol = y + base;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float inv_ai = __shfl_sync(0xffffffffu, inv_a, i);
               if (i < nrow && col < N) {
-                ycol[i * N] = rescale_elem(v[i], inv_ai, inv_w);
+                ycol[i * N] = round_out<YT>(rescale_elem(v[i], inv_ai, inv_w));
                 if (acc_out) acc_out[base + i * N] = __float2int_rn(v[i]);
               }
             }
@@ -364,8 +376,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (y_by_tma && rows_ok) {
         const int nch = (min(BW, N - n0) + 31) >> 5;  // 32-column chunks holding outputs
-        // rescale the chunk in r (columns n0 + 32 ch ..) and store it as two blocks
+        // rescale the chunk in r (columns n0 + 32 ch ..) and store it as two
+        // fp32 blocks, or as one block of 16-bit values
         auto emit = [&](const uint32_t(&r)[32], int ch) {
+          if constexpr (sizeof(YT) == 2) {
+            // the store issued two chunks ago, from this buffer, must have read it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            uint8_t* const buf = stg + (ch & 1) * 2048;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 o;
+              o.x = pack2_out<YT>(rescale_elem(__uint_as_float(r[8 * v + 0]), inv_a, inv_w),
+                                  rescale_elem(__uint_as_float(r[8 * v + 1]), inv_a, inv_w));
+              o.y = pack2_out<YT>(rescale_elem(__uint_as_float(r[8 * v + 2]), inv_a, inv_w),
+                                  rescale_elem(__uint_as_float(r[8 * v + 3]), inv_a, inv_w));
+              o.z = pack2_out<YT>(rescale_elem(__uint_as_float(r[8 * v + 4]), inv_a, inv_w),
+                                  rescale_elem(__uint_as_float(r[8 * v + 5]), inv_a, inv_w));
+              o.w = pack2_out<YT>(rescale_elem(__uint_as_float(r[8 * v + 6]), inv_a, inv_w),
+                                  rescale_elem(__uint_as_float(r[8 * v + 7]), inv_a, inv_w));
+              *reinterpret_cast<uint4*>(buf + lane * 64 + ((v ^ swz) << 4)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            // rows >= M and columns >= N of the block are clipped by the copy
+            if (lane == 0) {
+              tma_store_2d(&tm_y, buf, n0 + 32 * ch, m0 + q * 32);
+              bulk_commit_group();
+            }
+            return;
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int col = n0 + 32 * ch + 16 * h;
@@ -385,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            // rows >= M of the block are clipped by the copy
+            // rows >= M and columns >= N of the block are clipped by the copy
             if (lane == 0) {
               tma_store_2d(&tm_y, buf, col, m0 + q * 32);
               bulk_commit_group();
@@ -411,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_reg_fence(ra);
         }
       } else if (!y_by_tma && rows_ok) {
-        float* yrow = y + static_cast<int64_t>(m) * N;
+        YT* yrow = y + static_cast<int64_t>(m) * N;
 #pragma unroll 1
         for (int j0 = 0; j0 < BW; j0 += 32) {
           const int nb = n0 + j0;
@@ -425,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int jj = 0; jj < 32; ++jj) {
             if (nb + jj < N) {
               const float accf = __uint_as_float(r[jj]);
-              yrow[nb + jj] = rescale_elem(accf, inv_a, inv_w);
+              yrow[nb + jj] = round_out<YT>(rescale_elem(accf, inv_a, inv_w));
               if (acc_out) acc_out[static_cast<int64_t>(m) * N + nb + jj] = __float2int_rn(accf);
             }
           }
@@ -447,9 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BW>
+template <int BW, typename YT>
 cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __half* codes_f16, const float* a_scale,
-                      const uint8_t* packed_w, float inv_w, int M, int N, int K, int S, float* y, int32_t* acc_out,
+                      const uint8_t* packed_w, float inv_w, int M, int N, int K, int S, YT* y, int32_t* acc_out,
                       float* ws, int* tickets, bool pdl, cudaStream_t s, int* status) {
   using L = TcLayout<BW>;
   CUtensorMap tm_tok, tm_w;
@@ -479,16 +519,20 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
       return cudaErrorInvalidValue;
     }
   }
-  // y through TMA stores: fp32 [M, N], 32-row x 16-column boxes, 64B swizzle (the row
-  // pitch N * 4 must be a multiple of 16 bytes)
+  // y through TMA stores: [M, N], 32-row boxes of 64-byte rows (16 fp32 or 32
+  // 16-bit columns), 64B swizzle (the row pitch must be a multiple of 16 bytes)
+  constexpr int kYBytes = static_cast<int>(sizeof(YT));
   CUtensorMap tm_y = tm_tok;  // placeholder, never read unless y_by_tma
-  const int y_by_tma = (N % 4 == 0 && acc_out == nullptr && S == 1) ? 1 : 0;
+  const int y_by_tma = ((static_cast<int64_t>(N) * kYBytes) % 16 == 0 && acc_out == nullptr && S == 1) ? 1 : 0;
   if (y_by_tma) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
-    cuuint32_t box[2] = {16, 32};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * kYBytes};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / kYBytes), 32};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = encode(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, es,
+    const CUtensorMapDataType yt = kYBytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : (std::is_same<YT, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    CUresult r = encode(&tm_y, yt, 2, y, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -496,7 +540,7 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
       return cudaErrorInvalidValue;
     }
   }
-  auto kern = k_gemm_tc<BW>;
+  auto kern = k_gemm_tc<BW, YT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   const int units = ((N + BW - 1) / BW) * ((M + kBT - 1) / kBT) * S;
@@ -557,9 +601,9 @@ size_t gemm_tc_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t
 }
 
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
-                           const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
-                           int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
-                           int* status) {
+                           const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, void* y,
+                           int y_dtype, int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl,
+                           cudaStream_t s, int* status) {
   *status = BITNET_OK;
   EncodeTiledFn encode = encode_tiled_fn();
   if (!encode) {
@@ -582,16 +626,25 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
       if (e != cudaSuccess) return e;
     }
   }
-  switch (pl.bw) {
-    case 64:
-      return launch_bw<64>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, y, acc_out, ws, tickets,
-                           pdl, s, status);
-    case 128:
-      return launch_bw<128>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, y, acc_out, ws,
-                            tickets, pdl, s, status);
-    default:
-      return launch_bw<256>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, y, acc_out, ws,
-                            tickets, pdl, s, status);
+  auto go = [&](auto* yt) {
+    using YT = std::remove_pointer_t<decltype(yt)>;
+    switch (pl.bw) {
+      case 64:
+        return launch_bw<64, YT>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, yt, acc_out, ws,
+                                 tickets, pdl, s, status);
+      case 128:
+        return launch_bw<128, YT>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, yt, acc_out, ws,
+                                  tickets, pdl, s, status);
+      default:
+        return launch_bw<256, YT>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, yt, acc_out, ws,
+                                  tickets, pdl, s, status);
+    }
+  };
+  switch (y_dtype) {
+    case BITNET_DTYPE_F32: return go(static_cast<float*>(y));
+    case BITNET_DTYPE_F16: return go(static_cast<__half*>(y));
+    case BITNET_DTYPE_BF16: return go(static_cast<__nv_bfloat16*>(y));
+    default: return cudaErrorInvalidValue;
   }
 }
 

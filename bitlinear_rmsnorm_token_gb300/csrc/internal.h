@@ -52,6 +52,13 @@ int64_t rmsnorm_quant_ctas(int64_t M, int K);
 cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int K, float eps, int8_t* codes_i8,
                                  __half* codes_f16, float* a_scale, int32_t* rowsum, float* xn_out,
                                  bool pdl, cudaStream_t s);
+// The same norm/quant to fp16 codes with x in x_dtype (BITNET_DTYPE_F32, _F16
+// or _BF16), widened to fp32 as it is loaded.
+cudaError_t launch_rmsnorm_quant_f16_in(const void* x, int x_dtype, const float* g, int64_t M, int K, float eps,
+                                        __half* codes_f16, float* a_scale, bool pdl, cudaStream_t s);
+// Element-wise conversion of `count` values between BITNET_DTYPE_* types:
+// widening is exact, narrowing rounds to nearest, ties to even.
+cudaError_t launch_convert(const void* in, int in_dtype, void* out, int out_dtype, int64_t count, cudaStream_t s);
 
 // The down projection's input h = act(gate) * up (act 1: SiLU, 2: tanh GELU):
 // fused into the norm launch for K <= 3072, or elementwise into h (count a
@@ -104,10 +111,11 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
 // gemm_tc_workspace() bytes of device memory, zero on entry (zeroed here on the
 // stream unless workspace_zeroed); with a null workspace it does not split.
 size_t gemm_tc_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
+// y is y_dtype (BITNET_DTYPE_F32, _F16 or _BF16): the fp32 result rounded once.
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
-                           const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
-                           int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
-                           int* status);
+                           const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, void* y,
+                           int y_dtype, int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl,
+                           cudaStream_t s, int* status);
 
 // Tensor-core contraction for 9..63 tokens (weights as the MMA's M side, K
 // split across CTAs).  Needs gemm_skinny_workspace() bytes of device memory

@@ -133,7 +133,7 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   int st = BITNET_OK;
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
-               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, tc_ws, true, true, s, &st);
+               : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, nullptr, tc_ws, true, true, s, &st);
   if (st != BITNET_OK) return st;
   return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
 }

@@ -5,7 +5,9 @@
 // "BitNet Inference Framework", "Quantization (W1.58A8)".  The arithmetic is
 // the shared definition in rowquant.cuh.
 //
-// HBM-bound: it reads x (4 B/elem) once from DRAM and writes 1 B (int8) or 2 B
+// x is fp32, or fp16 / bf16 (InT: widened to fp32 as it is loaded, exactly, so
+// everything after the load is the fp32 definition).
+// HBM-bound: it reads x (4 or 2 B/elem) once from DRAM and writes 1 B (int8) or 2 B
 // (fp16, the tensor-core operand) per element.  The sum of squares, the absmax
 // and the quantisation are three sweeps over the row; rows up to K = 3072 are
 // held in registers, longer ones are re-read through L1/L2.
@@ -43,8 +45,8 @@ __device__ __forceinline__ void store_codes4<__half>(__half* dst, float4 n, floa
 // kNC == 0: any K, the row is read three times (L1/L2 after the first).
 // kGlu (kNC > 0 only): the row is act(x) * up, computed as it is loaded.
 // (kGlu: at most 128 registers, two CTAs per SM, like the plain long-row form)
-template <typename OutT, int kNC, bool kExact, bool kGlu = false>
-__global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(const float* __restrict__ x, const float* __restrict__ g,
+template <typename InT, typename OutT, int kNC, bool kExact, bool kGlu = false>
+__global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(const InT* __restrict__ x, const float* __restrict__ g,
                                                                  int64_t M, int K, float eps, OutT* __restrict__ codes,
                                                                  float* __restrict__ a_scale,
                                                                  int32_t* __restrict__ rowsum,
@@ -52,6 +54,7 @@ __global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(c
                                                                  const float* __restrict__ up = nullptr,
                                                                  int act = 0) {
   static_assert(!kGlu || kNC > 0, "the activation is applied to rows held in registers");
+  static_assert(!kGlu || sizeof(InT) == 4, "the activation form reads fp32 gate and up rows");
   // dependents may start only once the kernels before this one have completed
   // (they may then read any input this kernel does not write before their own
   // wait)
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(c
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kNqWarps + (threadIdx.x >> 5);
   if (row >= M) return;
-  const float* xr = x + row * K + 4 * lane;
+  const InT* xr = x + row * K + 4 * lane;
   const float* gr = g + 4 * lane;
   const int nc = kExact ? kNC : (K >> 7);
   OutT* cr = codes + row * K + 4 * lane;
@@ -73,7 +76,7 @@ __global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(c
 #pragma unroll
     for (int c = 0; c < kNC; ++c) {
       if (c < nc) {
-        v[c] = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
+        v[c] = load4(xr + 128 * c);
         if constexpr (kGlu) v[c] = glu4(v[c], __ldg(reinterpret_cast<const float4*>(up + row * K + 4 * lane + 128 * c)), act);
       }
     }
@@ -110,9 +113,9 @@ __global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(c
       if (rowsum) rowsum[row] = rs;
     }
   } else {
-    const float rstd = warp_row_rstd<true>(x + row * K, K, lane, eps);
+    const float rstd = warp_row_rstd<true, InT>(x + row * K, K, lane, eps);
     for (int c = 0; c < nc; ++c) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
+      const float4 v = load4(xr + 128 * c);
       const float4 gv = __ldg(reinterpret_cast<const float4*>(gr + 128 * c));
       const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
                                    norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(c
     }
     const float as = act_scale_from_amax(warp_max(amax));
     for (int c = 0; c < nc; ++c) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(xr + 128 * c));
+      const float4 v = load4(xr + 128 * c);
       const float4 gv = __ldg(reinterpret_cast<const float4*>(gr + 128 * c));
       const float4 n = make_float4(norm_elem(v.x, rstd, gv.x), norm_elem(v.y, rstd, gv.y),
                                    norm_elem(v.z, rstd, gv.z), norm_elem(v.w, rstd, gv.w));
@@ -141,8 +144,8 @@ __global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(c
 // (float4 groups t, t+T, t+2T, t+3T of the row: every load instruction of a
 // warp is coalesced).  Otherwise 1024 threads loop over the row's float4 groups
 // with the same stride and read the row again from L2 in every pass.
-template <typename OutT, bool kRegs>
-__global__ void __launch_bounds__(1024) k_rmsnorm_quant_rows(const float* __restrict__ x,
+template <typename InT, typename OutT, bool kRegs>
+__global__ void __launch_bounds__(1024) k_rmsnorm_quant_rows(const InT* __restrict__ x,
                                                              const float* __restrict__ g, int K, float eps,
                                                              OutT* __restrict__ codes, float* __restrict__ a_scale,
                                                              int32_t* __restrict__ rowsum,
@@ -166,14 +169,14 @@ __global__ void __launch_bounds__(1024) k_rmsnorm_quant_rows(const float* __rest
     s_amax = 0u;
     s_rs = 0;
   }
-  const float4* xr = reinterpret_cast<const float4*>(x + row * K);
+  const InT* xr = x + row * K;
   const float4* gr = reinterpret_cast<const float4*>(g);
   float4 v[kV];
   if (kRegs) {
 #pragma unroll
-    for (int i = 0; i < kV; ++i) v[i] = __ldg(xr + tid + T * i);
+    for (int i = 0; i < kV; ++i) v[i] = load4(xr + 4 * (tid + T * i));
   }
-  auto xv = [&](int i) { return kRegs ? v[i] : __ldg(xr + tid + T * i); };
+  auto xv = [&](int i) { return kRegs ? v[i] : load4(xr + 4 * (tid + T * i)); };
   __syncthreads();
   int key = 0;
 #pragma unroll 4
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(1024) k_rmsnorm_quant_rows(const float* __rest
   int rs = 0;
 #pragma unroll 4
   for (int i = 0; i < nv; ++i) {
-    const float4 n = kRegs ? v[i] : norm4(__ldg(xr + tid + T * i), __ldg(gr + tid + T * i));
+    const float4 n = kRegs ? v[i] : norm4(load4(xr + 4 * (tid + T * i)), __ldg(gr + tid + T * i));
     store_codes4<OutT>(codes + row * K + 4 * (tid + T * i), n, as, rs);
   }
   if (rowsum) {
@@ -239,8 +242,8 @@ __global__ void __launch_bounds__(256) k_codes_to_f16(const int8_t* __restrict__
   *reinterpret_cast<uint2*>(out + 4 * t) = o;
 }
 
-template <typename OutT, int kNC, bool kExact = false, bool kGlu = false>
-cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
+template <typename InT, typename OutT, int kNC, bool kExact = false, bool kGlu = false>
+cudaError_t launch_nq(const InT* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
                       int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s, const float* up = nullptr,
                       int act = 0) {
   cudaLaunchConfig_t cfg = {};
@@ -252,12 +255,12 @@ cudaError_t launch_nq(const float* x, const float* g, int64_t M, int K, float ep
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant<OutT, kNC, kExact, kGlu>, x, g, M, K, eps, codes, a_scale, rowsum,
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant<InT, OutT, kNC, kExact, kGlu>, x, g, M, K, eps, codes, a_scale, rowsum,
                             xn_out, up, act);
 }
 
-template <typename OutT>
-cudaError_t launch_nq_rows(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
+template <typename InT, typename OutT>
+cudaError_t launch_nq_rows(const InT* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
                            int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   const bool regs = K <= 16384;
@@ -269,26 +272,27 @@ cudaError_t launch_nq_rows(const float* x, const float* g, int64_t M, int K, flo
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (regs) return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant_rows<OutT, true>, x, g, K, eps, codes, a_scale, rowsum, xn_out);
-  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant_rows<OutT, false>, x, g, K, eps, codes, a_scale, rowsum, xn_out);
+  if (regs)
+    return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant_rows<InT, OutT, true>, x, g, K, eps, codes, a_scale, rowsum, xn_out);
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm_quant_rows<InT, OutT, false>, x, g, K, eps, codes, a_scale, rowsum, xn_out);
 }
 
-template <typename OutT>
-cudaError_t launch_nq_k(const float* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
+template <typename InT, typename OutT>
+cudaError_t launch_nq_k(const InT* x, const float* g, int64_t M, int K, float eps, OutT* codes, float* a_scale,
                         int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
   const int nc = K >> 7;
   if (nc > 24 && K % 2048 == 0 && M < (int64_t(1) << 31))  // keep in step with rmsnorm_quant_ctas
-    return launch_nq_rows<OutT>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    return launch_nq_rows<InT, OutT>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
   switch (nc) {  // the model widths of the prefill shapes: K = 640, 1024, 2048, 3072
-    case 5: return launch_nq<OutT, 5, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
-    case 8: return launch_nq<OutT, 8, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
-    case 16: return launch_nq<OutT, 16, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
-    case 24: return launch_nq<OutT, 24, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 5: return launch_nq<InT, OutT, 5, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 8: return launch_nq<InT, OutT, 8, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 16: return launch_nq<InT, OutT, 16, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+    case 24: return launch_nq<InT, OutT, 24, true>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
     default: break;
   }
-  if (nc <= 8) return launch_nq<OutT, 8>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
-  if (nc <= 24) return launch_nq<OutT, 24>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
-  return launch_nq<OutT, 0>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+  if (nc <= 8) return launch_nq<InT, OutT, 8>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+  if (nc <= 24) return launch_nq<InT, OutT, 24>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
+  return launch_nq<InT, OutT, 0>(x, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s);
 }
 
 template <typename OutT>
@@ -296,15 +300,18 @@ cudaError_t launch_nq_glu_k(const float* gate, const float* up, int act, const f
                             OutT* codes, float* a_scale, int32_t* rowsum, float* xn_out, bool pdl, cudaStream_t s) {
   switch (K >> 7) {  // the down-projection widths: 2048 (Gemma3), 3072 (Qwen3)
     case 16:
-      return launch_nq<OutT, 16, true, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+      return launch_nq<float, OutT, 16, true, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up,
+                                                    act);
     case 24:
-      return launch_nq<OutT, 24, true, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+      return launch_nq<float, OutT, 24, true, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up,
+                                                    act);
     default:
       break;
   }
   if ((K >> 7) <= 8)
-    return launch_nq<OutT, 8, false, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
-  return launch_nq<OutT, 24, false, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
+    return launch_nq<float, OutT, 8, false, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up,
+                                                  act);
+  return launch_nq<float, OutT, 24, false, true>(gate, g, M, K, eps, codes, a_scale, rowsum, xn_out, pdl, s, up, act);
 }
 
 __global__ void __launch_bounds__(256) k_glu(const float* __restrict__ gate, const float* __restrict__ up, int act,
@@ -348,9 +355,26 @@ cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int 
                                  cudaStream_t s) {
   if (codes_f16) {
     if (rowsum) return cudaErrorInvalidValue;  // row sums are produced with int8 codes only
-    return launch_nq_k<__half>(x, g, M, K, eps, codes_f16, a_scale, nullptr, xn_out, pdl, s);
+    return launch_nq_k<float, __half>(x, g, M, K, eps, codes_f16, a_scale, nullptr, xn_out, pdl, s);
   }
-  return launch_nq_k<int8_t>(x, g, M, K, eps, codes_i8, a_scale, rowsum, xn_out, pdl, s);
+  return launch_nq_k<float, int8_t>(x, g, M, K, eps, codes_i8, a_scale, rowsum, xn_out, pdl, s);
+}
+
+cudaError_t launch_rmsnorm_quant_f16_in(const void* x, int x_dtype, const float* g, int64_t M, int K, float eps,
+                                        __half* codes_f16, float* a_scale, bool pdl, cudaStream_t s) {
+  switch (x_dtype) {
+    case BITNET_DTYPE_F32:
+      return launch_nq_k<float, __half>(static_cast<const float*>(x), g, M, K, eps, codes_f16, a_scale, nullptr,
+                                        nullptr, pdl, s);
+    case BITNET_DTYPE_F16:
+      return launch_nq_k<__half, __half>(static_cast<const __half*>(x), g, M, K, eps, codes_f16, a_scale, nullptr,
+                                         nullptr, pdl, s);
+    case BITNET_DTYPE_BF16:
+      return launch_nq_k<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(x), g, M, K, eps, codes_f16, a_scale,
+                                                nullptr, nullptr, pdl, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* codes, __half* out, int64_t count, cudaStream_t s) {

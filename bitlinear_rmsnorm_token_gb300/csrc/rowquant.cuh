@@ -19,6 +19,7 @@
 // unless that value lies within ~2^-40 (relative) of a float rounding boundary.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -199,26 +200,53 @@ __device__ __forceinline__ float rstd_from_fixed(unsigned long long acc, int key
   return (j >= -126 && j <= 127) ? __fmul_rn(r, __int_as_float((j + 127) << 23)) : mul_pow2(r, j);
 }
 
-// rstd of a row read by one full warp (global or shared memory).
-template <bool kGlobal>
-__device__ __forceinline__ float warp_row_rstd(const float* __restrict__ xrow, int K, int lane, float eps) {
-  const float* p = xrow + 4 * lane;
+// Four consecutive input elements from global memory, widened to fp32 (exact
+// for fp32, fp16 and bf16 alike: every such value is an fp32 value).
+__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __half* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// An fp32 result rounded once to the output element type (to nearest, ties to
+// even; fp16 overflows to infinity past 65504).
+template <typename T>
+__device__ __forceinline__ T round_out(float v);
+template <>
+__device__ __forceinline__ float round_out<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __half round_out<__half>(float v) { return __float2half_rn(v); }
+template <>
+__device__ __forceinline__ __nv_bfloat16 round_out<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// rstd of a row read by one full warp (global memory of any input type, or
+// fp32 in shared memory).
+template <bool kGlobal, typename InT = float>
+__device__ __forceinline__ float warp_row_rstd(const InT* __restrict__ xrow, int K, int lane, float eps) {
+  static_assert(kGlobal || sizeof(InT) == 4, "rows in shared memory are fp32");
+  const InT* p = xrow + 4 * lane;
   const int nc = K >> 7;
+  auto ld = [&](int c) -> float4 {
+    if constexpr (kGlobal) return load4(p + 128 * c);
+    else return *reinterpret_cast<const float4*>(p + 128 * c);
+  };
   int key = 0;
-  for (int c = 0; c < nc; ++c)
-    key = max(key, sq_key4(kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
-                                   : *reinterpret_cast<const float4*>(p + 128 * c)));
+  for (int c = 0; c < nc; ++c) key = max(key, sq_key4(ld(c)));
   key = warp_max_int(key);
   const float scale = sq_scale(key);
   unsigned long long acc = 0ull;
   for (int c0 = 0; c0 < nc; c0 += 128) {  // folds every 512 elements per lane
     SqPartial part = {0ull, 0u};
     const int c1 = min(nc, c0 + 128);
-    for (int c = c0; c < c1; ++c)
-      sq_add4(part,
-              kGlobal ? __ldg(reinterpret_cast<const float4*>(p + 128 * c))
-                      : *reinterpret_cast<const float4*>(p + 128 * c),
-              scale);
+    for (int c = c0; c < c1; ++c) sq_add4(part, ld(c), scale);
     acc += sq_fold(part, 4 * (c1 - c0));
   }
   return rstd_from_fixed(warp_sum_u64(acc), key, K, eps);

@@ -238,6 +238,34 @@ BITNET_API int bitnet_bitlinear_forward_glu(const float* gate, const float* up, 
                                             const uint8_t* packed_w, float w_scale, int64_t M, int64_t K,
                                             int64_t N, float eps, float* y, bitnet_stream_t stream);
 
+/* Element types of bitnet_bitlinear_forward_typed. */
+#define BITNET_DTYPE_F32 0
+#define BITNET_DTYPE_F16 1  /* IEEE binary16                                       */
+#define BITNET_DTYPE_BF16 2 /* bfloat16: the upper 16 bits of an fp32              */
+
+/* The projection of bitnet_bitlinear_forward with 16-bit input and output
+ * tensors: x[M, K] in x_dtype (F32, F16 or BF16; "gguf-gemv", "Requirements":
+ * f32 or bf16 activations, the output in the input's type), norm_w[K] in
+ * norm_w_dtype (F32 or F16: the conversion stores norm weights as float16,
+ * "BitNet Embeddings GGUF Conversion Implementation", section 6.1) and y[M, N]
+ * in y_dtype (F32, F16 or BF16).
+ * Every input value is widened to fp32 (exact), the projection is computed as
+ * bitnet_bitlinear_forward computes it on the widened values, and y is that
+ * fp32 result rounded once to y_dtype (to nearest, ties to even; fp16 results
+ * beyond 65504 become infinities).  So y equals bitnet_bitlinear_forward of
+ * the widened inputs, rounded.
+ * Layout, alignment (16 bytes), ownership and pool memory as for
+ * bitnet_bitlinear_forward.  From 9 tokens on, the norm launch reads 16-bit x
+ * itself and the tensor-core launch of 64 or more tokens writes 16-bit y
+ * itself; otherwise x and y pass through fp32 copies in pool memory
+ * (M * K * 4 and M * N * 4 bytes), converted by extra launches, as does an
+ * fp16 norm weight (K * 4 bytes).
+ * Errors: BITNET_ERR_INVALID_ARG for an unknown dtype or BF16 norm weights,
+ * otherwise as bitnet_bitlinear_forward. */
+BITNET_API int bitnet_bitlinear_forward_typed(const void* x, int x_dtype, const void* norm_w, int norm_w_dtype,
+                                              const uint8_t* packed_w, float w_scale, int64_t M, int64_t K,
+                                              int64_t N, float eps, void* y, int y_dtype, bitnet_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 BITNET_API const char* bitnet_status_string(int status);
 

@@ -267,3 +267,50 @@ def bitlinear_forward_glu(gate, up, act: int, g, packed, w_scale: float, N: int,
                           rows=None):
     """The down projection: y = BitLinear(act(gate) * up)."""
     return bitlinear_forward(glu(gate, up, act), g, packed, w_scale, N, eps, rows=rows)
+
+
+# ----------------------------------------------------------- 16-bit tensors
+# The 16-bit activations and outputs of "gguf-gemv" ("Requirements": f32 or
+# bf16 activations, the output in the input's type) and the float16 norm
+# weights of "BitNet Embeddings GGUF Conversion Implementation" (section 6.1).
+# Every fp16 / bf16 value is an fp32 value, so widening is exact; narrowing is
+# IEEE 754 rounding to nearest, ties to even, of an fp32 value to a format with
+# 11 (fp16) or 8 (bf16) significand bits.
+
+DTYPE_F32, DTYPE_F16, DTYPE_BF16 = 0, 1, 2
+
+
+def round_bf16(a) -> np.ndarray:
+    """fp32 values rounded to bfloat16 (the upper half of an fp32 pattern), to
+    nearest with ties to even; returned widened to float32.  Finite inputs only
+    (values at or past the largest bfloat16 plus half a unit become infinity)."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    # add half a unit of the kept part, plus one when the kept part is odd
+    # (a tie then carries into an even pattern), and drop the low 16 bits
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).reshape(np.shape(a))
+
+
+def round_f16(a) -> np.ndarray:
+    """fp32 values rounded to IEEE binary16 (nearest, ties to even; past 65504
+    by half a unit or more: infinity), returned widened to float32."""
+    with np.errstate(over="ignore"):
+        return np.asarray(a, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
+def round_to(a, dtype: int) -> np.ndarray:
+    if dtype == DTYPE_F32:
+        return _f32(a)
+    if dtype == DTYPE_F16:
+        return round_f16(a)
+    if dtype == DTYPE_BF16:
+        return round_bf16(a)
+    raise ValueError(f"unknown dtype {dtype}")
+
+
+def bitlinear_forward_typed(x, g, packed, w_scale: float, N: int, eps: float = 1e-6, y_dtype: int = DTYPE_F32,
+                            rows=None) -> np.ndarray:
+    """The projection with 16-bit tensors: x and g hold the widened 16-bit
+    values (exact fp32 values), y is the fp32 projection rounded once to y_dtype
+    (returned widened to float32)."""
+    return round_to(bitlinear_forward(x, g, packed, w_scale, N, eps, rows=rows), y_dtype)

@@ -117,3 +117,18 @@ def test_glu_argument_errors(L):
     q.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                   ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     assert q(FAKE, FAKE, 1, FAKE, 4, 4096, 1e-6, FAKE, FAKE, None, None, None) == bn.ERR_UNSUPPORTED_SHAPE
+
+
+def test_typed_forward_argument_errors(L):
+    f = L.bitnet_bitlinear_forward_typed
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p]
+    assert bn.DTYPE_F32 == 0 and bn.DTYPE_F16 == 1 and bn.DTYPE_BF16 == 2  # the header's values
+    assert f(None, 2, FAKE, 0, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, 2, None) == bn.ERR_INVALID_ARG  # no x
+    assert f(FAKE, 3, FAKE, 0, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, 2, None) == bn.ERR_INVALID_ARG  # unknown x type
+    assert f(FAKE, 2, FAKE, 2, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, 2, None) == bn.ERR_INVALID_ARG  # bf16 norm weight
+    assert f(FAKE, 2, FAKE, 1, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, -1, None) == bn.ERR_INVALID_ARG  # unknown y type
+    assert f(FAKE, 2, FAKE, 1, FAKE, 1.0, 1, 128, 1, 0.0, FAKE, 1, None) == bn.ERR_INVALID_ARG    # eps = 0
+    assert f(FAKE, 2, FAKE, 1, FAKE, 1.0, 1, 100, 1, 1e-6, FAKE, 1, None) == bn.ERR_UNSUPPORTED_SHAPE
+    assert f(ODD, 2, FAKE, 1, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, 1, None) == bn.ERR_MISALIGNED

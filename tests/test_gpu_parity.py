@@ -327,6 +327,56 @@ def test_forward_matches_oracle(oracle_mod, M, K, N):
     assert_rows_close(host(y), ref, f"forward M={M} K={K} N={N}")
 
 
+# 16-bit x / y and fp16 norm weights: every path (decode launches on fp32
+# copies, the split-K kernel with an fp32 y copy, the tokens-as-M kernel
+# reading 16-bit x in its norm launch and writing 16-bit y by TMA stores, by
+# direct stores when the row pitch is not a multiple of 16 bytes, and by the
+# split-K read-back)
+TYPED_CASES = [(1, 1024, 2048), (4, 16384, 600), (16, 16384, 1024), (300, 1024, 640), (200, 3072, 130),
+               (128, 16384, 1024), (2048, 640, 2048)]
+TYPED_DTYPES = [("bf16", "f32", "bf16"), ("f16", "f16", "f16"), ("f32", "f16", "bf16"), ("bf16", "f16", "f32")]
+_TT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+_OT = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+@pytest.mark.parametrize("M,K,N", TYPED_CASES)
+@pytest.mark.parametrize("xt,gt,yt", TYPED_DTYPES)
+def test_forward_typed_matches_oracle(oracle_mod, M, K, N, xt, gt, yt):
+    # inputs rounded to their 16-bit types on the host (torch CPU casts); the
+    # oracle gets the same values widened, which is exact
+    x = torch.from_numpy(_x_with_edges(M, K, seed=M + 3 * K + N)).to(_TT[xt])
+    g = torch.from_numpy(wl.gen_norm_w(K, seed=N + 1)).to(_TT[gt])
+    packed, ws = bn.pack_i2s(dev(wl.gen_latent_w(N, K, seed=M * N + K + 5)))
+    y = bn.bitlinear_forward_typed(x.cuda(), g.cuda(), packed, ws, N, wl.EPS, y_dtype=_TT[yt])
+    assert y.dtype == _TT[yt] and y.shape == (M, N)
+    ref = oracle_mod.bitlinear_forward_typed(x.float().numpy(), g.float().numpy(), host(packed), ws, N, wl.EPS,
+                                             y_dtype=_OT[yt])
+    assert_rows_close(host(y.float()), ref, f"typed forward {xt}/{gt}/{yt} M={M} K={K} N={N}")
+
+
+def test_forward_typed_all_fp32_is_forward():
+    M, K, N = 40, 1024, 300
+    x = dev(wl.gen_x(M, K, seed=1))
+    g = dev(wl.gen_norm_w(K, seed=2))
+    packed, ws = bn.pack_i2s(dev(wl.gen_latent_w(N, K, seed=3)))
+    assert torch.equal(bn.bitlinear_forward_typed(x, g, packed, ws, N), bn.bitlinear_forward(x, g, packed, ws, N))
+    # 16-bit y is the fp32 projection of the same (widened) inputs, rounded once
+    yb = bn.bitlinear_forward_typed(x, g, packed, ws, N, y_dtype=torch.bfloat16)
+    assert torch.equal(yb, bn.bitlinear_forward(x, g, packed, ws, N).to(torch.bfloat16))
+
+
+def test_forward_typed_argument_errors():
+    x = torch.zeros((2, 128), dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(128, dtype=torch.bfloat16, device="cuda")  # bf16 norm weights: not a supported type
+    packed, ws = bn.pack_i2s(torch.ones((4, 128), device="cuda"))
+    with pytest.raises(TypeError):
+        bn.bitlinear_forward_typed(x, g, packed, ws, 4)
+    y = torch.empty((2, 4), dtype=torch.float16, device="cuda")
+    rc = bn.lib().bitnet_bitlinear_forward_typed(x.data_ptr(), 2, g.data_ptr(), 7, packed.data_ptr(), ws, 2, 128, 4,
+                                                 1e-6, y.data_ptr(), 1, None)
+    assert rc == bn.ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("K", [1024, 3072, 16384])
 def test_forward_is_composition_of_the_two_calls(K):
     """The row reduction is implemented three ways (registers, global re-read,

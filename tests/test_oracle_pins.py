@@ -363,3 +363,98 @@ def test_glu_forward_is_forward_of_glu(oracle_mod):
     packed, ws = oracle_mod.pack_i2s(wl.gen_latent_w(N, K, seed=5))
     y = oracle_mod.bitlinear_forward_glu(gate, up, 1, g, packed, ws, N)
     assert np.array_equal(y, oracle_mod.bitlinear_forward(oracle_mod.glu(gate, up, 1), g, packed, ws, N))
+
+
+# --------------------------------------------------------- 16-bit tensors
+# Rounding fp32 to bfloat16 / fp16 (IEEE 754, nearest, ties to even) is pinned
+# against a brute-force search: of the two representable neighbours of each
+# input (its value truncated toward zero in the format, and the next value up
+# in magnitude, infinity past the largest finite one), the nearer one, the one
+# with an even last significand bit on a tie; distances in fp64 are exact.
+
+def _bf16_neighbours(x):
+    u = np.asarray(x, np.float32).view(np.uint32)
+    lo = (u & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+    # the next bfloat16 up in magnitude; past the largest finite, 2^128 stands
+    # in for the rounding (it is where infinity takes over)
+    step = np.ldexp(1.0, (np.frexp(np.abs(lo))[1] - 8).astype(np.int32))
+    hi = lo + np.sign(x.astype(np.float64)) * step
+    lo_even = ((u >> 16) & 1) == 0
+    return lo, hi, lo_even
+
+
+def test_bf16_rounding_worked_values(oracle_mod):
+    cases = [
+        (1.0, 1.0),
+        (1.0 + 2.0**-8, 1.0),                      # halfway, 1.0 is even: stays
+        (1.0 + 3 * 2.0**-8, 1.0 + 2.0**-6),        # halfway, 1 + 2^-7 is odd: up
+        (1.0 + 2.0**-8 + 2.0**-20, 1.0 + 2.0**-7),  # just past halfway: up
+        (-(1.0 + 2.0**-8 + 2.0**-20), -(1.0 + 2.0**-7)),
+        (1.0 + 2.0**-8 - 2.0**-20, 1.0),           # just below halfway: down
+        (3.0e38, 226 * 2.0**120),                   # 225.7 units of 2^120 at this exponent
+        (65504.0, 65536.0),
+    ]
+    x = np.array([c[0] for c in cases], np.float32)
+    want = np.array([c[1] for c in cases], np.float32)
+    assert np.array_equal(oracle_mod.round_bf16(x), want)
+    big = np.array([np.finfo(np.float32).max], np.float32)
+    assert np.isinf(oracle_mod.round_bf16(big)[0])  # past the largest bfloat16 by more than half a unit
+
+
+def test_bf16_rounding_is_nearest_even(oracle_mod):
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 0x7F7FFFFF, size=200000, dtype=np.uint32)
+    bits[:1000] = (bits[:1000] & 0xFFFF0000) | 0x8000  # exact ties
+    x = bits.view(np.float32) * np.where(rng.random(bits.size) < 0.5, -1, 1).astype(np.float32)
+    x = x[np.abs(x) >= np.finfo(np.float32).tiny]  # normal numbers
+    lo, hi, lo_even = _bf16_neighbours(x)
+    xd = x.astype(np.float64)
+    dlo, dhi = np.abs(xd - lo), np.abs(hi - xd)
+    want = np.where((dlo < dhi) | ((dlo == dhi) & lo_even), lo, hi)
+    want = np.where(np.abs(want) >= 2.0**128, np.sign(want) * np.inf, want)
+    got = oracle_mod.round_bf16(x).astype(np.float64)
+    assert np.array_equal(got, want)
+
+
+def test_f16_rounding_is_nearest_even(oracle_mod):
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.normal(0, 300, 50000), rng.uniform(-70000, 70000, 50000),
+                        rng.normal(0, 1e-5, 20000)]).astype(np.float32)
+    all16 = np.arange(0, 0x7C01, dtype=np.uint16).view(np.float16).astype(np.float64)  # 0 .. +inf, ascending
+    mag = np.abs(x.astype(np.float64))
+    i = np.clip(np.searchsorted(all16, mag, side="right") - 1, 0, all16.size - 2)
+    lo, hi = all16[i], all16[i + 1]
+    hi_f = np.where(np.isinf(hi), 65536.0, hi)  # where infinity takes over
+    lo_even = (i % 2) == 0
+    pick = np.where((mag - lo < hi_f - mag) | ((mag - lo == hi_f - mag) & lo_even), lo, hi)
+    want = np.sign(x) * pick
+    got = oracle_mod.round_f16(x).astype(np.float64)
+    assert np.array_equal(got, want)
+    # worked values: 65504 is the largest finite; the halfway point to 65536 rounds to infinity (even)
+    v = oracle_mod.round_f16(np.array([65504.0, 65519.0, 65520.0, 1 + 2.0**-11, 1 + 3 * 2.0**-11], np.float32))
+    assert v[0] == 65504.0 and v[1] == 65504.0 and np.isinf(v[2]) and v[3] == 1.0 and v[4] == 1 + 2.0**-9
+
+
+def test_rounding_is_idempotent_and_widening_exact(oracle_mod):
+    x = np.random.default_rng(13).normal(0, 10, 10000).astype(np.float32)
+    for rnd in (oracle_mod.round_bf16, oracle_mod.round_f16):
+        r = rnd(x)
+        assert np.array_equal(rnd(r), r)
+    # the oracle's rounding agrees with torch's casts (a second implementation)
+    import torch
+    t = torch.from_numpy(x)
+    assert np.array_equal(oracle_mod.round_bf16(x), t.to(torch.bfloat16).float().numpy())
+    assert np.array_equal(oracle_mod.round_f16(x), t.to(torch.float16).float().numpy())
+
+
+def test_typed_forward_rounds_the_fp32_projection(oracle_mod):
+    rng = np.random.default_rng(14)
+    M, K, N = 3, 256, 50
+    x = oracle_mod.round_bf16(rng.normal(0, 1, (M, K)).astype(np.float32))
+    g = oracle_mod.round_f16(wl.gen_norm_w(K, seed=2))
+    packed, ws = oracle_mod.pack_i2s(wl.gen_latent_w(N, K, seed=3))
+    y32 = oracle_mod.bitlinear_forward(x, g, packed, ws, N)
+    assert np.array_equal(oracle_mod.bitlinear_forward_typed(x, g, packed, ws, N, y_dtype=oracle_mod.DTYPE_F32), y32)
+    yb = oracle_mod.bitlinear_forward_typed(x, g, packed, ws, N, y_dtype=oracle_mod.DTYPE_BF16)
+    assert np.array_equal(yb, oracle_mod.round_bf16(y32))
+    assert np.all(np.abs(yb - y32) <= np.abs(y32) * 2.0**-8)  # half a unit of 8 significand bits
