@@ -15,7 +15,8 @@ projection, --m/--k/--n), gemma3_prefill
 (seven Gemma3-shaped projections at M=32768 with 1% x20 outlier features),
 qwen3_prefill_stack (28 layers x 7 projections at M=32768), sweep (K, N in
 {1024,4096,8192,16384} x M in {1,16,128,2048,16384}), glu_proj (the down
-projection BitLinear(act(gate) * up), --m/--k/--n/--act).  --io f16|bf16 runs the
+projection BitLinear(act(gate) * up), --m/--k/--n/--act), qk_proj (a q/k projection
+with its QK head norm, --m/--k/--n/--head-dim).  --io f16|bf16 runs the
 prefill workloads with 16-bit x and y (bitnet_bitlinear_forward_typed).
 
 --impl reference times the CPU oracle (test infrastructure, plain C) on the
@@ -659,6 +660,65 @@ def run_glu_proj(args, rank, world, local):
             "parity": {"oracle_worst_row_rel_l2": worst}}
 
 
+def run_qk_proj(args, rank, world, local):
+    """The q/k projection with its QK head norm (--m/--k/--n/--head-dim; default
+    the Qwen3 q projection at 32768 tokens, heads of 128): the projection alone
+    and chained with the head norm (several weight sets, inputs larger than L2),
+    and the head norm alone on y in place, replayed from a CUDA graph."""
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    import oracle
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    M, K, N, hd = args.m, args.k, args.n, args.head_dim
+    stream = torch.cuda.Stream(device)
+    x = wl.gen_device((M, K), wl.seed_for(6, M, K, N), device)
+    g = torch.from_numpy(wl.gen_norm_w(K, seed=K)).to(device)
+    hw = torch.from_numpy(wl.gen_norm_w(hd, seed=hd)).to(device)
+    sets = []
+    for i in range(4):
+        w = wl.gen_device((N, K), wl.seed_for(6, K, N, i), device, std=0.02)
+        sets.append(bn.pack_i2s(w))
+        del w
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+
+    def fwd():
+        for packed, ws in sets:
+            bn.bitlinear_forward(x, g, packed, ws, N, wl.EPS, y, stream=stream)
+
+    def fwd_qk():
+        for packed, ws in sets:
+            bn.bitlinear_forward_qk(x, g, packed, ws, N, hd, hw, wl.EPS, y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        ms_f = time_region(torch, stream, fwd, 5, 2) / len(sets)
+        ms_qk = time_region(torch, stream, fwd_qk, 5, 2) / len(sets)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(8):
+                bn.head_rmsnorm(y, hd, hw, wl.EPS, out=y, stream=stream)
+        ms_h = time_region(torch, stream, graph.replay, 5, 2) / 8
+    hbm, _, _, _ = peaks()
+    hb = M * N * 8 + hd * 4
+    rows = np.random.default_rng(0).choice(M, min(M, 16), replace=False)
+    fwd_qk()
+    packed, ws = sets[-1]
+    ref = oracle.bitlinear_forward_qk(x[rows].cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws, N, hd,
+                                      hw.cpu().numpy())
+    yy = y[rows].cpu().numpy()
+    worst = float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max())
+    return {"metric": METRIC, "value": round(2.0 * M * N * K / (ms_qk * 1e-3) / 1e12, 2), "unit": "TOPS",
+            "n_gpus": world, "ms_per_step": ms_qk, "us_projection": ms_f * 1e3, "us_projection_qk": ms_qk * 1e3,
+            "us_head_norm_alone": ms_h * 1e3, "head_norm_GBps": hb / (ms_h * 1e-3) / 1e9,
+            "head_norm_hbm_frac": hb / (ms_h * 1e-3) / 1e9 / hbm,
+            "config": {"workload": f"qk_proj_M{M}_K{K}_N{N}_hd{hd}", "weights_cycled": len(sets),
+                       "launch": "eager projections; head norm alone: CUDA graph"},
+            "parity": {"oracle_worst_row_rel_l2": worst}}
+
+
 def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, outlier_frac, stream,
                             io_dtype=None):
     """Buffers for one layer's projections at M tokens (x drawn on the device;
@@ -828,11 +888,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_decode_layer",
                     choices=["qwen3_decode_layer", "q_proj_m8", "gemma3_prefill", "qwen3_prefill_stack", "sweep",
-                             "proj", "glu_proj"])
+                             "proj", "glu_proj", "qk_proj"])
     ap.add_argument("--m", type=int, default=16, help="--workload proj: tokens")
     ap.add_argument("--k", type=int, default=16384, help="--workload proj: input features")
     ap.add_argument("--n", type=int, default=16384, help="--workload proj: output features")
     ap.add_argument("--act", type=int, default=1, help="--workload glu_proj: 1 SiLU, 2 tanh GELU")
+    ap.add_argument("--head-dim", type=int, default=128, help="--workload qk_proj: values per head")
     ap.add_argument("--io", choices=["f32", "f16", "bf16"], default="f32",
                     help="prefill workloads: element type of x and y (bitnet_bitlinear_forward_typed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -854,6 +915,8 @@ def main():
         out = run_proj(args, rank, world, local)
     elif args.workload == "glu_proj":
         out = run_glu_proj(args, rank, world, local)
+    elif args.workload == "qk_proj":
+        out = run_qk_proj(args, rank, world, local)
     else:
         out = run_prefill(args, rank, world, local, args.workload)
     if rank == 0 and out is not None:

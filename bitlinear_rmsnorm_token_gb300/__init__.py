@@ -19,7 +19,7 @@ __all__ = [
     "bitlinear_forward", "bitlinear_forward_group", "last_device_status", "status_string",
     "FLAG_WEIGHTS_STATIC", "MAX_GROUP", "EXPORTED_FUNCTIONS", "bitlinear_forward_noalloc",
     "selftest_bounded_wait", "glu", "glu_rmsnorm_quant_a8", "bitlinear_forward_glu", "ACT_SILU", "ACT_GELU_TANH",
-    "bitlinear_forward_typed", "DTYPE_F32", "DTYPE_F16", "DTYPE_BF16",
+    "bitlinear_forward_typed", "DTYPE_F32", "DTYPE_F16", "DTYPE_BF16", "head_rmsnorm", "bitlinear_forward_qk",
 ]
 
 OK = 0
@@ -44,7 +44,7 @@ EXPORTED_FUNCTIONS = (
     "bitnet_i2s_gemm", "bitnet_bitlinear_forward", "bitnet_bitlinear_forward_group",
     "bitnet_status_string", "bitnet_last_device_status", "bitnet_bitlinear_forward_noalloc",
     "bitnet_selftest_bounded_wait", "bitnet_glu", "bitnet_glu_rmsnorm_quant_a8", "bitnet_bitlinear_forward_glu",
-    "bitnet_bitlinear_forward_typed",
+    "bitnet_bitlinear_forward_typed", "bitnet_head_rmsnorm", "bitnet_bitlinear_forward_qk",
 )
 
 
@@ -103,6 +103,10 @@ def lib(build: bool = False) -> ctypes.CDLL:
     L.bitnet_glu_rmsnorm_quant_a8.argtypes = [vp, vp, ctypes.c_int, vp, i64, i64, f32, vp, vp, vp, vp, vp]
     L.bitnet_bitlinear_forward_glu.restype = ctypes.c_int
     L.bitnet_bitlinear_forward_glu.argtypes = [vp, vp, ctypes.c_int, vp, vp, f32, i64, i64, i64, f32, vp, vp]
+    L.bitnet_head_rmsnorm.restype = ctypes.c_int
+    L.bitnet_head_rmsnorm.argtypes = [vp, i64, i64, i64, vp, f32, vp, vp]
+    L.bitnet_bitlinear_forward_qk.restype = ctypes.c_int
+    L.bitnet_bitlinear_forward_qk.argtypes = [vp, vp, vp, f32, i64, i64, i64, f32, i64, vp, vp, vp]
     L.bitnet_bitlinear_forward_typed.restype = ctypes.c_int
     L.bitnet_bitlinear_forward_typed.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, vp, f32, i64, i64, i64, f32, vp,
                                                  ctypes.c_int, vp]
@@ -251,6 +255,37 @@ def bitlinear_forward_typed(x, norm_w, packed_w, w_scale: float, N: int, eps: fl
         _dev(x, x.dtype, "x"), xt, _dev(norm_w, norm_w.dtype, "norm_w"), gt, _dev(packed_w, torch.uint8, "packed_w"),
         float(w_scale), M, K, N, float(eps), _dev(y, y.dtype, "y"), yt, _stream(stream))
     _check(rc, "bitnet_bitlinear_forward_typed")
+    return y
+
+
+def head_rmsnorm(y, head_dim: int, head_w, eps: float = 1e-6, out=None, stream=None):
+    """Per-head RMSNorm of y[M, N] (heads of head_dim consecutive values) times
+    head_w[head_dim]; out=y works in place."""
+    import torch
+
+    M, N = y.shape
+    if out is None:
+        out = torch.empty_like(y)
+    rc = lib().bitnet_head_rmsnorm(_dev(y, torch.float32, "y"), M, N, int(head_dim),
+                                   _dev(head_w, torch.float32, "head_w"), float(eps), _dev(out, torch.float32, "out"),
+                                   _stream(stream))
+    _check(rc, "bitnet_head_rmsnorm")
+    return out
+
+
+def bitlinear_forward_qk(x, norm_w, packed_w, w_scale: float, N: int, head_dim: int, head_w, eps: float = 1e-6,
+                         y=None, stream=None):
+    """The q/k projection followed by its head norm."""
+    import torch
+
+    M, K = x.shape
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    rc = lib().bitnet_bitlinear_forward_qk(
+        _dev(x, torch.float32, "x"), _dev(norm_w, torch.float32, "norm_w"), _dev(packed_w, torch.uint8, "packed_w"),
+        float(w_scale), M, K, N, float(eps), int(head_dim), _dev(head_w, torch.float32, "head_w"),
+        _dev(y, torch.float32, "y"), _stream(stream))
+    _check(rc, "bitnet_bitlinear_forward_qk")
     return y
 
 

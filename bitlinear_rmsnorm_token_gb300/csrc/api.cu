@@ -262,8 +262,12 @@ size_t glu_buffer_bytes(int act, int64_t M, int64_t K) {
 
 // bitnet_bitlinear_forward (act == 0) and bitnet_bitlinear_forward_glu: x is the
 // input, or the gate projection's output when act != 0 (the row is act(x) * up).
+// head_w / head_dim / head_fused: the QK head norm, applied in the tensor-core
+// epilogue when that route is taken and its plan allows (*head_fused then true).
 int forward_impl(const float* x, const float* up, int act, const float* norm_w, const uint8_t* packed_w,
-                 float w_scale, int64_t M, int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream) {
+                 float w_scale, int64_t M, int64_t K, int64_t N, float eps, float* y, bitnet_stream_t stream,
+                 const float* head_w = nullptr, int head_dim = 0, bool* head_fused = nullptr) {
+  if (head_fused) *head_fused = false;
   if (!x || !norm_w || !packed_w || !y || (act != 0 && !up)) return BITNET_ERR_INVALID_ARG;
   if (act != 0 && act != BITNET_ACT_SILU && act != BITNET_ACT_GELU_TANH) return BITNET_ERR_INVALID_ARG;
   if (!(eps > 0.0f) || !(w_scale > 0.0f) || w_scale == INFINITY) return BITNET_ERR_INVALID_ARG;
@@ -343,7 +347,7 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
   if (e == cudaSuccess)
     e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
                : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, nullptr, gws_bytes ? gws : nullptr, true,
-                                true, s, &st);
+                                true, s, &st, head_w, head_dim, eps, head_fused);
   pool_free(ws, s);
   if (st != BITNET_OK) return st;
   return cuda_status(e);
@@ -429,6 +433,36 @@ int forward_typed(const void* x, int x_dtype, const void* norm_w, int g_dtype, c
 }  // namespace
 
 extern "C" {
+
+int bitnet_head_rmsnorm(const float* y, int64_t M, int64_t N, int64_t head_dim, const float* head_w, float eps,
+                        float* out, bitnet_stream_t stream) {
+  if (!y || !head_w || !out || M < 1 || N < 1 || !(eps > 0.0f)) return BITNET_ERR_INVALID_ARG;
+  if (head_dim < 128 || head_dim % 128 != 0 || head_dim > BITNET_MAX_K || N % head_dim != 0)
+    return BITNET_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(y) || !aligned16(head_w) || !aligned16(out)) return BITNET_ERR_MISALIGNED;
+  DeviceContext* ctx;
+  int rc = device_context(&ctx);
+  if (rc) return rc;
+  return cuda_status(launch_head_rmsnorm(y, M * (N / head_dim), static_cast<int>(head_dim), head_w, eps, out, false,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bitnet_bitlinear_forward_qk(const float* x, const float* norm_w, const uint8_t* packed_w, float w_scale, int64_t M,
+                                int64_t K, int64_t N, float eps, int64_t head_dim, const float* head_w, float* y,
+                                bitnet_stream_t stream) {
+  if (!head_w) return BITNET_ERR_INVALID_ARG;
+  if (head_dim < 128 || head_dim % 128 != 0 || head_dim > BITNET_MAX_K || N < 1 || N % head_dim != 0)
+    return BITNET_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(head_w)) return BITNET_ERR_MISALIGNED;
+  bool fused = false;
+  int rc = forward_impl(x, nullptr, 0, norm_w, packed_w, w_scale, M, K, N, eps, y, stream, head_w,
+                        static_cast<int>(head_dim), &fused);
+  if (rc || fused) return rc;
+  // otherwise one more launch, chained to the projection's last: the head norm
+  // waits for it on the device
+  return cuda_status(launch_head_rmsnorm(y, M * (N / head_dim), static_cast<int>(head_dim), head_w, eps, y, true,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
 
 int bitnet_bitlinear_forward_typed(const void* x, int x_dtype, const void* norm_w, int norm_w_dtype,
                                    const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float eps,

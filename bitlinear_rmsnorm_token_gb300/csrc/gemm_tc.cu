@@ -35,6 +35,10 @@
 //              the accumulator test output, threads store directly.
 //              y is fp32, or fp16 / bf16 (YT: the fp32 result rounded once;
 //              a 16-bit block holds 32 columns in the same 64-byte rows).
+//              With a QK head norm (hd > 0, hd dividing BW, no K split) each
+//              thread normalises its token's heads of hd columns itself: three
+//              passes over the head in TMEM (largest |y|, the fixed-point sum
+//              of squares, the output), the row arithmetic of the input norm.
 // Split K: when the output tiles are too few to give every SM work (a few
 // hundred tokens, long rows), the K blocks of each tile are split into S
 // ranges and the CTAs iterate over (tile, range) units.  A unit's epilogue adds
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_y, int y_by_tma, const float* __restrict__ a_scale,
               float inv_w, int M, int N, int K, int S, YT* __restrict__ y, int32_t* __restrict__ acc_out,
-              float* __restrict__ ws, int* __restrict__ tickets, unsigned* err) {
+              float* __restrict__ ws, int* __restrict__ tickets, const float* __restrict__ head_w, int hd,
+              float eps, unsigned* err) {
   using L = TcLayout<BW>;
   constexpr int kTpr = kUnpackWarps * 32 / BW;  // unpack threads per weight row (1, 2 or 4)
   constexpr int kCpt = 8 / kTpr;                 // 16-byte chunks of a slab row per thread
@@ -374,7 +379,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*abort_flag) break;
         continue;
       }
-      if (y_by_tma && rows_ok) {
+      if (BW >= 128 && hd > 0) {  // (heads of 128 or 256 values never fit 64-wide tiles)
+        if (rows_ok) {
+          // 32 values of this thread's token, columns c .. c + 31 of the tile
+          auto load32 = [&](int c, uint32_t(&r)[32]) {
+            tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+            tmem_ld_wait();
+            tmem_reg_fence(r);
+          };
+          auto y4 = [&](const uint32_t(&r)[32], int v) {
+            return make_float4(rescale_elem(__uint_as_float(r[4 * v + 0]), inv_a, inv_w),
+                               rescale_elem(__uint_as_float(r[4 * v + 1]), inv_a, inv_w),
+                               rescale_elem(__uint_as_float(r[4 * v + 2]), inv_a, inv_w),
+                               rescale_elem(__uint_as_float(r[4 * v + 3]), inv_a, inv_w));
+          };
+          int blk = 0;  // staging blocks written so far (they alternate between two buffers)
+          const int ncols = min(BW, N - n0);  // whole heads: hd divides N and BW
+          for (int h0 = 0; h0 < ncols; h0 += hd) {
+            uint32_t r[32];
+            int key = 0;
+            for (int c = h0; c < h0 + hd; c += 32) {
+              load32(c, r);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) key = max(key, sq_key4(y4(r, v)));
+            }
+            const float scale = sq_scale(key);
+            SqPartial part = {0ull, 0u};
+            for (int c = h0; c < h0 + hd; c += 32) {
+              load32(c, r);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) sq_add4(part, y4(r, v), scale);
+            }
+            const float rstd = rstd_from_fixed(sq_fold(part, hd), key, hd, eps);
+            for (int c = h0; c < h0 + hd; c += 32) {
+              load32(c, r);
+              const float* hw = head_w + (c - h0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const float4 yv = y4(r, v);
+                const float4 g = __ldg(reinterpret_cast<const float4*>(hw + 4 * v));
+                r[4 * v + 0] = __float_as_uint(norm_elem(yv.x, rstd, g.x));
+                r[4 * v + 1] = __float_as_uint(norm_elem(yv.y, rstd, g.y));
+                r[4 * v + 2] = __float_as_uint(norm_elem(yv.z, rstd, g.z));
+                r[4 * v + 3] = __float_as_uint(norm_elem(yv.w, rstd, g.w));
+              }
+              const int col = n0 + c;
+              if (y_by_tma) {
+                constexpr int kPer = sizeof(YT) == 2 ? 32 : 16;  // columns per 64-byte staging row
+#pragma unroll
+                for (int b = 0; b < 32 / kPer; ++b) {
+                  if (lane == 0) bulk_wait_group_read<1>();
+                  __syncwarp();
+                  uint8_t* const buf = stg + (blk & 1) * 2048;
+#pragma unroll
+                  for (int v = 0; v < 4; ++v) {
+                    uint4 o;
+                    if constexpr (sizeof(YT) == 2) {
+                      o.x = pack2_out<YT>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                      o.y = pack2_out<YT>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                      o.z = pack2_out<YT>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                      o.w = pack2_out<YT>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                    } else {
+                      o = make_uint4(r[16 * b + 4 * v + 0], r[16 * b + 4 * v + 1], r[16 * b + 4 * v + 2],
+                                     r[16 * b + 4 * v + 3]);
+                    }
+                    *reinterpret_cast<uint4*>(buf + lane * 64 + ((v ^ swz) << 4)) = o;
+                  }
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  if (lane == 0) {
+                    tma_store_2d(&tm_y, buf, col + kPer * b, m0 + q * 32);
+                    bulk_commit_group();
+                  }
+                  ++blk;
+                }
+              } else if (m_ok) {
+                YT* yrow = y + static_cast<int64_t>(m) * N + col;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) yrow[j] = round_out<YT>(__uint_as_float(r[j]));
+              }
+            }
+          }
+        }
+      } else if (y_by_tma && rows_ok) {
         const int nch = (min(BW, N - n0) + 31) >> 5;  // 32-column chunks holding outputs
         // rescale the chunk in r (columns n0 + 32 ch ..) and store it as two
         // fp32 blocks, or as one block of 16-bit values
@@ -490,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BW, typename YT>
 cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __half* codes_f16, const float* a_scale,
                       const uint8_t* packed_w, float inv_w, int M, int N, int K, int S, YT* y, int32_t* acc_out,
-                      float* ws, int* tickets, bool pdl, cudaStream_t s, int* status) {
+                      float* ws, int* tickets, const float* head_w, int hd, float eps, bool pdl, cudaStream_t s,
+                      int* status) {
   using L = TcLayout<BW>;
   CUtensorMap tm_tok, tm_w;
   {
@@ -556,7 +644,7 @@ cudaError_t launch_bw(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, tm_y, y_by_tma, a_scale, inv_w, M, N, K, S, y, acc_out, ws,
-                            tickets, ctx->err_word);
+                            tickets, head_w, hd, eps, ctx->err_word);
 }
 
 // Weight-tile width and number of K ranges.  Wide tiles re-read the tokens
@@ -603,8 +691,10 @@ size_t gemm_tc_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
                            const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, void* y,
                            int y_dtype, int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl,
-                           cudaStream_t s, int* status) {
+                           cudaStream_t s, int* status, const float* head_w, int head_dim, float eps,
+                           bool* head_fused) {
   *status = BITNET_OK;
+  if (head_fused) *head_fused = false;
   EncodeTiledFn encode = encode_tiled_fn();
   if (!encode) {
     *status = BITNET_ERR_CUDA;
@@ -626,18 +716,23 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
       if (e != cudaSuccess) return e;
     }
   }
+  // the head norm rides in the epilogue when a tile holds whole heads and K is not split
+  const bool fuse = head_w && head_dim > 0 && head_fused && pl.S == 1 && pl.bw % head_dim == 0 && acc_out == nullptr;
+  if (fuse) *head_fused = true;
+  const float* hw = fuse ? head_w : nullptr;
+  const int hd = fuse ? head_dim : 0;
   auto go = [&](auto* yt) {
     using YT = std::remove_pointer_t<decltype(yt)>;
     switch (pl.bw) {
       case 64:
         return launch_bw<64, YT>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, yt, acc_out, ws,
-                                 tickets, pdl, s, status);
+                                 tickets, hw, hd, eps, pdl, s, status);
       case 128:
         return launch_bw<128, YT>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, yt, acc_out, ws,
-                                  tickets, pdl, s, status);
+                                  tickets, hw, hd, eps, pdl, s, status);
       default:
         return launch_bw<256, YT>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, n, k, pl.S, yt, acc_out, ws,
-                                  tickets, pdl, s, status);
+                                  tickets, hw, hd, eps, pdl, s, status);
     }
   };
   switch (y_dtype) {

@@ -56,6 +56,10 @@ cudaError_t launch_rmsnorm_quant(const float* x, const float* g, int64_t M, int 
 // or _BF16), widened to fp32 as it is loaded.
 cudaError_t launch_rmsnorm_quant_f16_in(const void* x, int x_dtype, const float* g, int64_t M, int K, float eps,
                                         __half* codes_f16, float* a_scale, bool pdl, cudaStream_t s);
+// Head norm of projection outputs: rows of hd values (a multiple of 128),
+// out = (y * rstd(row)) * w, the input norm's row arithmetic; out may be y.
+cudaError_t launch_head_rmsnorm(const float* y, int64_t rows, int hd, const float* w, float eps, float* out, bool pdl,
+                                cudaStream_t s);
 // Element-wise conversion of `count` values between BITNET_DTYPE_* types:
 // widening is exact, narrowing rounds to nearest, ties to even.
 cudaError_t launch_convert(const void* in, int in_dtype, void* out, int out_dtype, int64_t count, cudaStream_t s);
@@ -112,10 +116,13 @@ cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs, int n
 // stream unless workspace_zeroed); with a null workspace it does not split.
 size_t gemm_tc_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
 // y is y_dtype (BITNET_DTYPE_F32, _F16 or _BF16): the fp32 result rounded once.
+// With head_w / head_dim / head_fused given, the QK head norm is applied in the
+// epilogue when the plan allows it (*head_fused says whether it was).
 cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
                            const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, void* y,
                            int y_dtype, int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl,
-                           cudaStream_t s, int* status);
+                           cudaStream_t s, int* status, const float* head_w = nullptr, int head_dim = 0,
+                           float eps = 0.0f, bool* head_fused = nullptr);
 
 // Tensor-core contraction for 9..63 tokens (weights as the MMA's M side, K
 // split across CTAs).  Needs gemm_skinny_workspace() bytes of device memory

@@ -322,7 +322,44 @@ __global__ void __launch_bounds__(256) k_glu(const float* __restrict__ gate, con
                                          __ldg(reinterpret_cast<const float4*>(up) + t), act);
 }
 
+// Head norm of projection outputs: one warp per (token, head) row of hd
+// values (a multiple of 128), out = (y * rstd) * w with the row arithmetic of
+// the input norm.  out may be y (each element is read by the thread that
+// writes it, after the row's reductions), hence no __restrict__.
+__global__ void __launch_bounds__(kNqWarps * 32) k_head_rmsnorm(const float* y, int64_t rows, int hd,
+                                                                const float* __restrict__ w, float eps, float* out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kNqWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float* yr = y + row * hd;
+  const float rstd = warp_row_rstd<true>(yr, hd, lane, eps);
+  for (int c = 0; c < (hd >> 7); ++c) {
+    const float4 v = load4(yr + 128 * c + 4 * lane);
+    const float4 g = __ldg(reinterpret_cast<const float4*>(w + 128 * c + 4 * lane));
+    *reinterpret_cast<float4*>(out + row * hd + 128 * c + 4 * lane) =
+        make_float4(norm_elem(v.x, rstd, g.x), norm_elem(v.y, rstd, g.y), norm_elem(v.z, rstd, g.z),
+                    norm_elem(v.w, rstd, g.w));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_head_rmsnorm(const float* y, int64_t rows, int hd, const float* w, float eps, float* out, bool pdl,
+                                cudaStream_t s) {
+  if (rows < 1) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + kNqWarps - 1) / kNqWarps));
+  cfg.blockDim = dim3(kNqWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_head_rmsnorm, y, rows, hd, w, eps, out);
+}
 
 bool rmsnorm_quant_glu_fused_supported(int K) { return K >= 128 && K % 128 == 0 && (K >> 7) <= 24; }
 

@@ -266,6 +266,33 @@ BITNET_API int bitnet_bitlinear_forward_typed(const void* x, int x_dtype, const 
                                               const uint8_t* packed_w, float w_scale, int64_t M, int64_t K,
                                               int64_t N, float eps, void* y, int y_dtype, bitnet_stream_t stream);
 
+/* QK head norm of a projection's output ("BitNet Embeddings GGUF Conversion
+ * Implementation", section 4.5, "Attention per-projection norms": after the q
+ * and k matmuls, an RMSNorm with the attention eps times attn_q_norm /
+ * attn_k_norm, the "QK head norms" of the model table).  Read per head: y[M, N]
+ * holds N / head_dim heads of head_dim consecutive values per token, and for
+ * every (token, head) row r of head_dim values
+ *   out[r] = (r * rstd) * head_w,  rstd = 1 / sqrt(sum(r^2) / head_dim + eps),
+ * with the same arithmetic as the input norm of bitnet_rmsnorm_quant_a8 (rstd
+ * the float rounding of the exact value, two float multiplies).
+ * head_w[head_dim] fp32; out may be y (in place).  head_dim a multiple of 128
+ * (Qwen3 128, Gemma3 256) dividing N.  Errors: BITNET_ERR_INVALID_ARG (NULL,
+ * M or N < 1, eps <= 0), BITNET_ERR_UNSUPPORTED_SHAPE, BITNET_ERR_MISALIGNED
+ * (16 bytes), BITNET_ERR_CUDA. */
+BITNET_API int bitnet_head_rmsnorm(const float* y, int64_t M, int64_t N, int64_t head_dim, const float* head_w,
+                                   float eps, float* out, bitnet_stream_t stream);
+
+/* The q or k projection followed by its head norm: y = head_rmsnorm(
+ * bitnet_bitlinear_forward(x, ...)), eps used by both norms, bit for bit.  On
+ * the tensor-core route (64 tokens and more) the head norm runs in the
+ * contraction's epilogue when a weight tile holds whole heads and K is not
+ * split; otherwise one more launch, chained to the projection's, normalises y
+ * in place.  Arguments and errors as bitnet_bitlinear_forward and
+ * bitnet_head_rmsnorm. */
+BITNET_API int bitnet_bitlinear_forward_qk(const float* x, const float* norm_w, const uint8_t* packed_w, float w_scale,
+                                           int64_t M, int64_t K, int64_t N, float eps, int64_t head_dim,
+                                           const float* head_w, float* y, bitnet_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 BITNET_API const char* bitnet_status_string(int status);
 

@@ -314,3 +314,25 @@ def bitlinear_forward_typed(x, g, packed, w_scale: float, N: int, eps: float = 1
     values (exact fp32 values), y is the fp32 projection rounded once to y_dtype
     (returned widened to float32)."""
     return round_to(bitlinear_forward(x, g, packed, w_scale, N, eps, rows=rows), y_dtype)
+
+
+
+# ------------------------------------------------------------ QK head norms
+# "BitNet Embeddings GGUF Conversion Implementation", section 4.5 ("Attention
+# per-projection norms"): after the q / k matmul, RMSNorm with the attention
+# eps times attn_q_norm / attn_k_norm, the per-head "QK head norms" of the model
+# table: each head's head_dim consecutive outputs are one RMSNorm row.
+
+def head_rmsnorm(y, head_dim: int, w, eps: float = 1e-6) -> np.ndarray:
+    """RMSNorm of every (token, head) row of y[M, N] with weight w[head_dim]."""
+    y = _f32(y)
+    M, N = y.shape
+    if N % head_dim:
+        raise ValueError("head_rmsnorm: head_dim must divide N")
+    return rmsnorm(y.reshape(M * (N // head_dim), head_dim), w, eps).reshape(M, N)
+
+
+def bitlinear_forward_qk(x, g, packed, w_scale: float, N: int, head_dim: int, head_w, eps: float = 1e-6,
+                         rows=None) -> np.ndarray:
+    """The q / k projection followed by its head norm (eps shared by both norms)."""
+    return head_rmsnorm(bitlinear_forward(x, g, packed, w_scale, N, eps, rows=rows), head_dim, head_w, eps)

@@ -132,3 +132,22 @@ def test_typed_forward_argument_errors(L):
     assert f(FAKE, 2, FAKE, 1, FAKE, 1.0, 1, 128, 1, 0.0, FAKE, 1, None) == bn.ERR_INVALID_ARG    # eps = 0
     assert f(FAKE, 2, FAKE, 1, FAKE, 1.0, 1, 100, 1, 1e-6, FAKE, 1, None) == bn.ERR_UNSUPPORTED_SHAPE
     assert f(ODD, 2, FAKE, 1, FAKE, 1.0, 1, 128, 1, 1e-6, FAKE, 1, None) == bn.ERR_MISALIGNED
+
+
+def test_head_norm_argument_errors(L):
+    h = L.bitnet_head_rmsnorm
+    h.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    assert h(None, 1, 256, 128, FAKE, 1e-6, FAKE, None) == bn.ERR_INVALID_ARG
+    assert h(FAKE, 0, 256, 128, FAKE, 1e-6, FAKE, None) == bn.ERR_INVALID_ARG
+    assert h(FAKE, 1, 256, 128, FAKE, 0.0, FAKE, None) == bn.ERR_INVALID_ARG
+    assert h(FAKE, 1, 256, 64, FAKE, 1e-6, FAKE, None) == bn.ERR_UNSUPPORTED_SHAPE   # head_dim not a multiple of 128
+    assert h(FAKE, 1, 384, 256, FAKE, 1e-6, FAKE, None) == bn.ERR_UNSUPPORTED_SHAPE  # does not divide N
+    assert h(FAKE, 1, 256, 128, ODD, 1e-6, FAKE, None) == bn.ERR_MISALIGNED
+    q = L.bitnet_bitlinear_forward_qk
+    q.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int64, ctypes.c_float, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert q(FAKE, FAKE, FAKE, 1.0, 1, 128, 256, 1e-6, 128, None, FAKE, None) == bn.ERR_INVALID_ARG
+    assert q(FAKE, FAKE, FAKE, 1.0, 1, 128, 200, 1e-6, 128, FAKE, FAKE, None) == bn.ERR_UNSUPPORTED_SHAPE
+    assert q(FAKE, FAKE, FAKE, 1.0, 1, 128, 256, 1e-6, 128, ODD, FAKE, None) == bn.ERR_MISALIGNED
+    assert q(None, FAKE, FAKE, 1.0, 1, 128, 256, 1e-6, 128, FAKE, FAKE, None) == bn.ERR_INVALID_ARG

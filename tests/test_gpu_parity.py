@@ -377,6 +377,48 @@ def test_forward_typed_argument_errors():
     assert rc == bn.ERR_INVALID_ARG
 
 
+# QK head norms: per-head RMSNorm of a projection's output (heads of 128 and
+# 256 values), standalone (in place and out of place) and chained after the
+# projection on every dispatch route
+@pytest.mark.parametrize("M,H,hd", [(1, 16, 128), (3, 4, 256), (257, 8, 128), (4096, 1, 256)])
+def test_head_rmsnorm_matches_oracle(oracle_mod, M, H, hd):
+    y = wl.gen_x(M, H * hd, seed=M + hd, outlier_frac=0.01)
+    if M >= 3:
+        y[1, :hd] = 0.0       # a zero head stays zero
+        y[2, hd:] *= 1e-20    # tiny heads
+        y[0, :] *= 1e20       # huge ones
+    w = wl.gen_norm_w(hd, seed=hd)
+    out = bn.head_rmsnorm(dev(y), hd, dev(w), wl.EPS)
+    ref = oracle_mod.head_rmsnorm(y, hd, w, wl.EPS)
+    got = host(out)
+    # the row arithmetic of the input norm: bit-identical rows except where
+    # rstd sits on a rounding boundary (at most 1 row in 1000)
+    rows_off = np.sum(np.any(got.reshape(-1, hd) != ref.reshape(-1, hd), axis=1))
+    assert rows_off <= max(1, (M * H) // 1000)
+    yd = dev(y)
+    assert torch.equal(bn.head_rmsnorm(yd, hd, dev(w), wl.EPS, out=yd), out)  # in place
+
+
+# decode and split-K routes: a second launch; tokens-as-M tiles holding whole
+# heads (256- and 128-wide tiles, heads of 128 and 256): fused in the epilogue
+QK_CASES = [(1, 1024, 2048, 128), (1, 640, 1024, 256), (5, 3072, 1024, 128), (16, 16384, 1024, 128),
+            (300, 1024, 1024, 128), (2048, 640, 256, 256), (128, 16384, 1024, 128), (2048, 640, 640, 128)]
+
+
+@pytest.mark.parametrize("M,K,N,hd", QK_CASES)
+def test_forward_qk_matches_oracle(oracle_mod, M, K, N, hd):
+    x = _x_with_edges(M, K, seed=M + K + N + hd)
+    g = wl.gen_norm_w(K, seed=N)
+    hw = wl.gen_norm_w(hd, seed=hd + 7)
+    packed, ws = bn.pack_i2s(dev(wl.gen_latent_w(N, K, seed=M * N + K)))
+    y = bn.bitlinear_forward_qk(dev(x), dev(g), packed, ws, N, hd, dev(hw), wl.EPS)
+    # chained launch == projection then standalone head norm, bit for bit
+    y2 = bn.head_rmsnorm(bn.bitlinear_forward(dev(x), dev(g), packed, ws, N, wl.EPS), hd, dev(hw), wl.EPS)
+    assert torch.equal(y, y2)
+    ref = oracle_mod.bitlinear_forward_qk(x, g, host(packed), ws, N, hd, hw, wl.EPS)
+    assert_rows_close(host(y), ref, f"forward_qk M={M} K={K} N={N} hd={hd}")
+
+
 @pytest.mark.parametrize("K", [1024, 3072, 16384])
 def test_forward_is_composition_of_the_two_calls(K):
     """The row reduction is implemented three ways (registers, global re-read,

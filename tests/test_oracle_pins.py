@@ -458,3 +458,50 @@ def test_typed_forward_rounds_the_fp32_projection(oracle_mod):
     yb = oracle_mod.bitlinear_forward_typed(x, g, packed, ws, N, y_dtype=oracle_mod.DTYPE_BF16)
     assert np.array_equal(yb, oracle_mod.round_bf16(y32))
     assert np.all(np.abs(yb - y32) <= np.abs(y32) * 2.0**-8)  # half a unit of 8 significand bits
+
+
+# ------------------------------------------------------------ QK head norms
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_head_rmsnorm_matches_torch_per_head(oracle_mod, hd):
+    M, H = 5, 4
+    y = wl.gen_x(M, H * hd, seed=hd)
+    y[:, hd:2 * hd] *= 37.0   # heads at different scales
+    y[2, 3 * hd:] = 0.0       # a zero head stays zero
+    w = wl.gen_norm_w(hd, seed=hd + 1)
+    out = oracle_mod.head_rmsnorm(y, hd, w, wl.EPS)
+    # torch's rms_norm over the last dimension of [M, H, hd], in float64
+    import torch
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(y.astype(np.float64)).reshape(M, H, hd), (hd,),
+                                       torch.from_numpy(w.astype(np.float64)), eps=wl.EPS).reshape(M, H * hd).numpy()
+    tol = 3.01 * 2.0 ** -24 * np.abs(ref) + 1e-30
+    assert np.all(np.abs(out - ref) <= tol)
+    assert np.all(out[2, 3 * hd:] == 0.0)
+    # per head, not per row: the whole-row norm of the same data differs
+    whole = oracle_mod.rmsnorm(y, np.tile(w, H), wl.EPS)
+    assert not np.allclose(whole, out, rtol=1e-3)
+
+
+def test_head_rmsnorm_heads_are_independent(oracle_mod):
+    hd, H = 128, 3
+    y = wl.gen_x(2, H * hd, seed=9)
+    w = np.ones(hd, np.float32)
+    base = oracle_mod.head_rmsnorm(y, hd, w, wl.EPS)
+    y2 = y.copy()
+    y2[:, :hd] *= 8.0  # a power of two: the head's rstd scales exactly, its output is unchanged up to eps
+    out = oracle_mod.head_rmsnorm(y2, hd, w, wl.EPS)
+    assert np.array_equal(out[:, hd:], base[:, hd:])
+    assert np.allclose(out[:, :hd], base[:, :hd], rtol=1e-6)
+    # unit weights: every head's mean square is 1 up to eps
+    ms = (base.astype(np.float64) ** 2).reshape(2, H, hd).mean(axis=2)
+    assert np.allclose(ms, 1.0, rtol=1e-5)
+
+
+def test_forward_qk_is_head_norm_of_forward(oracle_mod):
+    M, K, N, hd = 3, 256, 256, 128
+    x = wl.gen_x(M, K, seed=1)
+    g = wl.gen_norm_w(K, seed=2)
+    hw = wl.gen_norm_w(hd, seed=3)
+    packed, ws = oracle_mod.pack_i2s(wl.gen_latent_w(N, K, seed=4))
+    y = oracle_mod.bitlinear_forward_qk(x, g, packed, ws, N, hd, hw)
+    assert np.array_equal(y, oracle_mod.head_rmsnorm(oracle_mod.bitlinear_forward(x, g, packed, ws, N), hd, hw))
