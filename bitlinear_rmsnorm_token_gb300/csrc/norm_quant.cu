@@ -44,9 +44,12 @@ __device__ __forceinline__ void store_codes4<__half>(__half* dst, float4 n, floa
 // which spares the predicated-off groups) is loaded once into registers;
 // kNC == 0: any K, the row is read three times (L1/L2 after the first).
 // kGlu (kNC > 0 only): the row is act(x) * up, computed as it is loaded.
-// (kGlu: at most 128 registers, two CTAs per SM, like the plain long-row form)
+// At most 128 registers (two CTAs per SM): a CTA normalises 8 rows and exits,
+// so a second resident CTA overlaps one's reductions with the other's loads
+// (the K = 2048 form took 168 registers, one CTA per SM and 53% of DRAM
+// bandwidth); every form, rows of up to 24 float4 per lane included, fits.
 template <typename InT, typename OutT, int kNC, bool kExact, bool kGlu = false>
-__global__ void __launch_bounds__(kNqWarps * 32, kGlu ? 2 : 1) k_rmsnorm_quant(const InT* __restrict__ x, const float* __restrict__ g,
+__global__ void __launch_bounds__(kNqWarps * 32, 2) k_rmsnorm_quant(const InT* __restrict__ x, const float* __restrict__ g,
                                                                  int64_t M, int K, float eps, OutT* __restrict__ codes,
                                                                  float* __restrict__ a_scale,
                                                                  int32_t* __restrict__ rowsum,
