@@ -151,3 +151,17 @@ def test_head_norm_argument_errors(L):
     assert q(FAKE, FAKE, FAKE, 1.0, 1, 128, 200, 1e-6, 128, FAKE, FAKE, None) == bn.ERR_UNSUPPORTED_SHAPE
     assert q(FAKE, FAKE, FAKE, 1.0, 1, 128, 256, 1e-6, 128, ODD, FAKE, None) == bn.ERR_MISALIGNED
     assert q(None, FAKE, FAKE, 1.0, 1, 128, 256, 1e-6, 128, FAKE, FAKE, None) == bn.ERR_INVALID_ARG
+
+
+def test_typed_binding_rejects_unsupported_dtypes():
+    """The binding checks element types before it touches a device."""
+    import torch
+
+    x = torch.zeros((2, 128), dtype=torch.bfloat16)
+    packed = torch.zeros(4 * 32 + 4, dtype=torch.uint8)
+    with pytest.raises(TypeError):  # bf16 norm weights are not a supported type
+        bn.bitlinear_forward_typed(x, torch.zeros(128, dtype=torch.bfloat16), packed, 1.0, 4)
+    with pytest.raises(TypeError):  # nor are float64 activations
+        bn.bitlinear_forward_typed(x.double(), torch.zeros(128), packed, 1.0, 4)
+    with pytest.raises(TypeError):  # nor an int8 output
+        bn.bitlinear_forward_typed(x, torch.zeros(128), packed, 1.0, 4, y=torch.zeros((2, 4), dtype=torch.int8))
