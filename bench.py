@@ -416,6 +416,24 @@ def run_decode(args, rank, world, local):
     e1.synchronize()
     _, _, e2e_eager = aggregate(e0.elapsed_time(e1), float(step_bytes) * eager_steps, world)
 
+    # cold: L2 flushed before each launch (a write of 2x L2), the layer timed
+    # alone between events (the flush is still running when the layer and its
+    # events are enqueued, so no host gap falls inside)
+    flush = torch.empty(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=device)
+    cold = []
+    with torch.cuda.stream(stream):
+        for i in range(21):
+            flush.fill_(float(i))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            cold.append(a.elapsed_time(b))
+    del flush
+    cold_ms = float(np.median(cold[1:]))
+
     hbm, _, _, peak_kind = peaks()
     per_launch_ms = ms_local / args.steps
     achieved = step_bytes / (per_launch_ms * 1e-3) / 1e9
@@ -445,16 +463,18 @@ def run_decode(args, rank, world, local):
                 "serial_api": "the same three calls in one stream, captured in a CUDA graph",
                 "eager_value": round(e2e_eager / 1e9, 2),
                 "eager_api": "the same three calls issued from Python every step, one stream"},
+        "cold_l2": {"us_per_layer": round(cold_ms * 1e3, 3), "GBps": round(step_bytes / (cold_ms * 1e-3) / 1e9, 2),
+                    "method": "L2 flushed by a 2x L2 write before each launch; median of 20 launches"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "parity": {"oracle_worst_row_rel_l2": worst, "device_status": bn.status_string(dev_status)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline_decode(args)
+        out["cpu_baseline"] = cpu_baseline_decode(args, single_thread=True)
     return out
 
 
-def cpu_baseline_decode(args, budget_s=None, max_steps=None, warmup=0):
+def cpu_baseline_decode(args, budget_s=None, max_steps=None, warmup=0, single_thread=False):
     """The oracle, as it stands, on the host cores: whole decode layers (7
     projections at M=1, packed on the host by the oracle).  `warmup` untimed
     layers, then timed layers until `max_steps` or ~budget_s, whichever first."""
@@ -487,9 +507,26 @@ def cpu_baseline_decode(args, budget_s=None, max_steps=None, warmup=0):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "steps": n, "seconds": dt,
-            "sample": f"{n} decode layers (7 projections each, M=1) in {dt:.1f} s"}
+    # the oracle parallelises over token rows; a decode layer has one, so one
+    # core does the work whatever the thread count
+    out = {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "threads_available": oracle.num_threads(), "kind": "oracle", "steps": n, "seconds": dt,
+           "sample": f"{n} decode layers (7 projections each, M=1, one token row: one core works) in {dt:.1f} s"}
+    if single_thread:
+        # the same with the thread count set to one (a short sample)
+        cores = oracle.num_threads()
+        oracle.set_num_threads(1)
+        try:
+            n1, t1 = 0, time.perf_counter()
+            while n1 < 2 or time.perf_counter() - t1 < min(3.0, budget_s):
+                one_layer(n1)
+                n1 += 1
+            d1 = time.perf_counter() - t1
+        finally:
+            oracle.set_num_threads(cores)
+        out["single_thread"] = {"value": round(step_bytes * n1 / d1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "sample": f"{n1} decode layers in {d1:.1f} s"}
+    return out
 
 
 # ----------------------------------------------------- other workloads
@@ -784,8 +821,11 @@ def run_prefill(args, rank, world, local, which):
         worst = max(worst, float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max()))
     ms_all, _, ops_per_s = aggregate(ms * args.steps, flops * args.steps, world)
     ms = ms_all / max(1, args.steps)
+    hbm, bf16, _, _ = peaks()
     return {"metric": METRIC, "value": round(ops_per_s / 1e12, 2), "unit": "TOPS", "n_gpus": world,
             "ms_per_step": ms, "steps": args.steps, "alg_GBps": alg_bytes * world / (ms * 1e-3) / 1e9,
+            "tensor_frac": round(ops_per_s / 1e12 / bf16, 4),
+            "hbm_frac": round(alg_bytes * world / (ms * 1e-3) / 1e9 / hbm, 4),
             "config": {"workload": which, "tokens": M, "layers": n_layers, "io": args.io,
                        "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
             "parity": {"oracle_worst_row_rel_l2": worst}}
