@@ -333,7 +333,8 @@ def test_forward_matches_oracle(oracle_mod, M, K, N):
 # direct stores when the row pitch is not a multiple of 16 bytes, and by the
 # split-K read-back)
 TYPED_CASES = [(1, 1024, 2048), (4, 16384, 600), (16, 16384, 1024), (300, 1024, 640), (200, 3072, 130),
-               (128, 16384, 1024), (2048, 640, 2048)]
+               (128, 16384, 1024), (2048, 640, 2048),
+               (70, 1280, 256), (70, 3200, 256)]  # norm launch: generic row widths (24 groups, re-read)
 TYPED_DTYPES = [("bf16", "f32", "bf16"), ("f16", "f16", "f16"), ("f32", "f16", "bf16"), ("bf16", "f16", "f32")]
 _TT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 _OT = {"f32": 0, "f16": 1, "bf16": 2}
