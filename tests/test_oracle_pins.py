@@ -271,6 +271,85 @@ def test_rescale_against_f64(oracle_mod):
     assert np.all(np.abs(y - ref) <= 4 * 2.0 ** -24 * np.abs(ref))
 
 
+def _nearest_f32(r):
+    """The float32 nearest to the rational r, ties to the even significand, found
+    from the exact value alone (no float32 arithmetic): normal range only."""
+    from fractions import Fraction
+
+    if r == 0:
+        return 0.0
+    a = abs(r)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    assert -126 <= e <= 127
+    unit = Fraction(2) ** (e - 23)
+    m = round(a / unit)  # Fraction rounding: half to even
+    v = m * unit
+    return float(v if r > 0 else -v)
+
+
+def test_rescale_each_operation_rounded_once_in_stated_order(oracle_mod):
+    """y = ((float)acc * (1/a_scale)) * (1/w_scale): each of the two reciprocals
+    and two products is the float32 nearest to its exact rational value, in that
+    order.  The other order gives different bits on these inputs, so a swapped
+    order fails here."""
+    from fractions import Fraction as F
+
+    rng = np.random.default_rng(19)
+    acc = rng.integers(-2_000_000, 2_000_000, size=(8, 16), dtype=np.int64)
+    a_scale = rng.uniform(1.0, 200.0, size=8).astype(np.float32)
+    w_scale = np.float32(rng.uniform(10.0, 80.0))
+    y = oracle_mod.rescale(acc, a_scale, float(w_scale))
+    inv_w = F(_nearest_f32(1 / F(float(w_scale))))
+    other_order = 0
+    for m in range(acc.shape[0]):
+        inv_a = F(_nearest_f32(1 / F(float(a_scale[m]))))
+        for n in range(acc.shape[1]):
+            a = F(int(acc[m, n]))  # |acc| < 2^24: exact in float
+            want = _nearest_f32(F(_nearest_f32(a * inv_a)) * inv_w)
+            assert float(y[m, n]) == want, (m, n)
+            other_order += _nearest_f32(F(_nearest_f32(a * inv_w)) * inv_a) != want
+    assert other_order > 0
+
+
+def _exact_dequant_dot(q, t, a, w):
+    """sum_k (q_k / a) * (t_k / w) in exact rationals."""
+    from fractions import Fraction as F
+
+    s = sum(int(qk) * int(tk) for qk, tk in zip(q, t))
+    return F(s) / (F(float(a)) * F(float(w)))
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 128, 1), (5, 128, 33), (17, 256, 9), (3, 256, 32)])
+def test_forward_matches_f64_dequantised_product(oracle_mod, M, K, N):
+    """The brute-force double product of the dequantised codes,
+    sum_k (q/a_scale)(t/w_scale), against the exact rationals, and the oracle's
+    float y against it: acc is exact in float (|acc| < 2^24), then two
+    reciprocals and two products each add at most 2^-24 relative error."""
+    x, g, w = wl.gen_projection(0, K, N, M, K, N)
+    x[0, :] = 0.0  # a zero row: y must be exactly zero
+    if M > 2:
+        x[2, :] = 3.0  # a constant row: its codes follow the norm weight, largest +127
+    packed, ws = oracle_mod.pack_i2s(w)
+    y, xn, q, a_s, acc = oracle_mod.bitlinear_forward(x, g, packed, ws, N, intermediates=True)
+    t = oracle_mod.quantize_ternary(w, ws)  # the weights' own ternary values (not unpacked)
+    y64 = oracle_mod.dequant_dot_f64(q, t, a_s, ws)
+    # double accumulation: at most (K+2) 2^-53 of the sum of |terms| from exact
+    sum_abs = (np.abs(q).astype(np.float64) @ np.abs(t).astype(np.float64).T) / a_s.astype(np.float64)[:, None] / float(ws)
+    acc_err = 1.01 * (K + 2) * 2.0 ** -53 * sum_abs
+    rng = np.random.default_rng(M * N)
+    for m, n in [(0, 0), (M - 1, N - 1)] + [tuple(v) for v in zip(rng.integers(0, M, 6), rng.integers(0, N, 6))]:
+        exact = _exact_dequant_dot(q[m], t[n], a_s[m], ws)
+        assert abs(float(exact) - y64[m, n]) <= acc_err[m, n] + 1e-300
+    assert np.all(np.abs(y.astype(np.float64) - y64) <= 4.01 * 2.0 ** -24 * np.abs(y64) + 2 * acc_err)
+    assert np.all(y[0] == 0.0)
+    if M > 2:
+        assert q[2].max() == 127 and q[2].min() > 0
+
+
 # ------------------------------------------------------------ whole chain ---
 
 @pytest.mark.parametrize("M,K,N", [(3, 128, 5), (4, 640, 33), (2, 1024, 17)])
