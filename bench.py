@@ -8,7 +8,11 @@ input, norm weight and ternary weights, run as ONE grouped launch
 (bitnet_bitlinear_forward_group).  Steps rotate through a pool of distinct
 layers whose I2_S weights total more than twice the L2 cache, so every step
 streams its weights from HBM.  Metric: weight-stream GB/s = algorithmic bytes
-(packed weights + scale + x + norm weight + y) per step / time.
+(packed weights + scale + x + norm weight + y) per step / time.  The same line
+carries a `prefill` object, the other half of the metric, timed in the same run:
+int8-TOPS of the Qwen3-shaped 28-layer stack at 32768 tokens and of one
+compute-bound projection (M=16384, K=4096, N=16384), each against the bf16 dense
+peak and HBM, with sampled rows checked against the oracle (--no-prefill skips it).
 
 Other workloads (--workload): q_proj_m8 (M=8, K=1024, N=2048), proj (one
 projection, --m/--k/--n), gemma3_prefill
@@ -196,6 +200,18 @@ def aggregate(ms_local, units_local, world):
 
 # --------------------------------------------------------- decode workload
 
+def decode_config(world):
+    """The workload the default line (and the reference arm) measures."""
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    shapes = wl.QWEN3_0P6B_LAYER
+    return {"workload": "qwen3_0p6b_decode_layer_M1_7proj", "tokens": 1,
+            "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes],
+            "bytes_per_step": decode_layer_bytes(shapes, 1),
+            "l2": "inputs larger than L2: GPU steps rotate through a weight pool > 2x L2 (no flush)",
+            "parallelism": f"replicas x{world}"}
+
+
 def decode_layer_bytes(layer_shapes, M=1):
     """Algorithmic bytes of one step: I2_S weights + scale, x, norm weight, y."""
     return sum(p.N * p.K // 4 + 4 + M * p.K * 4 + p.K * 4 + M * p.N * 4 for p in layer_shapes)
@@ -265,53 +281,62 @@ def run_decode(args, rank, world, local):
     # one graph holds `chunk` consecutive steps; replays continue the rotation
     chunk = n_layers * max(1, 512 // n_layers)
     with torch.cuda.stream(stream):
-        for i in range(n_layers):  # eager warm-up (also loads the module)
+        for i in range(n_layers):  # eager first calls (load the module, set up the device)
             bn.bitlinear_forward_group(pool[i]["desc"], M, wl.EPS, flags, stream=stream)
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(chunk):
-            bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
-    # tail graph so that exactly `steps` steps are timed
-    tail_n = args.steps % chunk
-    tail = None
-    if tail_n:
-        tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tail, stream=stream):
-            for i in range(tail_n):
-                bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+    graphs = {}
+
+    def graph_of(n):
+        """A CUDA graph of n consecutive steps of the rotation (n <= chunk)."""
+        if n not in graphs:
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_, stream=stream):
+                for i in range(n):
+                    bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+            graphs[n] = g_
+        return graphs[n]
 
     def run_steps(n):
+        """Exactly n steps: whole graphs of `chunk` steps, then one of the rest."""
         with torch.cuda.stream(stream):
             for _ in range(n // chunk):
-                graph.replay()
+                graph_of(chunk).replay()
             if n % chunk:
-                assert tail is not None and n % chunk == tail_n
-                tail.replay()
+                graph_of(n % chunk).replay()
 
+    # Timed region: exactly `steps` steps between two events, repeated
+    # `repeats` times; the per-step time is the median repeat's.  Ahead of each
+    # repeat an untimed pre-roll graph is queued, so the GPU is already busy
+    # when the first event fires and the host's graph-launch latency falls
+    # outside the region (the steps themselves run back to back as in a long run).
+    preroll = min(chunk, 64)
+    repeats = 5
+    graph_of(preroll)
+    graph_of(chunk)
+    if args.steps % chunk:
+        graph_of(args.steps % chunk)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.5)
-    warm_reps = max(1, -(-args.warmup // chunk))  # at least `warmup` steps, whole graphs
-    with torch.cuda.stream(stream):
-        for _ in range(warm_reps):
-            graph.replay()
-    args.warmup = warm_reps * chunk
+    run_steps(args.warmup)  # exactly `warmup` untimed steps
     stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(repeats)]
     t0 = time.time()
-    ev0.record(stream)
-    run_steps(args.steps)
-    ev1.record(stream)
-    ev1.synchronize()
+    with torch.cuda.stream(stream):
+        for ev0, ev1 in evs:
+            graph_of(preroll).replay()
+            ev0.record(stream)
+            run_steps(args.steps)
+            ev1.record(stream)
+    evs[-1][1].synchronize()
     t1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
     sampler.stop()
-    ms_local = ev0.elapsed_time(ev1)
+    rep_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_local = float(np.median(rep_ms))
     ms, _, value = aggregate(ms_local, float(step_bytes) * args.steps, world)
     value /= 1e9
     clocks = sampler.summary(t0, t1)
@@ -443,13 +468,13 @@ def run_decode(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 x ternary -> int32, fp32 I/O", "data": "synthetic",
-        "config": {"workload": "qwen3_0p6b_decode_layer_M1_7proj", "tokens": M,
-                   "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes],
-                   "bytes_per_step": step_bytes, "weight_pool_layers": n_layers,
-                   "weight_pool_bytes": n_layers * weight_bytes,
-                   "l2": "inputs larger than L2: steps rotate through a weight pool > 2x L2 (no flush)",
-                   "launch": "one grouped kernel per step, CUDA graph replay, programmatic dependent launch",
-                   "parallelism": f"replicas x{world}"},
+        "config": decode_config(world),
+        "setup": {"weight_pool_layers": n_layers, "weight_pool_bytes": n_layers * weight_bytes,
+                  "launch": "one grouped kernel per step, CUDA graph replay, programmatic dependent launch"},
+        "timing": {"repeats": repeats, "ms_per_repeat": [round(v, 6) for v in rep_ms],
+                   "statistic": "median repeat; each repeat times exactly `steps` steps between two events",
+                   "preroll_steps": preroll,
+                   "preroll": "an untimed graph of this many steps queued before each repeat's first event"},
         "roofline": {"bound": "hbm", "kernel": "k_decode (grouped BitLinear GEMV)", "achieved": round(achieved, 2),
                      "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic,
@@ -465,10 +490,20 @@ def run_decode(args, rank, world, local):
                 "eager_api": "the same three calls issued from Python every step, one stream"},
         "cold_l2": {"us_per_layer": round(cold_ms * 1e3, 3), "GBps": round(step_bytes / (cold_ms * 1e-3) / 1e9, 2),
                     "method": "L2 flushed by a 2x L2 write before each launch; median of 20 launches"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps,  # per timed region: one grouped launch per step
         "clocks": clocks,
         "parity": {"oracle_worst_row_rel_l2": worst, "device_status": bn.status_string(dev_status)},
     }
+    del pool, graphs
+    torch.cuda.empty_cache()
+    if not args.no_prefill:
+        # the prefill half of the metric, timed in the same run: the Qwen3-shaped
+        # 28-layer stack at 32768 tokens (fp32 I/O) and one compute-bound shape
+        out["prefill"] = {
+            "qwen3_0p6b_stack_M32768": measure_prefill(args, world, local, "qwen3_prefill_stack", "f32",
+                                                       steps=min(args.steps, 10), warmup=2),
+            "proj_M16384_K4096_N16384": measure_point(args, world, local, 16384, 4096, 16384),
+        }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_decode(args, single_thread=True)
     return out
@@ -507,11 +542,12 @@ def cpu_baseline_decode(args, budget_s=None, max_steps=None, warmup=0, single_th
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    # the oracle parallelises over token rows; a decode layer has one, so one
-    # core does the work whatever the thread count
-    out = {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
-           "threads_available": oracle.num_threads(), "kind": "oracle", "steps": n, "seconds": dt,
-           "sample": f"{n} decode layers (7 projections each, M=1, one token row: one core works) in {dt:.1f} s"}
+    # the oracle's contraction shares its (row, column) pairs among the threads,
+    # so the one token row of a decode layer spreads over every host core
+    cores = oracle.num_threads()
+    out = {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+           "kind": "oracle", "steps": n, "seconds": dt,
+           "sample": f"{n} decode layers (7 projections each, M=1) in {dt:.1f} s on {cores} threads"}
     if single_thread:
         # the same with the thread count set to one (a short sample)
         cores = oracle.num_threads()
@@ -778,7 +814,28 @@ def prefill_projection_step(torch, bn, wl, shapes, M, device, config, layer, out
     return items
 
 
-def run_prefill(args, rank, world, local, which):
+def sampled_row_parity(oracle, bn, x, g, packed, ws, N, y, rows, y_dtype=0):
+    """Oracle check of sampled rows: y under the row contract (worst relative
+    L2 distance), and the int8 codes of the same rows from the norm launch
+    against the oracle's (count and size of any differences)."""
+    xr = x[rows]
+    ref = oracle.bitlinear_forward_typed(xr.float().cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws, N,
+                                         y_dtype=y_dtype)
+    yy = y[rows].float().cpu().numpy()
+    worst = float((np.linalg.norm(yy - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)).max())
+    flips = 0
+    if y_dtype == 0:
+        codes, _, _ = bn.rmsnorm_quant_a8(xr.contiguous(), g)
+        q_o, _, _ = oracle.quant_a8(oracle.rmsnorm(xr.cpu().numpy(), g.cpu().numpy()))
+        d = np.abs(codes.cpu().numpy().astype(np.int32) - q_o.astype(np.int32))
+        flips = int(np.sum(d != 0))
+        assert d.max(initial=0) <= 1, "an int8 code differs from the oracle's by more than one"
+    return worst, flips
+
+
+def measure_prefill(args, world, local, which, io_name="f32", steps=None, warmup=None):
+    """One step = every projection of the workload at M = 32768 tokens, issued
+    eagerly on one stream (each call one norm launch and one contraction)."""
     import torch
 
     import bitlinear_rmsnorm_token_gb300 as bn
@@ -787,13 +844,15 @@ def run_prefill(args, rank, world, local, which):
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    steps = max(1, args.steps if steps is None else steps)
+    warmup = max(1, min(args.warmup, 3) if warmup is None else warmup)
     M = 32768
     if which == "gemma3_prefill":
         shapes, n_layers, frac, cfg = wl.GEMMA3_270M_LAYER, 1, 0.01, 2
     else:
         shapes, n_layers, frac, cfg = wl.QWEN3_0P6B_LAYER, wl.QWEN3_0P6B_LAYERS, 0.0, 3
     stream = torch.cuda.Stream(device)
-    io = {"f32": None, "f16": torch.float16, "bf16": torch.bfloat16}[args.io]
+    io = {"f32": None, "f16": torch.float16, "bf16": torch.bfloat16}[io_name]
     io_bytes = 4 if io is None else 2
     layers = [prefill_projection_step(torch, bn, wl, shapes, M, device, cfg, l, frac, stream, io)
               for l in range(n_layers)]
@@ -808,36 +867,93 @@ def run_prefill(args, rank, world, local, which):
                     bn.bitlinear_forward_typed(x, g, packed, ws, p.N, wl.EPS, y, stream=stream)
 
     with torch.cuda.stream(stream):
-        ms = time_region(torch, stream, step, max(1, args.steps), max(1, min(args.warmup, 3)))
+        ms = time_region(torch, stream, step, steps, warmup)
     flops = sum(2.0 * M * p.N * p.K for p in shapes) * n_layers
     alg_bytes = sum(M * p.K * io_bytes + p.K * 4 + p.N * p.K / 4 + 4 + M * p.N * io_bytes for p in shapes) * n_layers
     # sampled-row parity of the first and last projection
-    worst = 0.0
+    worst, flips = 0.0, 0
     rows = np.random.default_rng(0).choice(M, 32, replace=False)
     for (p, x, g, packed, ws, y) in (layers[0][0], layers[-1][-1]):
-        ref = oracle.bitlinear_forward_typed(x[rows].float().cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws,
-                                             p.N, y_dtype={"f32": 0, "f16": 1, "bf16": 2}[args.io])
-        yy = y[rows].float().cpu().numpy()
-        worst = max(worst, float((np.linalg.norm(yy - ref, axis=1) / np.linalg.norm(ref, axis=1)).max()))
-    ms_all, _, ops_per_s = aggregate(ms * args.steps, flops * args.steps, world)
-    ms = ms_all / max(1, args.steps)
-    hbm, bf16, _, _ = peaks()
-    return {"metric": METRIC, "value": round(ops_per_s / 1e12, 2), "unit": "TOPS", "n_gpus": world,
-            "ms_per_step": ms, "steps": args.steps, "alg_GBps": alg_bytes * world / (ms * 1e-3) / 1e9,
+        w_, f_ = sampled_row_parity(oracle, bn, x, g, packed, ws, p.N, y, rows,
+                                    {"f32": 0, "f16": 1, "bf16": 2}[io_name])
+        worst, flips = max(worst, w_), flips + f_
+    del layers
+    torch.cuda.empty_cache()
+    ms_all, _, ops_per_s = aggregate(ms * steps, flops * steps, world)
+    ms = ms_all / steps
+    hbm, bf16, bf16_s, kind = peaks()
+    return {"value": round(ops_per_s / 1e12, 2), "unit": "TOPS", "ms_per_step": ms, "steps": steps,
+            "warmup": warmup, "alg_GBps": alg_bytes * world / (ms * 1e-3) / 1e9,
             "tensor_frac": round(ops_per_s / 1e12 / bf16, 4),
+            "tensor_frac_sustained": round(ops_per_s / 1e12 / bf16_s, 4),
             "hbm_frac": round(alg_bytes * world / (ms * 1e-3) / 1e9 / hbm, 4),
-            "config": {"workload": which, "tokens": M, "layers": n_layers, "io": args.io,
-                       "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
-            "parity": {"oracle_worst_row_rel_l2": worst}}
+            "peaks": f"{kind}: bf16 dense {bf16} TFLOP/s burst, {bf16_s} sustained; HBM {hbm} GB/s",
+            "config": {"workload": which, "tokens": M, "layers": n_layers, "io": io_name,
+                       "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes],
+                       "launch": "eager, one stream; inputs larger than L2"},
+            "parity": {"oracle_worst_row_rel_l2": worst, "rows_checked": 2 * len(rows), "codes_off_by_one": flips}}
+
+
+def measure_point(args, world, local, M, K, N, steps=5, warmup=2):
+    """One projection shape, cycling through distinct weight tensors (inputs
+    larger than L2 through x and y), eager calls of bitnet_bitlinear_forward."""
+    import torch
+
+    import bitlinear_rmsnorm_token_gb300 as bn
+    import oracle
+    from bitlinear_rmsnorm_token_gb300 import workloads as wl
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    sets = []
+    for i in range(4):
+        w = wl.gen_device((N, K), wl.seed_for(4, K, N, i), device, std=0.02)
+        sets.append(bn.pack_i2s(w))
+        del w
+    g = torch.from_numpy(wl.gen_norm_w(K, seed=K)).to(device)
+    x = wl.gen_device((M, K), wl.seed_for(4, M, K, N), device)
+    y = torch.empty((M, N), dtype=torch.float32, device=device)
+
+    def cycle():
+        for packed, sc in sets:
+            bn.bitlinear_forward(x, g, packed, sc, N, wl.EPS, y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        ms = time_region(torch, stream, cycle, steps, warmup) / len(sets)
+    rows = np.random.default_rng(1).choice(M, 8, replace=False)
+    packed, sc = sets[-1]
+    worst, flips = sampled_row_parity(oracle, bn, x, g, packed, sc, N, y, rows)
+    del sets, x, y
+    torch.cuda.empty_cache()
+    ms_all, _, ops_per_s = aggregate(ms * steps, 2.0 * M * N * K * steps, world)
+    ms = ms_all / steps
+    b = N * K / 4 + 4 + M * K * 4 + K * 4 + M * N * 4
+    hbm, bf16, bf16_s, kind = peaks()
+    return {"value": round(ops_per_s / 1e12, 2), "unit": "TOPS", "us_per_projection": ms * 1e3,
+            "tensor_frac": round(ops_per_s / 1e12 / bf16, 4),
+            "tensor_frac_sustained": round(ops_per_s / 1e12 / bf16_s, 4),
+            "hbm_frac": round(b * world / (ms * 1e-3) / 1e9 / hbm, 4),
+            "config": {"workload": f"proj_M{M}_K{K}_N{N}", "weights_cycled": len(sets),
+                       "launch": "eager bitnet_bitlinear_forward, one stream"},
+            "parity": {"oracle_worst_row_rel_l2": worst, "rows_checked": len(rows), "codes_off_by_one": flips}}
+
+
+def run_prefill(args, rank, world, local, which):
+    r = measure_prefill(args, world, local, which, args.io)
+    out = {"metric": METRIC, "n_gpus": world}
+    out.update(r)
+    return out
 
 
 def run_sweep(args, rank, world, local):
     """K, N in {1024, 4096, 8192, 16384} x M in {1, 16, 128, 2048, 16384}.  Each
     point cycles through enough distinct weight tensors to exceed twice the L2
-    (at most 1024), one projection call per tensor.  Where the temporaries fit
-    the no-alloc entry point's fixed scratch, the whole cycle is one CUDA graph
-    (kernel time, not Python launch time); otherwise calls are issued eagerly
-    (those points run >= 80 us per call)."""
+    (at most 1024), one projection call per tensor.  Where every temporary of
+    the allocating path's plan fits the no-alloc entry point's fixed scratch,
+    the whole cycle is one CUDA graph of that entry point (kernel time, not
+    Python launch time); otherwise calls are issued eagerly through
+    bitnet_bitlinear_forward (those points run >= 80 us per call)."""
     import torch
 
     import bitlinear_rmsnorm_token_gb300 as bn
@@ -861,8 +977,14 @@ def run_sweep(args, rank, world, local):
             for M in wl.SWEEP_M:
                 x = wl.gen_device((M, K), wl.seed_for(4, M, K, N), device)
                 y = torch.empty((M, N), dtype=torch.float32, device=device)
+                # graphed through the no-alloc entry point only when its fixed array
+                # holds the codes, the scales and the largest K-split workspace any
+                # plan could ask for (fp32 partial sums and one ticket per 128x64
+                # tile), so that it runs the same plan as bitnet_bitlinear_forward
+                r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
                 code_bytes = M * K * (1 if M <= 8 else 2)
-                graphed = ((code_bytes + 255) // 256) * 256 + 4 * M <= bn.NOALLOC_SCRATCH_BYTES
+                ws_bound = r256(M * N * 4) + 4 * (-(-M // 128)) * (-(-N // 64))
+                graphed = r256(code_bytes) + r256(4 * M) + ws_bound <= bn.NOALLOC_SCRATCH_BYTES
                 fwd = bn.bitlinear_forward_noalloc if graphed else bn.bitlinear_forward
 
                 def cycle():
@@ -907,15 +1029,13 @@ def run_reference(args, rank, world):
     oracle.build()
     warm = min(args.warmup, 3)
     cb = cpu_baseline_decode(args, budget_s=None, max_steps=args.steps, warmup=warm)
-    shapes = __import__("bitlinear_rmsnorm_token_gb300.workloads", fromlist=["x"]).QWEN3_0P6B_LAYER
     value = cb["value"]
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": cb["steps"], "steps_requested": args.steps, "warmup": warm,
             "ms_per_step": cb["seconds"] / max(1, cb["steps"]) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 x ternary -> int64, fp32",
             "data": "synthetic",
-            "config": {"workload": "qwen3_0p6b_decode_layer_M1_7proj", "tokens": 1,
-                       "projections": [f"{p.name} {p.K}->{p.N}" for p in shapes]},
+            "config": decode_config(world),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -938,6 +1058,7 @@ def main():
                     help="prefill workloads: element type of x and y (bitnet_bitlinear_forward_typed)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="default workload: skip the prefill block")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.steps_ref = args.steps

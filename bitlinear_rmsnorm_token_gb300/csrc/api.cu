@@ -47,8 +47,10 @@ int device_context(DeviceContext** out) {
     c.num_sms = prop.multiProcessorCount;
     void* ew = nullptr;
     if (cudaGetSymbolAddress(&ew, g_error_word) != cudaSuccess) return BITNET_ERR_CUDA;
+    // the word starts at zero when the module loads; it is not cleared here, so
+    // a timeout an earlier call recorded (the no-alloc entry point's, say) stays
+    // until bitnet_last_device_status reports it
     c.err_word = static_cast<unsigned*>(ew);
-    if (cudaMemset(c.err_word, 0, sizeof(unsigned)) != cudaSuccess) return BITNET_ERR_CUDA;
     cudaMemPoolProps pp = {};
     pp.allocType = cudaMemAllocationTypePinned;
     pp.handleTypes = cudaMemHandleTypeNone;

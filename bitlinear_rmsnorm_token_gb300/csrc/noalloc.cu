@@ -7,13 +7,15 @@
 // fragment), or a latency-critical loop where an allocation's cost or possible
 // failure is not acceptable.  They still pass their own inputs and outputs.
 //
-// How: the prefill path needs temporary space for the fp16 activation codes and
-// the per-token scales.  Here that space is one file-scope device array of
-// fixed size, loaded with the library (every GPU the library is used on keeps
-// it until the process exits).  Its device address is looked up once per device
-// with cudaGetSymbolAddress -- the array's name in host code is only a host-side
-// stand-in and must never be handed to a kernel.  Small token counts take the
-// decode path, which needs no temporary space at all.
+// How: most shapes need temporary space for the activation codes, the per-token
+// scales and, where K is split over CTAs, fp32 partial sums.  Here that space is
+// one file-scope device array of fixed size.  CUDA loads this file's module
+// (and with it the array) on a device the first time its address is asked for,
+// so the first call on each device does that for every shape, including the
+// fused few-token shapes that never touch the array; from then on the device
+// keeps the array until the process exits.  The array's name in host code is
+// only a host-side stand-in and must never be handed to a kernel: the device
+// address comes from cudaGetSymbolAddress, once per device.
 #include <mutex>
 
 #include "common.cuh"
@@ -79,6 +81,10 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   DeviceContext* ctx;
   int rc = device_context_nopool(&ctx);
   if (rc) return rc;
+  // looked up on every route, so that the first call on a device does all of
+  // the one-time set-up whichever shape it has
+  void* scratch = nullptr;
+  if ((rc = scratch_for_current_device(&scratch))) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (fused) {
     DecodeJob j = {};
@@ -92,8 +98,6 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
     return launch_decode(ctx, &j, 1, static_cast<int>(M), eps, true, false, s) == cudaSuccess ? BITNET_OK
                                                                                           : BITNET_ERR_CUDA;
   }
-  void* scratch = nullptr;
-  if ((rc = scratch_for_current_device(&scratch))) return rc;
   float* as = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + code_bytes);
   // every element of the used scratch region is written by the norm launch
   // before the contraction reads it, so nothing has to be cleared first
@@ -118,8 +122,10 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
     return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;
   }
   __half* f16 = static_cast<__half*>(scratch);
-  // up to 128 tokens: the split-K contraction, when its workspace also fits;
-  // the tokens-as-M contraction splits K too when its workspace fits
+  // 9..63 tokens: the split-K contraction, when its workspace also fits; the
+  // tokens-as-M contraction splits K too when its workspace fits.  When the
+  // workspace does not fit, the tokens-as-M contraction runs without a K split
+  // (the same y: every plan sums the same integers exactly).
   const size_t scale_bytes = (static_cast<size_t>(M) * 4 + 255) & ~size_t(255);
   const bool sk_shape = gemm_skinny_supported(M, K, N);
   const size_t gws_bytes = sk_shape ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N);

@@ -180,19 +180,28 @@ BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, in
  * e.g. a server that reserved all device memory for its own allocator at start-up,
  * or a latency-critical loop where an allocation's cost or failure is not
  * acceptable.  Same arguments and the same y as bitnet_bitlinear_forward.
- *   - Temporary data (fp16 activation codes and per-token scales, 2*M*K + 4*M
- *     bytes, rounded up) lives in one fixed 16 MiB device array that every GPU
- *     using the library keeps until the process exits.  Larger problems return
- *     BITNET_ERR_SCRATCH_LIMIT without launching anything; the shapes that
- *     bitnet_bitlinear_forward_group accepts (M <= 8, see there) need no
- *     scratch at all (one fused launch).
- *   - The first call on each device does one-time set-up (device properties and
- *     the array's device address); make that first call before any stream
- *     capture.
+ *   - Temporary data lives in one fixed 16 MiB device array that every GPU
+ *     using the library keeps until the process exits: the activation codes
+ *     (int8 for M <= 8, fp16 otherwise: M*K or 2*M*K bytes) and per-token
+ *     scales (4*M bytes), each rounded up to 256 bytes, then the fp32 partial
+ *     sums of a K split (up to 4*M*N bytes plus 4 bytes per output tile) where
+ *     the contraction splits K.  Problems whose codes and scales do not fit
+ *     return BITNET_ERR_SCRATCH_LIMIT without launching anything.  When the
+ *     codes and scales fit but the partial sums do not, the contraction runs
+ *     without the K split (the same y; a slower plan than
+ *     bitnet_bitlinear_forward's for those shapes).  Only M <= 8 with the fused
+ *     norm prologue (bitnet_bitlinear_forward_group's shapes, except K > 16384
+ *     with K a multiple of 2048, which take a separate norm launch) leave the
+ *     array untouched.
+ *   - The first call on each device, whatever its shape, does the one-time
+ *     set-up: device properties, and loading the array onto the device to look
+ *     up its address.  Make that first call before reserving the rest of device
+ *     memory for other use and before any stream capture.
  *   - All calls on a device share the one array, and it keeps whatever the last
- *     call left (every byte a call reads it first writes).  Calls whose work can
- *     overlap on the GPU -- different streams without ordering between them, or
- *     several host threads -- race on it and must be serialised by the caller. */
+ *     call left (every byte a call reads it first writes, and partial sums are
+ *     zeroed on the stream before use).  Calls whose work can overlap on the
+ *     GPU -- different streams without ordering between them, or several host
+ *     threads -- race on it and must be serialised by the caller. */
 BITNET_API int bitnet_bitlinear_forward_noalloc(const float* x, const float* norm_w,
                                                 const uint8_t* packed_w, float w_scale, int64_t M,
                                                 int64_t K, int64_t N, float eps, float* y,

@@ -1,6 +1,7 @@
 """CPU oracle for the W1.58A8 BitLinear projection -- TEST INFRASTRUCTURE ONLY.
 
-Thin numpy/ctypes wrapper over ``bitnet_oracle.c`` (plain C, OpenMP over rows).
+Thin numpy/ctypes wrapper over ``bitnet_oracle.c`` (plain C; OpenMP over
+independent rows, and over (row, column) pairs in the contraction).
 Only ``tests/``, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline leg use
 it; the CUDA library never does.  The C file cites, per function, the passage of
 the pages it restates.

@@ -226,7 +226,9 @@ int oracle_i2s_matmul(const int8_t* q, const uint8_t* packed, int64_t M, int64_t
   int8_t* t = (int8_t*)malloc((size_t)(N * K));
   if (!t) return 2;
   oracle_unpack_i2s(packed, N, K, t);
-#pragma omp parallel for schedule(static)
+  /* every output is one sequential sum of its own; threads share the (m, n)
+     pairs, so a single token row still spreads over the host's cores */
+#pragma omp parallel for collapse(2) schedule(static)
   for (int64_t m = 0; m < M; ++m)
     for (int64_t n = 0; n < N; ++n) {
       int64_t s = 0;

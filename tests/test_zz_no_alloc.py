@@ -3,8 +3,9 @@
 The no-alloc entry point serves callers that may not allocate device memory once
 running (a server that reserved all of HBM for its own allocator, a
 latency-critical loop).  It keeps its temporary data in one fixed 16 MiB device
-array shared by all calls, so two calls in a row with different shapes and data
-must each give the same y as the allocating entry point.  This file is collected
+array shared by all calls, so calls in a row with different shapes and data must
+each give the same y as the allocating entry point (bit for bit: both run the
+same kernels on the same integers) and agree with the oracle.  This file is collected
 last on purpose; it also passes on its own in a fresh process.
 """
 import ctypes
@@ -42,17 +43,54 @@ def _call(fn, x, g, packed, ws, N, y):
     return fn(p(x), p(g), p(packed), ctypes.c_float(ws), M, K, N, ctypes.c_float(wl.EPS), p(y), stream)
 
 
-def _assert_close(y, ref):
-    y = y.double().cpu().numpy()
-    ref = ref.double().cpu().numpy()
+def _assert_rows_match_oracle(oracle_mod, x, g, packed, ws, N, y, rows):
+    """Sampled rows against the oracle under the end-to-end row contract."""
+    ref = oracle_mod.bitlinear_forward(x[rows].cpu().numpy(), g.cpu().numpy(), packed.cpu().numpy(), ws, N)
+    got = y[rows].double().cpu().numpy()
     nrm = np.linalg.norm(ref, axis=1)
     zero = nrm == 0
-    assert np.all(y[zero] == 0.0)
-    rel = np.linalg.norm(y - ref, axis=1)[~zero] / nrm[~zero]
+    assert np.all(got[zero] == 0.0)
+    rel = np.linalg.norm(got - ref, axis=1)[~zero] / nrm[~zero]
     assert rel.size == 0 or rel.max() <= REL_L2_TOL
 
 
-def test_noalloc_matches_forward_two_calls_in_a_row(L):
+# One shape per route through the fixed array (M, K, N):
+ROUTES = {
+    "fused decode, no scratch": (4, 1024, 256),
+    "norm launch + decode on int8 codes in the array": (2, 18432, 512),
+    "norm launch + decode, K = 32768": (2, 32768, 256),
+    "9..63 tokens, K split, partial sums in the array": (16, 16384, 1024),
+    "9..63 tokens, K = N = 4096": (16, 4096, 4096),
+    "tokens-as-M, K split, partial sums in the array": (128, 16384, 1024),
+    "tokens-as-M, no split": (1000, 2048, 384),
+    "tokens-as-M, ragged": (257, 1024, 130),
+    # codes and scales fit (15.6 MiB) but the K split's partial sums would not:
+    # the contraction runs unsplit, with the same y
+    "tokens-as-M, K split dropped for lack of room": (1000, 8192, 128),
+}
+
+
+@pytest.mark.parametrize("order", ["forward", "reversed"])
+def test_noalloc_equals_forward_on_every_route(L, oracle_mod, order):
+    """Each route, called one after another so that every call finds the
+    previous call's bytes in the shared array: y equal bit for bit to the
+    allocating entry point's, and sampled rows within the oracle contract."""
+    names = list(ROUTES) if order == "forward" else list(reversed(ROUTES))
+    for i, name in enumerate(names):
+        M, K, N = ROUTES[name]
+        x, g, packed, ws = _case(M, K, N, 100 + i + (50 if order == "reversed" else 0))
+        y_ref = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call(L.bitnet_bitlinear_forward, x, g, packed, ws, N, y_ref) == bn.OK, name
+        assert _call(L.bitnet_bitlinear_forward_noalloc, x, g, packed, ws, N, y) == bn.OK, name
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref), name
+        rows = np.arange(M) if M <= 16 else np.random.default_rng(M).choice(M, 12, replace=False)
+        _assert_rows_match_oracle(oracle_mod, x, g, packed, ws, N, y, rows)
+    assert L.bitnet_last_device_status(None) == bn.OK
+
+
+def test_noalloc_matches_forward_two_calls_in_a_row(L, oracle_mod):
     # both shapes take the tensor-core path, which uses the fixed scratch array;
     # the second, smaller call leaves stale bytes of the first beyond its end
     for (M, K, N, seed) in ((1000, 2048, 384, 11), (257, 1024, 130, 12)):
@@ -62,7 +100,8 @@ def test_noalloc_matches_forward_two_calls_in_a_row(L):
         assert _call(L.bitnet_bitlinear_forward, x, g, packed, ws, N, y_ref) == bn.OK
         assert _call(L.bitnet_bitlinear_forward_noalloc, x, g, packed, ws, N, y) == bn.OK
         torch.cuda.synchronize()
-        _assert_close(y, y_ref)
+        assert torch.equal(y, y_ref)
+        _assert_rows_match_oracle(oracle_mod, x, g, packed, ws, N, y, np.arange(0, M, 37))
     assert L.bitnet_last_device_status(None) == bn.OK
 
 
@@ -73,7 +112,7 @@ def test_noalloc_small_m_and_size_limit(L):
     assert _call(L.bitnet_bitlinear_forward, x, g, packed, ws, 256, y_ref) == bn.OK
     assert _call(L.bitnet_bitlinear_forward_noalloc, x, g, packed, ws, 256, y) == bn.OK
     torch.cuda.synchronize()
-    _assert_close(y, y_ref)
+    assert torch.equal(y, y_ref)
     # 4096 tokens x 2048 features need 16 MiB + 16 KiB: refused before any launch
     big = ctypes.c_void_p(1 << 20)
     rc = L.bitnet_bitlinear_forward_noalloc(big, big, big, ctypes.c_float(1.0), 4096, 2048, 64,
