@@ -305,16 +305,50 @@ def run_decode(args, rank, world, local):
                 graph_of(n % chunk).replay()
 
     # Timed region: exactly `steps` steps between two events, repeated
-    # `repeats` times; the per-step time is the median repeat's.  Ahead of each
-    # repeat an untimed pre-roll graph is queued, so the GPU is already busy
-    # when the first event fires and the host's graph-launch latency falls
-    # outside the region (the steps themselves run back to back as in a long run).
+    # `repeats` times; the per-step time is the median repeat's.  Each repeat
+    # starts with one graph holding an untimed pre-roll of `preroll` steps and
+    # then the first timed steps.  The start event is recorded inside that graph
+    # on a side branch that waits for the last pre-roll step, so it fires when
+    # that step completes while the first timed step keeps its programmatic
+    # launch overlap with it (as every step has in a long run): the region is
+    # exactly `steps` step-to-step intervals of the steady state.  The rest of
+    # the steps follow as whole graphs; the end event follows the last step.
     preroll = min(chunk, 64)
     repeats = 5
+    first_n = min(args.steps, chunk)
+    side = torch.cuda.Stream(device)
+
+    def first_graph(ev0):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=stream):
+            for i in range(preroll):
+                bn.bitlinear_forward_group(pool[i % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            side.wait_event(fork)
+            ev0.record(side)
+            for i in range(first_n):
+                bn.bitlinear_forward_group(pool[(preroll + i) % n_layers]["desc"], M, wl.EPS, flags, stream=stream)
+            stream.wait_stream(side)
+        return g_
+
+    try:
+        starts = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(repeats)]
+        firsts = [first_graph(e) for e in starts]
+        start_event = "recorded inside the first graph on a branch after the last pre-roll step"
+    except (TypeError, RuntimeError):
+        # no event nodes in graphs: record the start event between the pre-roll
+        # graph and the timed steps instead (the first timed step then loses its
+        # overlap with the pre-roll)
+        torch.cuda.synchronize()
+        starts, firsts = [torch.cuda.Event(enable_timing=True) for _ in range(repeats)], None
+        first_n = 0
+        start_event = "recorded on the stream between the pre-roll graph and the first timed step"
+    rest = args.steps - first_n
     graph_of(preroll)
     graph_of(chunk)
-    if args.steps % chunk:
-        graph_of(args.steps % chunk)
+    if rest % chunk:
+        graph_of(rest % chunk)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.5)
@@ -322,13 +356,16 @@ def run_decode(args, rank, world, local):
     stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(repeats)]
+    evs = [(starts[r], torch.cuda.Event(enable_timing=True)) for r in range(repeats)]
     t0 = time.time()
     with torch.cuda.stream(stream):
-        for ev0, ev1 in evs:
-            graph_of(preroll).replay()
-            ev0.record(stream)
-            run_steps(args.steps)
+        for r, (ev0, ev1) in enumerate(evs):
+            if firsts is not None:
+                firsts[r].replay()
+            else:
+                graph_of(preroll).replay()
+                ev0.record(stream)
+            run_steps(rest)
             ev1.record(stream)
     evs[-1][1].synchronize()
     t1 = time.time()
@@ -473,8 +510,7 @@ def run_decode(args, rank, world, local):
                   "launch": "one grouped kernel per step, CUDA graph replay, programmatic dependent launch"},
         "timing": {"repeats": repeats, "ms_per_repeat": [round(v, 6) for v in rep_ms],
                    "statistic": "median repeat; each repeat times exactly `steps` steps between two events",
-                   "preroll_steps": preroll,
-                   "preroll": "an untimed graph of this many steps queued before each repeat's first event"},
+                   "preroll_steps": preroll, "start_event": start_event},
         "roofline": {"bound": "hbm", "kernel": "k_decode (grouped BitLinear GEMV)", "achieved": round(achieved, 2),
                      "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic,
@@ -494,7 +530,7 @@ def run_decode(args, rank, world, local):
         "clocks": clocks,
         "parity": {"oracle_worst_row_rel_l2": worst, "device_status": bn.status_string(dev_status)},
     }
-    del pool, graphs
+    del pool, graphs, firsts
     torch.cuda.empty_cache()
     if not args.no_prefill:
         # the prefill half of the metric, timed in the same run: the Qwen3-shaped
@@ -924,6 +960,7 @@ def measure_point(args, world, local, M, K, N, steps=5, warmup=2):
     rows = np.random.default_rng(1).choice(M, 8, replace=False)
     packed, sc = sets[-1]
     worst, flips = sampled_row_parity(oracle, bn, x, g, packed, sc, N, y, rows)
+    n_sets = len(sets)
     del sets, x, y
     torch.cuda.empty_cache()
     ms_all, _, ops_per_s = aggregate(ms * steps, 2.0 * M * N * K * steps, world)
@@ -934,7 +971,7 @@ def measure_point(args, world, local, M, K, N, steps=5, warmup=2):
             "tensor_frac": round(ops_per_s / 1e12 / bf16, 4),
             "tensor_frac_sustained": round(ops_per_s / 1e12 / bf16_s, 4),
             "hbm_frac": round(b * world / (ms * 1e-3) / 1e9 / hbm, 4),
-            "config": {"workload": f"proj_M{M}_K{K}_N{N}", "weights_cycled": len(sets),
+            "config": {"workload": f"proj_M{M}_K{K}_N{N}", "weights_cycled": n_sets,
                        "launch": "eager bitnet_bitlinear_forward, one stream"},
             "parity": {"oracle_worst_row_rel_l2": worst, "rows_checked": len(rows), "codes_off_by_one": flips}}
 
