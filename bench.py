@@ -659,10 +659,23 @@ def run_q_proj_m8(args, rank, world, local):
             "config": {"workload": "q_proj_M8_K1024_N2048", "launch": "CUDA graph, weight pool > 2x L2"}}
 
 
+def noalloc_fits(bn, M, K, N):
+    """True when the no-alloc entry point's fixed array holds the codes, the
+    scales and the largest K-split workspace any plan could ask for (fp32
+    partial sums and one ticket per 128x64 tile), so that it runs the same plan
+    as bitnet_bitlinear_forward."""
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    code_bytes = M * K * (1 if M <= 8 else 2)
+    ws_bound = r256(M * N * 4) + 4 * (-(-M // 128)) * (-(-N // 64))
+    return r256(code_bytes) + r256(4 * M) + ws_bound <= bn.NOALLOC_SCRATCH_BYTES
+
+
 def run_proj(args, rank, world, local):
-    """One projection of M tokens, K -> N (--m, --k, --n), through the no-alloc
-    entry point, a CUDA graph cycling through distinct weight tensors totalling
-    more than twice the L2 (kernel time, not launch time)."""
+    """One projection of M tokens, K -> N (--m, --k, --n), cycling through
+    distinct weight tensors totalling more than twice the L2.  Where the no-alloc
+    entry point's fixed scratch holds the plan's temporaries, the cycle is one
+    CUDA graph of that entry point (kernel time, not launch time); otherwise
+    bitnet_bitlinear_forward is called eagerly (such shapes run >= 80 us)."""
     import torch
 
     import bitlinear_rmsnorm_token_gb300 as bn
@@ -682,27 +695,34 @@ def run_proj(args, rank, world, local):
     x = wl.gen_device((M, K), wl.seed_for(5, M, K, N), device)
     y = torch.empty((M, N), dtype=torch.float32, device=device)
     stream = torch.cuda.Stream(device)
+    graphed = noalloc_fits(bn, M, K, N)
+    fwd = bn.bitlinear_forward_noalloc if graphed else bn.bitlinear_forward
 
     def cycle():
         for packed, sc in ws_list:
-            bn.bitlinear_forward_noalloc(x, g, packed, sc, N, wl.EPS, y, stream=stream)
+            fwd(x, g, packed, sc, N, wl.EPS, y, stream=stream)
 
     with torch.cuda.stream(stream):
         cycle()
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        cycle()
     reps = max(1, args.steps // nw)
-    with torch.cuda.stream(stream):
-        ms = time_region(torch, stream, graph.replay, reps, max(1, min(args.warmup, 3))) / nw
+    if graphed:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            cycle()
+        with torch.cuda.stream(stream):
+            ms = time_region(torch, stream, graph.replay, reps, max(1, min(args.warmup, 3))) / nw
+    else:
+        with torch.cuda.stream(stream):
+            ms = time_region(torch, stream, cycle, reps, max(1, min(args.warmup, 3))) / nw
     b = wb + 4 + M * K * 4 + K * 4 + M * N * 4
     hbm, bf16, _, _ = peaks()
     return {"metric": METRIC, "value": round(b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": world,
             "steps": reps * nw, "ms_per_step": ms, "us_per_projection": ms * 1e3,
             "tops": 2.0 * M * N * K / (ms * 1e-3) / 1e12, "hbm_frac": b / (ms * 1e-3) / 1e9 / hbm,
             "config": {"workload": f"proj_M{M}_K{K}_N{N}", "weights_cycled": nw,
-                       "launch": "CUDA graph of bitnet_bitlinear_forward_noalloc"}}
+                       "launch": "CUDA graph of bitnet_bitlinear_forward_noalloc" if graphed
+                       else "eager bitnet_bitlinear_forward, one stream"}}
 
 
 def run_glu_proj(args, rank, world, local):
@@ -1014,14 +1034,7 @@ def run_sweep(args, rank, world, local):
             for M in wl.SWEEP_M:
                 x = wl.gen_device((M, K), wl.seed_for(4, M, K, N), device)
                 y = torch.empty((M, N), dtype=torch.float32, device=device)
-                # graphed through the no-alloc entry point only when its fixed array
-                # holds the codes, the scales and the largest K-split workspace any
-                # plan could ask for (fp32 partial sums and one ticket per 128x64
-                # tile), so that it runs the same plan as bitnet_bitlinear_forward
-                r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
-                code_bytes = M * K * (1 if M <= 8 else 2)
-                ws_bound = r256(M * N * 4) + 4 * (-(-M // 128)) * (-(-N // 64))
-                graphed = r256(code_bytes) + r256(4 * M) + ws_bound <= bn.NOALLOC_SCRATCH_BYTES
+                graphed = noalloc_fits(bn, M, K, N)
                 fwd = bn.bitlinear_forward_noalloc if graphed else bn.bitlinear_forward
 
                 def cycle():

@@ -110,6 +110,13 @@ __device__ __forceinline__ void bulk_load_hint(void* dst_smem, const void* src, 
       : "memory");
 }
 
+// Brings [src, src + bytes) into the L2 (bytes % 16 == 0, src 16-byte aligned).
+// A prefetch has no effect on the values any load returns, so it may be issued
+// before the data is known to be final.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared (TMA).  x is the innermost coordinate.
 __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(

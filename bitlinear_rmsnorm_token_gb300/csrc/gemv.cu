@@ -823,6 +823,8 @@ bool decode_fused_supported(int64_t M, int64_t K) {
 cudaError_t launch_decode(const DeviceContext* ctx, const DecodeJob* jobs_in, int njobs, int M, float eps, bool fused,
                           bool weights_static, cudaStream_t s, int reserve_sms) {
   if (njobs < 1 || njobs > BITNET_MAX_GROUP) return cudaErrorInvalidValue;
+  if (njobs == 1 && fused && jobs_in[0].act == 0 && gemv_row1_supported(M, jobs_in[0].K))
+    return launch_gemv_row1(ctx, jobs_in[0], eps, weights_static, s);
   // Projections with the longest rows (the longest prologues) take the lowest
   // CTA indices: the CTAs dispatched last start latest, and the launch ends
   // with its slowest CTA.  Each projection's outputs do not depend on the order.

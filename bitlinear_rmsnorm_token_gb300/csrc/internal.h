@@ -104,6 +104,12 @@ bool decode_fused_glu_supported(int64_t M, int64_t K);  // the same, with the do
 // kernel with one CTA per row, then the decode kernel streaming weights
 // during it, beats every CTA normalising the whole row in its prologue.
 bool decode_split_preferred(int64_t M, int64_t K);
+// One token, K = 4096, 8192 or 16384, fused norm + quant: the row kernel
+// (activation codes in registers, 32 KB weight stages); launch_decode sends
+// such single-projection launches there.
+bool gemv_row1_supported(int64_t M, int64_t K);
+cudaError_t launch_gemv_row1(const DeviceContext* ctx, const DecodeJob& job, float eps, bool weights_static,
+                             cudaStream_t s);
 // reserve_sms: SMs left to the kernel this launch follows (its CTAs still
 // running when the decode CTAs start), so that every decode CTA is resident at
 // once.

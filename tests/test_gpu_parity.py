@@ -304,6 +304,11 @@ FWD_CASES = [
     (3, 16384, 300), (8, 8192, 64), (2, 16384, 4096),
     # fewer weight rows than CTAs, a single row, K = 12288
     (1, 16384, 96), (2, 4096, 150), (4, 4096, 5000), (1, 12288, 1),
+    # one token, K = 4096 / 8192 / 16384: the row kernel (CTA pairs sharing the
+    # prologue; one row, one row per CTA of a pair, a pair's second CTA with
+    # one row or none, partial 32 KB stages, slots reused across laps)
+    (1, 4096, 1), (1, 8192, 2), (1, 16384, 3), (1, 4096, 5), (1, 16384, 151), (1, 8192, 1000),
+    (1, 4096, 20000),
     # longer rows: row-per-CTA norm launch, then the decode launch streaming its
     # weight ring during it
     (1, 65536, 300), (2, 32768, 40),
