@@ -26,11 +26,14 @@
 //    passed a stage it adds up each row's partial sums, rescales the rows,
 //    writes y and refills the slot with the stage one lap later;
 //  * weights stream through a ring of three 64 KB stages (1-D bulk copies with
-//    an L2 evict-first policy).  The copies may start before the grid-dependency
-//    wait only when the caller declares the weights unchanged by earlier work on
-//    the stream; otherwise the first stages are prefetched into the L2 (no
-//    effect on any value read) before it.  The ring covers the prologue: the HBM
-//    stream runs while the row is normalised.
+//    an L2 evict-first policy).  The ring's first fill is prefetched into the L2
+//    before the grid-dependency wait (a prefetch changes no value any load
+//    returns, so this holds whatever earlier work on the stream writes); the
+//    copies themselves are issued once this CTA's share of x is loaded: issued
+//    earlier, they queue the prologue's loads of x (L2 hits) behind the weight
+//    misses (measured: ~1.6 us later prologue at K = 16384).  Deeper L2
+//    prefetching measured slower.  The ring then covers the rest of the
+//    prologue: the stream runs while the row is normalised.
 #include "common.cuh"
 #include "internal.h"
 #include "rowquant.cuh"
@@ -58,7 +61,7 @@ struct Row1Params {
   float* y;
   int32_t* acc_out;
   float eps;
-  int weights_static;
+  int weights_static;  // the norm weight may be read before the dependency wait
   int rows_per_cta;
 };
 
@@ -139,12 +142,9 @@ __global__ void __launch_bounds__(kR1Block, 1) k_gemv_row1(const __grid_constant
     tail->last_issued[s] = st;
   };
   const int first = min(kR1Stages, nst);
-  if (streamer && lane == 0) {
-    for (int st = 0; st < first; ++st) {
-      if (P.weights_static) issue(st);
-      else bulk_prefetch_l2(wsrc + static_cast<int64_t>(st) * kR1StageBytes, static_cast<unsigned>(stage_len(st)));
-    }
-  }
+  if (streamer && lane == 0)
+    for (int st = 0; st < first; ++st)
+      bulk_prefetch_l2(wsrc + static_cast<int64_t>(st) * kR1StageBytes, static_cast<unsigned>(stage_len(st)));
 
   // ------------------------------------------------------------- prologue
   // RMSNorm + absmax quant of the row by the 512 consumer threads: thread tid
@@ -168,8 +168,6 @@ __global__ void __launch_bounds__(kR1Block, 1) k_gemv_row1(const __grid_constant
   };
   if (P.weights_static) load_g();
   pdl_wait();  // x (and y) belong to the previous kernel's stream order
-  if (streamer && lane == 0 && !P.weights_static)
-    for (int st = 0; st < first; ++st) issue(st);
   if (!P.weights_static) load_g();
   int key = 0;
 #pragma unroll
@@ -180,6 +178,8 @@ __global__ void __launch_bounds__(kR1Block, 1) k_gemv_row1(const __grid_constant
   key = warp_max_int(key);
   if (lane == 0 && !streamer) tail->red_key[warp] = key;
   __syncthreads();
+  if (streamer && lane == 0)
+    for (int st = 0; st < first; ++st) issue(st);
   key = warp_max_int(lane < kR1Warps ? tail->red_key[lane] : 0);
   {
     const float scale = sq_scale(key);
