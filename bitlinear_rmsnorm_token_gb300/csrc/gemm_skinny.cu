@@ -23,20 +23,27 @@
 //   warp 12    TMA producer: the tokens' fp16 codes of the stage (two 64-wide
 //              slabs, 128-byte swizzle) into a 64 KB ring of their own that
 //              runs up to 16 stages ahead (a token load takes ~1.5 us to land);
-//              the tile's packed bytes arrive in
-//              groups of 4 block columns (128 rows x 128 contiguous bytes,
-//              128-byte swizzle, so that 8 consecutive rows read their columns
-//              from 8 different bank groups) into a ring of 4 slots (the
-//              weight stream needs ~64 KB in flight per SM to cover the HBM
-//              latency); K is split in whole groups
-//   warps 0-7  unpack: warps 0-3 write the first 64-value slab of rows
-//              0..127, warps 4-7 the second, into the MMA's A operand (fp16,
-//              128-byte swizzle, K-major: a warp's stores are conflict-free)
-//   warp 13    TMEM allocation (2 x BN columns: two accumulators); one lane
-//              issues tcgen05.mma (M=128, N=BN, K=16), 8 per stage
+//              the tile's packed bytes arrive in groups of 4 block columns (128
+//              rows x 128 contiguous bytes, 128-byte swizzle, so that 8
+//              consecutive rows read their columns from 8 different bank
+//              groups) into a ring of 8 slots (128 KB in flight per SM keeps
+//              the HBM stream busy); K is split in whole groups
+//   warps 0-7  unpack: warp w holds weight rows 32 (w % 4) .. + 31 (the TMEM
+//              lanes it may write) and half w / 4 of each block's bytes, and
+//              turns them into the MMA's A operand directly in tensor memory
+//              (fp16 pairs, one tcgen05.st of 32 columns per thread and stage):
+//              the weights never pass through shared memory as fp16, which is
+//              16x the bytes of their packed form
+//   warp 13    TMEM allocation (all 512 columns: two accumulators and four A
+//              stages of 64 columns); one lane issues tcgen05.mma (M=128,
+//              N=BN, K=16, A from TMEM), 8 per stage
 //   warps 8-11 epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 weight rows;
 //              each thread owns one weight row, so for every token the warp
 //              writes (or atomically adds) 32 consecutive outputs
+// The eight MMAs of a stage take the block's K values in the order (slot s,
+// half h) = (t mod 4, t / 4), t = 0..7: A stage columns 32 h + 8 s .. + 7 hold
+// elements 32 s + 16 h + 0..15 (so each unpack thread writes 32 consecutive
+// columns), and the token operand of step t starts at element 32 s + 16 h.
 // Every wait is bounded; an expired wait sets the device error word and the CTA
 // unwinds without trapping.
 #include "common.cuh"
@@ -50,29 +57,31 @@ namespace {
 constexpr int kSkThreads = 448;
 constexpr int kSkUnpackWarps = 8;
 constexpr int kSkBM = 128;  // weight rows per tile (MMA M)
+constexpr int kSkAStages = 4;      // A operand stages in TMEM
+constexpr int kSkAStageCols = 64;  // TMEM columns per stage: 128 K values as fp16 pairs
+constexpr int kSkTmemCols = 512;   // accumulators in columns 0 .. 2 BN - 1, A stages from kSkACol0
+constexpr int kSkACol0 = 256;
 
 constexpr int kSkPkGroup = 4;  // block columns per packed-weight load: 128 bytes per row
 
 template <int BN>
 struct SkLayout {
-  static constexpr int kPkSlots = 4;
+  static constexpr int kPkSlots = 8;
   static constexpr int kPk = kSkBM * 32 * kSkPkGroup;  // packed bytes of a slot: 128 rows x 128 B
-  static constexpr int kA = 2 * kSkBM * 64 * 2;        // two 64-wide fp16 slabs of the weights
   static constexpr int kB = 2 * BN * 64 * 2;           // two 64-wide fp16 slabs of the tokens
-  static constexpr int kStages = 3;                    // unpacked weight stages
   static constexpr int kBSlots = (64 * 1024) / kB;     // token slots
-  static constexpr int offA = 0;                           // [stages][kA]
-  static constexpr int offB = offA + kStages * kA;         // [token slots][kB]
+  static constexpr int offB = 0;                           // [token slots][kB]
   static constexpr int offPk = offB + kBSlots * kB;        // [packed slots][kPk]
   static constexpr int offInv = offPk + kPkSlots * kPk;    // [BN] float: 1 / a_scale
-  static constexpr int kNumBars = 2 * kStages + 2 * kBSlots + 2 * kPkSlots + 4;
+  static constexpr int kNumBars = 2 * kSkAStages + 2 * kBSlots + 2 * kPkSlots + 4;
   static constexpr int offBar = offInv + BN * 4;
   static constexpr int offMisc = offBar + kNumBars * 8;  // tmem base, abort flag, last flag
   static constexpr int kBytes = offMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kBSlots >= 4, "token ring too shallow");
-  static_assert(kA % 1024 == 0 && kB % 1024 == 0 && kPk % 1024 == 0, "swizzled operands need 1 KB alignment");
+  static_assert(kB % 1024 == 0 && kPk % 1024 == 0, "swizzled operands need 1 KB alignment");
   static_assert(kAlloc <= 232448, "over the 227 KB of shared memory a CTA may use");
+  static_assert(2 * BN <= kSkACol0 && kSkACol0 + kSkAStages * kSkAStageCols <= kSkTmemCols, "TMEM columns");
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
@@ -114,21 +123,19 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                   float* __restrict__ y, int32_t* __restrict__ acc_out, float* __restrict__ ws,
                   int* __restrict__ tickets, unsigned* err) {
   using L = SkLayout<BN>;
-  constexpr int kSt = L::kStages;
   constexpr int kBS = L::kBSlots;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* sA = smem + L::offA;
   uint8_t* sB = smem + L::offB;
   uint8_t* sPk = smem + L::offPk;
   float* sInv = reinterpret_cast<float*>(smem + L::offInv);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
-  uint64_t* afull = bars;                 // weight slabs unpacked
-  uint64_t* aempty = bars + kSt;          // MMAs reading the weight stage done
-  uint64_t* bfull = bars + 2 * kSt;       // token slabs landed
-  uint64_t* bempty = bfull + kBS;         // MMAs reading the token slot done
-  uint64_t* pk_full = bempty + kBS;       // packed group landed
+  uint64_t* afull = bars;                  // A stage written to TMEM (and the stage's tokens landed)
+  uint64_t* aempty = bars + kSkAStages;    // MMAs reading the A stage done
+  uint64_t* bfull = bars + 2 * kSkAStages; // token slabs landed
+  uint64_t* bempty = bfull + kBS;          // MMAs reading the token slot done
+  uint64_t* pk_full = bempty + kBS;        // packed group landed
   uint64_t* pk_empty = pk_full + L::kPkSlots;
   uint64_t* acc_full = pk_empty + L::kPkSlots;
   uint64_t* acc_empty = acc_full + 2;
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int units = n_wt * S;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSt; ++i) {
+    for (int i = 0; i < kSkAStages; ++i) {
       mbar_init(&afull[i], kSkUnpackWarps);
       mbar_init(&aempty[i], 1);
     }
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     fence_barrier_init();
   }
   if (warp == 13) {
-    tmem_alloc(tmem_slot, 2 * BN);
+    tmem_alloc(tmem_slot, kSkTmemCols);
     tmem_relinquish();
   }
   if (warp == 12 && lane == 0) {
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(kSkBM, BN);
-      int s = 0, ph = 0, b = 0, bph = 0, tl = 0;
+      int s = 0, ph = 0, b = 0, tl = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
         const SkUnit w = sk_unit(u, S, nkb);
         const int a = tl & 1;
@@ -220,18 +227,18 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             break;
           }
           tc_fence_after();
+          const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kSkACol0 + s * kSkAStageCols);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * L::kA + h * (L::kA / 2)));
-            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + b * L::kB + h * (L::kB / 2)));
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (i || h || kk) ? 1u : 0u);
+          for (int t = 0; t < 8; ++t) {
+            const int sl = t & 3, hh = t >> 2;
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + b * L::kB + (sl >> 1) * (L::kB / 2))) +
+                                   static_cast<uint64_t>(2 * (2 * (sl & 1) + hh));
+            tc_mma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(8 * t), bdesc, idesc, (i || t) ? 1u : 0u);
           }
           tc_commit(&aempty[s]);
           tc_commit(&bempty[b]);
-          if (++s == kSt) { s = 0; ph ^= 1; }
-          if (++b == kBS) { b = 0; bph ^= 1; }
+          if (++s == kSkAStages) { s = 0; ph ^= 1; }
+          if (++b == kBS) b = 0;
         }
         if (!ok) break;
         tc_commit(&acc_full[a]);
@@ -239,30 +246,31 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
   } else if (warp < kSkUnpackWarps) {
     // --------------------------------------------------------------- unpack
-    const int row = threadIdx.x & 127;  // weight row of the tile
-    const int hf = threadIdx.x >> 7;    // 64-value slab
-    uint8_t* const arow = sA + hf * (L::kA / 2) + (row >> 3) * 1024 + (row & 7) * 128;
+    const int q = warp & 3;             // TMEM lane quadrant: weight rows 32q .. 32q + 31
+    const int hf = warp >> 2;           // half of each block's 32 bytes
+    const int row = 32 * q + lane;      // weight row of the tile
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                        static_cast<uint32_t>(kSkACol0 + 32 * hf);
     int s = 0, ph = 0, p = 0, pph = 0, b = 0, bph = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const SkUnit w = sk_unit(u, S, nkb);
       for (int i = 0; i < w.len(); ++i) {
         const int gi = i % kSkPkGroup;  // column within the packed group (groups stay whole)
         if (gi == 0 && !mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
-        // the MMAs of the stage's previous use must have read its A slab
+        // chunk 2 gi + hf of the row (stored at chunk c ^ (row & 7))
+        const uint4 u4 = *reinterpret_cast<const uint4*>(sPk + p * L::kPk + row * 128 +
+                                                           (((2 * gi + hf) ^ (row & 7)) << 4));
+        uint32_t cols[32];
+        unpack_half_block_cols(u4, cols);
+        // the MMAs of the A stage's previous use must be done with it
         if (!mbar_wait(&aempty[s], ph ^ 1, err, abort_flag)) goto unpack_done;
-        uint32_t wd[8];
-        {
-          // 16-byte chunks 2 gi, 2 gi + 1 of the row, stored at chunk c ^ (row & 7)
-          const uint8_t* prow = sPk + p * L::kPk + row * 128;
-          const uint4 lo4 = *reinterpret_cast<const uint4*>(prow + (((2 * gi) ^ (row & 7)) << 4));
-          const uint4 hi4 = *reinterpret_cast<const uint4*>(prow + (((2 * gi + 1) ^ (row & 7)) << 4));
-          wd[0] = lo4.x; wd[1] = lo4.y; wd[2] = lo4.z; wd[3] = lo4.w;
-          wd[4] = hi4.x; wd[5] = hi4.y; wd[6] = hi4.z; wd[7] = hi4.w;
-        }
-        unpack_row_slab<8>(wd, hf, 0, arow + s * L::kA, row & 7);
-        // orders this thread's shared-memory accesses (the packed reads, the
-        // slab writes) before later async-proxy accesses: the MMA reading the
-        // slab, the next TMA overwriting the packed group
+        tc_fence_after();
+        __syncwarp();
+        tmem_st_32x32b_x32(tq + static_cast<uint32_t>(s * kSkAStageCols), cols);
+        tmem_st_wait();
+        tc_fence_before();
+        // the packed bytes are consumed: order the reads before the next TMA
+        // into the slot
         fence_proxy_async_smem();
         // afull also tells the MMA thread that the stage's token slabs have
         // landed: it then waits on one barrier per stage instead of two
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (gi == kSkPkGroup - 1 || i == w.len() - 1) {
           if (++p == L::kPkSlots) { p = 0; pph ^= 1; }
         }
-        if (++s == kSt) { s = 0; ph ^= 1; }
+        if (++s == kSkAStages) { s = 0; ph ^= 1; }
       }
     }
   unpack_done:;
@@ -292,7 +300,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       const int a = tl & 1;
       const int n = w.wt * kSkBM + q * 32 + lane;  // this thread's weight row
       const bool n_ok = n < N;
-      if (!mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
+      if (!mbar_wait_idle(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BN);
       // 16 tokens at a time: y (one split) or the partial sum (several splits;
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   __syncthreads();
   if (warp == 13) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * BN);
+    tmem_dealloc(tmem_base, kSkTmemCols);
   }
 }
 

@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with split K the four epilogue warps meet at named barriers for every
       // unit, so they leave the loop together: a failed wait only skips the
       // unit's work and the abort flag is read after the unit's last barrier
-      const bool got = mbar_wait(&acc_full[a], (tl >> 1) & 1, err, abort_flag);
+      const bool got = mbar_wait_idle(&acc_full[a], (tl >> 1) & 1, err, abort_flag);
       if (!got && S == 1) break;
       if (got) tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * BW);
