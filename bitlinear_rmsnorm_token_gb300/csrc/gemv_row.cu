@@ -31,9 +31,10 @@
 //    returns, so this holds whatever earlier work on the stream writes); the
 //    copies themselves are issued once this CTA's share of x is loaded: issued
 //    earlier, they queue the prologue's loads of x (L2 hits) behind the weight
-//    misses (measured: ~1.6 us later prologue at K = 16384).  Deeper L2
-//    prefetching measured slower.  The ring then covers the rest of the
-//    prologue: the stream runs while the row is normalised.
+//    misses (measured: ~1.6 us later prologue at K = 16384).  With the copies,
+//    the next two stages are prefetched into the L2, so that the HBM stream
+//    keeps going through the rest of the prologue (K = N = 16384: 14.8 ->
+//    13.6 us; deeper prefetching, or prefetching before x, measured slower).
 #include "common.cuh"
 #include "internal.h"
 #include "rowquant.cuh"
@@ -50,6 +51,7 @@ constexpr int kR1RowsPerGroup = 4;               // rows of a stage per row grou
 constexpr int kR1MaxRows = kR1StageBytes / 1024;  // rows per stage at K = 4096
 constexpr int kR1MaxParts = 4;                    // consumer warps per row at K = 16384
 constexpr int kR1MaxGroups = 8;                   // float4 groups of x per thread: 16384 / 4 / 512
+constexpr int kR1PrefetchAhead = 2;               // stages past the ring prefetched into L2 once x is in
 
 struct Row1Params {
   const float* x;
@@ -178,8 +180,12 @@ __global__ void __launch_bounds__(kR1Block, 1) k_gemv_row1(const __grid_constant
   key = warp_max_int(key);
   if (lane == 0 && !streamer) tail->red_key[warp] = key;
   __syncthreads();
-  if (streamer && lane == 0)
+  if (streamer && lane == 0) {
     for (int st = 0; st < first; ++st) issue(st);
+    // the HBM stream keeps going through the rest of the prologue
+    for (int st = first; st < min(nst, first + kR1PrefetchAhead); ++st)
+      bulk_prefetch_l2(wsrc + static_cast<int64_t>(st) * kR1StageBytes, static_cast<unsigned>(stage_len(st)));
+  }
   key = warp_max_int(lane < kR1Warps ? tail->red_key[lane] : 0);
   {
     const float scale = sq_scale(key);
