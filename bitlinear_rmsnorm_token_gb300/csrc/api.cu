@@ -342,7 +342,8 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
   float* as = reinterpret_cast<float*>(ws + code_bytes);
   uint8_t* gws = ws + code_bytes + scale_bytes;
   float* h = h_bytes ? reinterpret_cast<float*>(ws + code_bytes + scale_bytes + gws_bytes) : nullptr;
-  cudaError_t e = gws_bytes ? cudaMemsetAsync(gws, 0, gws_bytes, s) : cudaSuccess;
+  const size_t zero_bytes = skinny ? gemm_skinny_zeroed_bytes(ctx, M, K, N) : gws_bytes;
+  cudaError_t e = zero_bytes ? cudaMemsetAsync(gws, 0, zero_bytes, s) : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_norm_any(x, up, act, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, h, true, s);
   int st = BITNET_OK;
@@ -417,7 +418,8 @@ int forward_typed(const void* x, int x_dtype, const void* norm_w, int g_dtype, c
       if (st != BITNET_OK) e = cudaErrorUnknown;
     }
   } else {
-    if (e == cudaSuccess && gws_bytes) e = cudaMemsetAsync(gws, 0, gws_bytes, s);
+    const size_t zero_bytes = skinny ? gemm_skinny_zeroed_bytes(ctx, M, K, N) : gws_bytes;
+    if (e == cudaSuccess && zero_bytes) e = cudaMemsetAsync(gws, 0, zero_bytes, s);
     if (e == cudaSuccess)
       e = launch_rmsnorm_quant_f16_in(x, x_dtype, g, M, static_cast<int>(K), eps, f16, as, true, s);
     if (e == cudaSuccess)

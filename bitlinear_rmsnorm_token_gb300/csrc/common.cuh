@@ -155,13 +155,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* m
       : "memory");
 }
 
-// 3-D tiled tensor copy global -> shared (TMA); x innermost.
-__device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* map, int x, int y, int z,
+// 4-D tiled tensor copy global -> shared (TMA); x innermost.
+__device__ __forceinline__ void tma_load_4d(void* dst_smem, const CUtensorMap* map, int x, int y, int z, int w,
                                             uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_u32(dst_smem)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(smem_u32(dst_smem)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -232,14 +232,15 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 operands, fp32 accumulate.  A (M = 128
-// rows) sits in TMEM with row i in lane i and fp16 K pair (2c, 2c + 1) in
-// column c (low half = element 2c).
-__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T with 8-bit operands (kind::f8f6f4; the
+// types are in the instruction descriptor), fp32 accumulate, K = 32 per
+// instruction: A's TMEM column c holds K elements 4c .. 4c + 3 (lowest byte
+// first), row i in lane i.
+__device__ __forceinline__ void tc_mma_f8_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -330,6 +331,10 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
          | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A/B (format code 0 in the
+// A and B fields), fp32 D, both K-major: the same bits as idesc_f16_f32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) { return idesc_f16_f32(m, n); }
 
 // --------------------------------------------------------------- integer math
 // dp4a with unsigned bytes in a and signed bytes in b.

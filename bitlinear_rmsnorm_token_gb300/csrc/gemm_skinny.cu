@@ -1,5 +1,6 @@
-// gemm_skinny.cu -- BitLinear contraction for a few tens of tokens (9..64) on
-// the 5th-generation tensor cores, with the K dimension split across CTAs.
+// gemm_skinny.cu -- BitLinear contraction for a few tens of tokens (9..63) on
+// the 5th-generation tensor cores with 8-bit operands, the K dimension split
+// across CTAs where that pays.
 //
 // acc[m, n] = sum_k q[m, k] * (code(n, k) - 1) (int8 activations x ternary
 // weights, the product of ggml_vec_dot_i2_i8_s named in section 6.4 of "BitNet
@@ -7,105 +8,110 @@
 // w_scale in fp32 ("BitNet Inference Framework", "Quantization (W1.58A8)").
 //
 // With few tokens the weight stream is the cost, so the weights are the MMA's
-// M side (128 rows per tile) and the tokens its N side (BN = 16, 32 or 64
-// columns, all tokens in one tile): the MMA work is proportional to the real
-// token count.  A weight matrix has only N/128 tiles, so the K dimension of
-// each tile is split into S ranges of whole I2_S blocks; (tile, range) units
-// are spread over one persistent CTA per SM.
+// M side (128 rows per tile) and the tokens its N side (all tokens in one
+// tile): the MMA work is proportional to the real token count.  A weight
+// matrix has only N/128 tiles, so the K dimension of each tile may be split
+// into S ranges of whole I2_S blocks; (tile, range) units are spread over one
+// persistent CTA per SM.
 //
-// Exactness: operands are integers exact in fp16, every partial sum is an
-// integer of magnitude <= 127 * K < 2^24, so the fp32 TMEM accumulator and the
-// fp32 atomic additions that combine the S partial sums of a tile are exact,
-// whatever their order.  The split that completes a tile (a per-tile ticket)
-// rescales it: y = ((float)acc * (1/a_scale)) * (1/w_scale).
+// Operands (tcgen05 kind::f8f6f4, e4m3 x e4m3, fp32 accumulation):
+//   weights: the 2-bit code c in {0, 1, 2} itself as an e4m3 byte, the
+//     subnormal c * 2^-9 (a shift and an AND per four weights);
+//   tokens: each int8 code written as q = 16 hi + lo with hi = floor(q / 16)
+//     in [-8, 7] and lo = q mod 16 in [0, 15], both exact e4m3 integers, in
+//     two operand rows per token (row 2t: hi, row 2t + 1: lo).
+// A token's two accumulator columns then hold D_hi = 2^-9 sum c hi and D_lo =
+// 2^-9 sum c lo: multiples of 2^-9 below 2^12 in magnitude (K <= 65536), held
+// exactly by the fp32 accumulator whatever the order of the additions
+// (checked on GB300 with e4m3 subnormal operands and sums to 2^21 units), and
+//     acc = 512 (16 D_hi + D_lo) - sum_k q[m, k]
+// in exact integer arithmetic, the last term (the row sum of the codes)
+// removing the +1 offset of the weight codes.  Partial sums of split tiles are
+// integers below 2^24, combined with exact fp32 atomic additions.
+//
+// k_token_planes rewrites the tokens' fp16 codes in place: each 128-value
+// block of a row (256 bytes as fp16) becomes its 128 hi bytes then its 128 lo
+// bytes, and sums of the codes per 2048-value chunk go to a small array.
 //
 // One stage = one I2_S block column (128 values of K) of the tile:
-//   warp 20    TMA producer: the tokens' fp16 codes of TG consecutive stages
-//              (2 TG 64-wide slabs of BN rows, 128-byte swizzle) in one copy, a
-//              3-D view of the [M, K] codes (64 values, token, 64-value slab),
-//              into a 96 KB ring of their own: a TMA copy has a fixed cost of
-//              its own (measured on sm_103a: 2 KB boxes of 16 rows from L2
-//              arrive at ~25 GB/s per SM, 16 KB boxes at ~94), which with one
-//              copy per 2 KB slab set the stage rate; the tile's packed bytes
-//              arrive in groups of 4 block columns (128 rows x 128 contiguous
-//              bytes, 128-byte swizzle, so that 8 consecutive rows read their
-//              columns from 8 different bank groups) into a ring of 6 slots
-//              (96 KB in flight per SM keeps the HBM stream busy); K is split
-//              in whole groups
-//   two stage pipelines, j = 0, 1, take the stages of even and odd running
-//   index (over the CTA's units) in turn, each with
-//     8 unpack warps (warps 8j .. 8j+7): warp w holds weight rows 32 (w % 4)
-//              .. + 31 (the TMEM lanes it may write) and half (w % 8) / 4 of
-//              each block's bytes, and turns them into the MMA's A operand
-//              directly in tensor memory (fp16 pairs, one tcgen05.st of 32
-//              columns per thread and stage): the weights never pass through
-//              shared memory as fp16, which is 16x the bytes of their packed
-//              form
-//     1 MMA warp (warp 21 + j): one lane issues tcgen05.mma (M=128, N=BN,
-//              K=16, A from TMEM), 8 per stage, into the pipeline's own
-//              accumulator, from its own two A stages of 64 TMEM columns
-//   A stage is a chain of dependent steps (shared-memory load, unpack, wait
-//   for a free A stage, tensor-memory store and its wait, fences, arrival,
-//   the MMA thread's wait, MMAs, commit) that leaves the SM's pipes mostly
-//   idle (measured on sm_103a: ~1200 cycles per stage for one pipeline, ALU
-//   pipe 39% busy); two pipelines overlap two such chains.  Warp 21 also
-//   allocates all 512 TMEM columns (4 accumulators, then the A stages).
-//   warps 16-19 epilogue: warp q reads TMEM lanes 32q..32q+31 = 32 weight rows
-//              of both pipelines' accumulators and adds them (integers below
-//              2^24: exact); each thread owns one weight row, so for every
-//              token the warp writes (or atomically adds) 32 consecutive
-//              outputs
-// The eight MMAs of a stage take the block's K values in the order (slot s,
-// half h) = (t mod 4, t / 4), t = 0..7: A stage columns 32 h + 8 s .. + 7 hold
-// elements 32 s + 16 h + 0..15 (so each unpack thread writes 32 consecutive
-// columns), and the token operand of step t starts at element 32 s + 16 h.
+//   producer warp: the token planes of TG consecutive stages in one 4-D TMA
+//              copy (128 bytes, plane, token, block) into a 96 KB ring (a TMA
+//              copy has a fixed cost: measured on sm_103a, 2 KB boxes from L2
+//              arrive at ~25 GB/s per SM, 16 KB boxes at ~94); the tile's
+//              packed bytes in groups of 4 block columns (128 rows x 128
+//              contiguous bytes, 128-byte swizzle: 8 consecutive rows read 8
+//              different bank groups) into a ring of 6 slots (96 KB in flight
+//              per SM keeps the HBM stream busy); K is split in whole groups
+//   P stage pipelines (4, or 2 for 64-token tiles) take the stages of running
+//   index j mod P (over the CTA's units), each with
+//     4 unpack warps: warp q holds weight rows 32q .. 32q + 31 (the TMEM lanes
+//              it may write); each thread turns its row's 32 packed bytes into
+//              the 32 TMEM columns of the A stage (column 8 s + c: the four
+//              weights of slot s in bytes 4c .. 4c + 3, elements 32 s + 4c ..
+//              + 3) with one tcgen05.st
+//     1 MMA warp: one lane issues the stage's 4 MMAs (M = 128, N = 2 x token
+//              tile, K = 32, A from TMEM; MMA s covers slot s) into the
+//              pipeline's own accumulator
+//   A stage is a chain of dependent steps (loads, unpack, tensor-memory store,
+//   fences, barrier hand-offs, MMAs, commit) that leaves the SM's pipes idle
+//   most of the time (one pipeline: ~1200 cycles per stage measured on
+//   sm_103a), so several pipelines overlap their chains.
+//   4 epilogue warps: warp q reads TMEM lanes 32q..32q+31 = 32 weight rows of
+//              every pipeline's accumulator and adds them (exact integers);
+//              each thread owns one weight row, so for every token the warp
+//              writes (or atomically adds) 32 consecutive outputs
 // Every wait is bounded; an expired wait sets the device error word and the CTA
 // unwinds without trapping.
 #include "common.cuh"
 #include "internal.h"
 #include "rowquant.cuh"
-#include "unpack_f16.cuh"
+
+#include <cuda_fp8.h>
 
 namespace bitnet {
 namespace {
 
-constexpr int kSkPipes = 2;                                  // stage pipelines (running stage index mod 2)
-constexpr int kSkPipeWarps = 8;                              // unpack warps per pipeline
-constexpr int kSkUnpackWarps = kSkPipes * kSkPipeWarps;      // warps 0 .. 15
-constexpr int kSkEpiWarp0 = kSkUnpackWarps;                  // warps 16 .. 19
-constexpr int kSkProducerWarp = kSkEpiWarp0 + 4;             // warp 20
-constexpr int kSkMmaWarp0 = kSkProducerWarp + 1;             // warps 21, 22
-constexpr int kSkThreads = (kSkMmaWarp0 + kSkPipes) * 32;
-constexpr int kSkBM = 128;  // weight rows per tile (MMA M)
-constexpr int kSkAPerPipe = 2;                    // A operand stages in TMEM per pipeline
-constexpr int kSkAStages = kSkPipes * kSkAPerPipe;
-constexpr int kSkAStageCols = 64;  // TMEM columns per stage: 128 K values as fp16 pairs
-constexpr int kSkTmemCols = 512;   // accumulator of buffer a, pipeline j at columns (2 a + j) BN; A stages from kSkACol0
-constexpr int kSkACol0 = 256;
+constexpr int kSkBM = 128;         // weight rows per tile (MMA M)
+constexpr int kSkAStageCols = 32;  // TMEM columns per A stage: 128 K values of one byte
+constexpr int kSkTmemCols = 512;
+constexpr int kSkPkGroup = 4;      // block columns per packed-weight load: 128 bytes per row
 
-constexpr int kSkPkGroup = 4;  // block columns per packed-weight load: 128 bytes per row
-
+// BN: token tile (16, 32 or 64 tokens); the MMA's N is 2 BN (two planes).
 template <int BN>
 struct SkLayout {
+  static constexpr int kN2 = 2 * BN;                     // MMA N
+  static constexpr int kPipes = BN == 64 ? 2 : 4;
+  static constexpr int kUnpackWarps = 4 * kPipes;        // warps 0 .. 4P - 1
+  static constexpr int kEpiWarp0 = kUnpackWarps;         // 4 warps
+  static constexpr int kProducerWarp = kEpiWarp0 + 4;
+  static constexpr int kMmaWarp0 = kProducerWarp + 1;    // P warps
+  static constexpr int kThreads = (kMmaWarp0 + kPipes) * 32;
+  // TMEM: accumulator of buffer a, pipeline j at columns (a P + j) 2 BN, then
+  // the A stages
+  static constexpr int kAccBufs = 2 * kPipes * kN2 <= 256 ? 2 : 1;
+  static constexpr int kACol0 = kAccBufs * kPipes * kN2;
+  static constexpr int kAStages = (kSkTmemCols - kACol0) / kSkAStageCols;
+  static constexpr int kAPerPipe = kAStages / kPipes;
   static constexpr int kPkSlots = 6;
   static constexpr int kPk = kSkBM * 32 * kSkPkGroup;  // packed bytes of a slot: 128 rows x 128 B
-  static constexpr int kB = 2 * BN * 64 * 2;           // a stage's two 64-wide fp16 slabs of the tokens
+  static constexpr int kB = kN2 * 128;                 // a stage's token rows (2 per token) of 128 B
   static constexpr int kTG = BN == 64 ? 2 : 4;         // stages per token copy (a divisor of kSkPkGroup)
   static constexpr int kTSlot = kTG * kB;              // bytes of a token slot
   static constexpr int kTSlots = (96 * 1024) / kTSlot; // token slots
   static constexpr int offB = 0;                           // [token slots][kTG stages][kB]
   static constexpr int offPk = offB + kTSlots * kTSlot;    // [packed slots][kPk]
   static constexpr int offInv = offPk + kPkSlots * kPk;    // [BN] float: 1 / a_scale
-  static constexpr int kNumBars = 2 * kSkAStages + 2 * kTSlots + 2 * kPkSlots + 4;
-  static constexpr int offBar = offInv + BN * 4;
+  static constexpr int offRs = offInv + BN * 4;            // [BN] int: row sums of the codes
+  static constexpr int kNumBars = 2 * kAStages + 2 * kTSlots + 2 * kPkSlots + 2 * kAccBufs;
+  static constexpr int offBar = offRs + BN * 4;
   static constexpr int offMisc = offBar + kNumBars * 8;  // tmem base, abort flag, last flag
   static constexpr int kBytes = offMisc + 32;
   static constexpr int kAlloc = kBytes + 1024;
   static_assert(kTSlots >= 3 && kSkPkGroup % kTG == 0, "token ring too shallow");
   static_assert(kB % 1024 == 0 && kPk % 1024 == 0, "swizzled operands need 1 KB alignment");
   static_assert(kAlloc <= 232448, "over the 227 KB of shared memory a CTA may use");
-  static_assert(2 * kSkPipes * BN <= kSkACol0 && kSkACol0 + kSkAStages * kSkAStageCols <= kSkTmemCols,
-                "TMEM columns");
+  static_assert(kAPerPipe >= 2 && kACol0 + kAStages * kSkAStageCols <= kSkTmemCols, "TMEM columns");
+  static_assert(kThreads <= 1024, "block size");
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
@@ -113,6 +119,61 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
+
+__device__ __forceinline__ uint32_t e4m3_byte(int v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(static_cast<float>(v), __NV_SATFINITE, __NV_E4M3));
+}
+
+// One CTA per (token row, 2048-value chunk): the chunk's fp16 codes rewritten
+// in place as the two e4m3 planes, block by block (a warp reads its two
+// 256-byte blocks, both loads in flight, before writing them back), and the
+// chunk's code sum in rowsum_part[m][chunk] (the epilogue adds a row's
+// partials: integers, order-free).
+constexpr int kPlaneThreads = 256;
+constexpr int kPlaneChunk = 2048;  // values per CTA: 8 warps x 2 blocks of 128
+__global__ void __launch_bounds__(kPlaneThreads) k_token_planes(__half* codes, int K, int* __restrict__ rowsum_part) {
+  __shared__ int red[kPlaneThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* row = reinterpret_cast<uint8_t*>(codes) + static_cast<int64_t>(blockIdx.y) * K * 2;
+  const int nkb = K >> 7;
+  const int kb0 = blockIdx.x * (kPlaneChunk / 128) + 2 * warp;
+  uint2 v[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    v[h] = kb0 + h < nkb ? *reinterpret_cast<const uint2*>(row + (kb0 + h) * 256 + lane * 8) : make_uint2(0u, 0u);
+  __syncwarp();  // both blocks are read before any lane writes into them
+  int sum = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (kb0 + h >= nkb) break;
+    const __half2 h01 = *reinterpret_cast<const __half2*>(&v[h].x);
+    const __half2 h23 = *reinterpret_cast<const __half2*>(&v[h].y);
+    const int q[4] = {static_cast<int>(__low2float(h01)), static_cast<int>(__high2float(h01)),
+                      static_cast<int>(__low2float(h23)), static_cast<int>(__high2float(h23))};
+    uint32_t hi = 0, lo = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int l = q[i] & 15;
+      lo |= e4m3_byte(l) << (8 * i);
+      hi |= e4m3_byte((q[i] - l) / 16) << (8 * i);
+      sum += q[i];
+    }
+    uint8_t* blk = row + (kb0 + h) * 256;
+    *reinterpret_cast<uint32_t*>(blk + lane * 4) = hi;
+    *reinterpret_cast<uint32_t*>(blk + 128 + lane * 4) = lo;
+  }
+  sum = warp_sum_int(sum);
+  if (lane == 0) red[warp] = sum;
+  __syncthreads();
+  if (warp == 0) {
+    sum = warp_sum_int(lane < kPlaneThreads / 32 ? red[lane] : 0);
+    if (lane == 0) rowsum_part[blockIdx.y * gridDim.x + blockIdx.x] = sum;
+  }
+}
+
+__host__ __device__ constexpr int plane_chunks(int K) { return (K + kPlaneChunk - 1) / kPlaneChunk; }
 
 // Unit u = (weight tile, K range): the tile's I2_S blocks [kb0, kb1), whole
 // groups of kSkPkGroup blocks (the last one cut at K).  The i-th block a unit
@@ -141,29 +202,32 @@ __device__ __forceinline__ SkUnit sk_unit(int u, int S, int nkb) {
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kSkThreads, 1)
+__global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
-                  const float* __restrict__ a_scale, float inv_w, int M, int N, int K, int S,
-                  float* __restrict__ y, int32_t* __restrict__ acc_out, float* __restrict__ ws,
+                  const float* __restrict__ a_scale, const int* __restrict__ rowsum_part, float inv_w, int M, int N,
+                  int K, int S, float* __restrict__ y, int32_t* __restrict__ acc_out, float* __restrict__ ws,
                   int* __restrict__ tickets, unsigned* err) {
   using L = SkLayout<BN>;
+  constexpr int kP = L::kPipes;
   constexpr int kTS = L::kTSlots;
   constexpr int kTG = L::kTG;
+  constexpr int kAS = L::kAStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* sB = smem + L::offB;
   uint8_t* sPk = smem + L::offPk;
   float* sInv = reinterpret_cast<float*>(smem + L::offInv);
+  int* sRs = reinterpret_cast<int*>(smem + L::offRs);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
   uint64_t* afull = bars;                  // A stage written to TMEM (and the stage's tokens landed)
-  uint64_t* aempty = bars + kSkAStages;    // MMAs reading the A stage done
-  uint64_t* tfull = bars + 2 * kSkAStages; // token slabs of a slot landed
+  uint64_t* aempty = bars + kAS;           // MMAs reading the A stage done
+  uint64_t* tfull = bars + 2 * kAS;        // token planes of a slot landed
   uint64_t* tempty = tfull + kTS;          // MMAs of every stage of the token slot done
   uint64_t* pk_full = tempty + kTS;        // packed group landed
   uint64_t* pk_empty = pk_full + L::kPkSlots;
-  uint64_t* acc_full = pk_empty + L::kPkSlots;
-  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* acc_full = pk_empty + L::kPkSlots;  // every pipeline done with the unit
+  uint64_t* acc_empty = acc_full + L::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 8);
@@ -175,8 +239,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int units = n_wt * S;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSkAStages; ++i) {
-      mbar_init(&afull[i], kSkPipeWarps);
+    for (int i = 0; i < kAS; ++i) {
+      mbar_init(&afull[i], 4);
       mbar_init(&aempty[i], 1);
     }
     for (int i = 0; i < kTS; ++i) {
@@ -185,20 +249,20 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     }
     for (int i = 0; i < L::kPkSlots; ++i) {
       mbar_init(&pk_full[i], 1);
-      mbar_init(&pk_empty[i], kSkUnpackWarps);
+      mbar_init(&pk_empty[i], L::kUnpackWarps);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], kSkPipes);
+    for (int i = 0; i < L::kAccBufs; ++i) {
+      mbar_init(&acc_full[i], kP);
       mbar_init(&acc_empty[i], 4);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kSkMmaWarp0) {
+  if (warp == L::kMmaWarp0) {
     tmem_alloc(tmem_slot, kSkTmemCols);
     tmem_relinquish();
   }
-  if (warp == kSkProducerWarp && lane == 0) {
+  if (warp == L::kProducerWarp && lane == 0) {
     prefetch_tensormap(&tm_tok);
     prefetch_tensormap(&tm_w);
   }
@@ -207,15 +271,17 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // everything below reads what the previous kernel on the stream produced
+  // everything below reads what the previous kernels on the stream produced
   pdl_wait();
 
-  if (warp == kSkProducerWarp) {
+  if (warp == L::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int s = 0, ph = 0, p = 0, pph = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const SkUnit w = sk_unit(u, S, nkb);
+        // the stages of a packed group (and of a token slot) have consecutive
+        // block columns: rotations are whole groups
         for (int i = 0; i < w.len(); ++i) {
           const int kb = w.kb(i);
           if (i % kSkPkGroup == 0) {
@@ -226,52 +292,49 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (++p == L::kPkSlots) { p = 0; pph ^= 1; }
           }
           if (i % kTG == 0) {
-            // slabs 2 kb .. 2 (kb + kTG) - 1: the stages of a token slot have
-            // consecutive block columns (rotations are whole packed groups);
-            // slabs past K read as 0
+            // blocks kb .. kb + kTG - 1 of every token's two planes (tokens >=
+            // M and blocks past K read as 0)
             if (!mbar_wait(&tempty[s], ph ^ 1, err, abort_flag)) goto producer_done;
             mbar_arrive_expect_tx(&tfull[s], static_cast<unsigned>(L::kTSlot));
-            tma_load_3d(sB + s * L::kTSlot, &tm_tok, 0, 0, 2 * kb, &tfull[s]);
+            tma_load_4d(sB + s * L::kTSlot, &tm_tok, 0, 0, 0, kb, &tfull[s]);
             if (++s == kTS) { s = 0; ph ^= 1; }
           }
         }
       }
     producer_done:;
     }
-  } else if (warp >= kSkMmaWarp0) {
+  } else if (warp >= L::kMmaWarp0) {
     // -------------------------------------------------------- MMA issuers
-    // pipeline j issues the stages of running index g = j mod 2; it walks
+    // pipeline j issues the stages of running index g = j mod P; it walks
     // every stage to keep its place in the token ring
     if (lane == 0) {
-      const int j = warp - kSkMmaWarp0;
-      constexpr uint32_t idesc = idesc_f16_f32(kSkBM, BN);
+      const int j = warp - L::kMmaWarp0;
+      constexpr uint32_t idesc = idesc_e4m3_f32(kSkBM, L::kN2);
       int n = 0, b = 0, g = 0, tl = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
         const SkUnit w = sk_unit(u, S, nkb);
-        const int a = tl & 1;
+        const int a = L::kAccBufs == 2 ? (tl & 1) : 0;
+        const int use = L::kAccBufs == 2 ? (tl >> 1) : tl;  // earlier uses of buffer a
         // also keeps a pipeline without stages in this unit from arriving on
         // acc_full ahead of the epilogue
-        if (!mbar_wait(&acc_empty[a], ((tl >> 1) & 1) ^ 1, err, abort_flag)) break;
+        if (!mbar_wait(&acc_empty[a], (use & 1) ^ 1, err, abort_flag)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((kSkPipes * a + j) * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((kP * a + j) * L::kN2);
         bool ok = true, any = false;
         for (int i = 0; i < w.len(); ++i, ++g) {
-          if ((g & 1) == j) {
-            const int s = kSkAPerPipe * j + n % kSkAPerPipe;
-            if (!mbar_wait(&afull[s], (n / kSkAPerPipe) & 1, err, abort_flag)) {  // also covers the token slot
+          if (g % kP == j) {
+            const int s = L::kAPerPipe * j + n % L::kAPerPipe;
+            if (!mbar_wait(&afull[s], (n / L::kAPerPipe) & 1, err, abort_flag)) {  // also covers the tokens
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kSkACol0 + s * kSkAStageCols);
-            const uint8_t* btok = sB + b * L::kTSlot + (i % kTG) * L::kB;
+            const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(L::kACol0 + s * kSkAStageCols);
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + b * L::kTSlot + (i % kTG) * L::kB));
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int sl = t & 3, hh = t >> 2;
-              const uint64_t bdesc = sw128_kmajor_desc(smem_u32(btok + (sl >> 1) * (L::kB / 2))) +
-                                     static_cast<uint64_t>(2 * (2 * (sl & 1) + hh));
-              tc_mma_f16_ta(d_tmem, a_tmem + static_cast<uint32_t>(8 * t), bdesc, idesc, (any || t) ? 1u : 0u);
-            }
+            for (int t = 0; t < 4; ++t)
+              tc_mma_f8_ta(d_tmem, a_tmem + static_cast<uint32_t>(8 * t), bdesc + static_cast<uint64_t>(2 * t),
+                           idesc, (any || t) ? 1u : 0u);
             any = true;
             tc_commit(&aempty[s]);
             tc_commit(&tempty[b]);
@@ -290,31 +353,35 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         else mbar_arrive(&acc_full[a]);
       }
     }
-  } else if (warp < kSkUnpackWarps) {
+  } else if (warp < L::kUnpackWarps) {
     // --------------------------------------------------------------- unpack
-    const int pj = warp / kSkPipeWarps;  // pipeline: stages of running index pj mod 2
+    const int pj = warp >> 2;            // pipeline: stages of running index pj mod P
     const int q = warp & 3;              // TMEM lane quadrant: weight rows 32q .. 32q + 31
-    const int hf = (warp & 7) >> 2;      // half of each block's 32 bytes
     const int row = 32 * q + lane;       // weight row of the tile
-    const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                        static_cast<uint32_t>(kSkACol0 + 32 * hf);
+    const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(L::kACol0);
     int n = 0, p = 0, pph = 0, b = 0, bph = 0, g = 0;
     bool pk_ready = false;  // the current packed group has been waited for
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const SkUnit w = sk_unit(u, S, nkb);
       for (int i = 0; i < w.len(); ++i, ++g) {
         const int gi = i % kSkPkGroup;  // column within the packed group (groups stay whole)
-        if ((g & 1) == pj) {
+        if (g % kP == pj) {
           if (!pk_ready && !mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
           pk_ready = true;
-          // chunk 2 gi + hf of the row (stored at chunk c ^ (row & 7))
-          const uint4 u4 = *reinterpret_cast<const uint4*>(sPk + p * L::kPk + row * 128 +
-                                                             (((2 * gi + hf) ^ (row & 7)) << 4));
+          // the row's 32 bytes of block column gi: chunks 2 gi, 2 gi + 1,
+          // stored at chunk c ^ (row & 7)
+          const uint8_t* src = sPk + p * L::kPk + row * 128;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(src + (((2 * gi) ^ (row & 7)) << 4));
+          const uint4 c1 = *reinterpret_cast<const uint4*>(src + (((2 * gi + 1) ^ (row & 7)) << 4));
+          const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           uint32_t cols[32];
-          unpack_half_block_cols(u4, cols);
-          const int s = kSkAPerPipe * pj + n % kSkAPerPipe;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) cols[8 * sl + c] = (wd[c] >> (6 - 2 * sl)) & 0x03030303u;
+          const int s = L::kAPerPipe * pj + n % L::kAPerPipe;
           // the MMAs of the A stage's previous use must be done with it
-          if (!mbar_wait(&aempty[s], ((n / kSkAPerPipe) & 1) ^ 1, err, abort_flag)) goto unpack_done;
+          if (!mbar_wait(&aempty[s], ((n / L::kAPerPipe) & 1) ^ 1, err, abort_flag)) goto unpack_done;
           tc_fence_after();
           __syncwarp();
           tmem_st_32x32b_x32(tq + static_cast<uint32_t>(s * kSkAStageCols), cols);
@@ -323,7 +390,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           // the packed bytes are consumed: order the reads before the next TMA
           // into the slot
           fence_proxy_async_smem();
-          // afull also tells the MMA thread that the stage's token slabs have
+          // afull also tells the MMA thread that the stage's token planes have
           // landed: it then waits on one barrier per stage instead of two
           if (!mbar_wait(&tfull[b], bph, err, abort_flag)) goto unpack_done;
           __syncwarp();
@@ -332,7 +399,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         if (i % kTG == kTG - 1 || i == w.len() - 1)
           if (++b == kTS) { b = 0; bph ^= 1; }
-        // every unpack warp of both pipelines releases the packed group once
+        // every unpack warp of every pipeline releases the packed group once
         // it is past the group's last stage
         if (gi == kSkPkGroup - 1 || i == w.len() - 1) {
           __syncwarp();
@@ -345,59 +412,64 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   unpack_done:;
   } else {
     // ------------------------------------------------------------- epilogue
-    const int et = threadIdx.x - kSkEpiWarp0 * 32;  // 0..127
-    const int q = warp & 3;            // TMEM lane quadrant this warp may access
-    for (int j = et; j < BN; j += 128) sInv[j] = j < M ? __frcp_rn(__ldg(a_scale + j)) : 0.0f;
+    const int et = threadIdx.x - L::kEpiWarp0 * 32;  // 0..127
+    const int q = warp & 3;                           // TMEM lane quadrant this warp may access
+    for (int t = et; t < BN; t += 128) {
+      sInv[t] = t < M ? __frcp_rn(__ldg(a_scale + t)) : 0.0f;
+      int rs = 0;
+      if (t < M)
+        for (int c = 0; c < plane_chunks(K); ++c) rs += __ldg(rowsum_part + t * plane_chunks(K) + c);
+      sRs[t] = rs;
+    }
     epi_bar();
     int tl = 0, g0 = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
       const SkUnit w = sk_unit(u, S, nkb);
-      const int a = tl & 1;
+      const int a = L::kAccBufs == 2 ? (tl & 1) : 0;
+      const int use = L::kAccBufs == 2 ? (tl >> 1) : tl;
       const int n = w.wt * kSkBM + q * 32 + lane;  // this thread's weight row
       const bool n_ok = n < N;
-      // pipelines with a stage in this unit (running indices g0 .. g0 + len - 1)
-      const bool act0 = w.len() >= 2 || (g0 & 1) == 0;
-      const bool act1 = w.len() >= 2 || (g0 & 1) == 1;
-      g0 += w.len();
-      if (!mbar_wait_idle(&acc_full[a], (tl >> 1) & 1, err, abort_flag)) break;
+      const int len = w.len(), r0 = g0 % kP;  // pipelines with a stage: those of running indices g0 ..
+      g0 += len;
+      if (!mbar_wait_idle(&acc_full[a], use & 1, err, abort_flag)) break;
       tc_fence_after();
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(kSkPipes * a * BN);
-      // 16 tokens at a time: y (one split) or the partial sum (several splits;
-      // exact fp32 atomic additions)
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(kP * a * L::kN2);
+      // 8 tokens (16 columns: hi, lo) at a time: y (one split) or the partial
+      // sum (several splits; exact fp32 atomic additions)
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN && j0 < M; j0 += 16) {
-        // the sum of the pipelines' accumulators (integers below 2^24: exact)
-        float acc[16];
+      for (int c0 = 0; c0 < L::kN2 && (c0 >> 1) < M; c0 += 16) {
+        int acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 16; ++i) acc[i] = 0;
 #pragma unroll 1
-        for (int pj = 0; pj < kSkPipes; ++pj) {
-          if (!(pj == 0 ? act0 : act1)) continue;
+        for (int pj = 0; pj < kP; ++pj) {
+          if (len < kP && (pj - r0 + kP) % kP >= len) continue;  // no stage of this unit
           uint32_t r[16];
-          tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(pj * BN + j0), r);
+          tmem_ld_32x32b_x16(tbase + static_cast<uint32_t>(pj * L::kN2 + c0), r);
           tmem_ld_wait();
           tmem_reg_fence16(r);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[i]);
+          for (int i = 0; i < 16; ++i) acc[i] += __float2int_rn(__fmul_rn(__uint_as_float(r[i]), 512.0f));
         }
         if (n_ok) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = j0 + i;
-            if (j < M) {
-              const float accf = acc[i];
+          for (int i = 0; i < 8; ++i) {
+            const int t = (c0 >> 1) + i;
+            if (t < M) {
+              const int v = 16 * acc[2 * i] + acc[2 * i + 1];  // sum c q over the unit's blocks
               if (S == 1) {
-                y[static_cast<int64_t>(j) * N + n] = rescale_elem(accf, sInv[j], inv_w);
-                if (acc_out) acc_out[static_cast<int64_t>(j) * N + n] = __float2int_rn(accf);
+                const int full = v - sRs[t];
+                y[static_cast<int64_t>(t) * N + n] = rescale_elem(static_cast<float>(full), sInv[t], inv_w);
+                if (acc_out) acc_out[static_cast<int64_t>(t) * N + n] = full;
               } else {
-                red_add_f32(ws + static_cast<int64_t>(j) * N + n, accf);
+                red_add_f32(ws + static_cast<int64_t>(t) * N + n, static_cast<float>(v));
               }
             }
           }
         }
       }
-      // the accumulator has been read: release it to the MMAs of a later unit
+      // the accumulators have been read: release them to a later unit's MMAs
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
@@ -410,10 +482,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       if (*last_flag) {
         __threadfence();
         if (n_ok) {
-          for (int j = 0; j < M && j < BN; ++j) {
-            const float accf = __ldcg(ws + static_cast<int64_t>(j) * N + n);
-            y[static_cast<int64_t>(j) * N + n] = rescale_elem(accf, sInv[j], inv_w);
-            if (acc_out) acc_out[static_cast<int64_t>(j) * N + n] = __float2int_rn(accf);
+          for (int t = 0; t < M && t < BN; ++t) {
+            // both exact integers below 2^24: the difference is exact
+            const float accf = __fsub_rn(__ldcg(ws + static_cast<int64_t>(t) * N + n), static_cast<float>(sRs[t]));
+            y[static_cast<int64_t>(t) * N + n] = rescale_elem(accf, sInv[t], inv_w);
+            if (acc_out) acc_out[static_cast<int64_t>(t) * N + n] = __float2int_rn(accf);
           }
         }
       }
@@ -423,7 +496,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kSkMmaWarp0) {
+  if (warp == L::kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kSkTmemCols);
   }
@@ -432,13 +505,13 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 // Number of K splits: the one with the least estimated time, which is the
 // busiest CTA's stages plus, with a split, the epilogues' fp32 atomic
 // additions (M N S of them, a throughput the whole GPU shares) and the per-unit
-// ticket and read-back.  Fitted to GB300 timings of this kernel with forced
-// split counts: ~0.5 us per stage, ~85 atomic additions per ns, ~1 us per
-// split unit (M = 63, K = N = 16384: 70 us unsplit, 89 / 121 / 182 us with
-// S = 2 / 4 / 8, where a count of stages alone picks 8).  Ties go to fewer
-// splits.
+// ticket and read-back.  Fitted to GB300 timings with forced split counts:
+// ~85 atomic additions per ns, ~1 us per split unit (M = 63, K = N = 16384,
+// fp16 operands: 70 us unsplit, 89 / 121 / 182 us with S = 2 / 4 / 8, where a
+// count of stages alone picks 8), and ~0.35 us per stage with 8-bit operands.
+// Ties go to fewer splits.
 int choose_splits(int64_t M, int n_wt, int nkb, int64_t N, int ctas) {
-  constexpr double kStageNs = 500.0, kAtomicsPerNs = 85.0, kSplitUnitNs = 1000.0;
+  constexpr double kStageNs = 350.0, kAtomicsPerNs = 85.0, kSplitUnitNs = 1000.0;
   const int ngrp = (nkb + kSkPkGroup - 1) / kSkPkGroup;
   int best = 1;
   double best_cost = 0.0;
@@ -459,21 +532,22 @@ int choose_splits(int64_t M, int n_wt, int nkb, int64_t N, int ctas) {
 }
 
 template <int BN>
-cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const __half* codes_f16, const float* a_scale,
-                      const uint8_t* packed_w, float inv_w, int M, int K, int N, int S, float* y, int32_t* acc_out,
-                      float* ws, int* tickets, bool pdl, cudaStream_t s, int* status) {
+cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const uint8_t* planes, const float* a_scale,
+                      const int* rowsum_part, const uint8_t* packed_w, float inv_w, int M, int K, int N, int S, float* y,
+                      int32_t* acc_out, float* ws, int* tickets, cudaStream_t s, int* status) {
   using L = SkLayout<BN>;
   CUtensorMap tm_tok, tm_w;
   {
-    // tokens: fp16 [M, K] viewed as (64 values, token, 64-value slab): boxes of
-    // 64 values x BN tokens x 2 kTG slabs, each slab a swizzled BN x 128 B
-    // block (tokens >= M and slabs past K read as 0)
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BN), static_cast<cuuint32_t>(2 * L::kTG)};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = encode(&tm_tok, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(codes_f16), dims, strides,
-                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    // token planes: bytes [M][K/128][2][128] viewed as (byte, plane, token,
+    // block); boxes of 128 bytes x 2 planes x BN tokens x TG blocks land as TG
+    // stages of 2 BN swizzled rows of 128 bytes, row 2 t + plane (tokens >= M
+    // and blocks past K read as 0)
+    cuuint64_t dims[4] = {128, 2, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 128)};
+    cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(K) * 2, 256};
+    cuuint32_t box[4] = {128, 2, static_cast<cuuint32_t>(BN), static_cast<cuuint32_t>(L::kTG)};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = encode(&tm_tok, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(planes), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       *status = BITNET_ERR_CUDA;
@@ -500,16 +574,35 @@ cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const __ha
   const int units = ((N + kSkBM - 1) / kSkBM) * S;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units < ctx->num_sms ? units : ctx->num_sms);
-  cfg.blockDim = dim3(kSkThreads);
+  cfg.blockDim = dim3(L::kThreads);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;  // behind the plane conversion
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, inv_w, M, N, K, S, y, acc_out, ws, tickets,
-                            ctx->err_word);
+  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, rowsum_part, inv_w, M, N, K, S, y, acc_out, ws,
+                            tickets, ctx->err_word);
+}
+
+// Workspace: [fp32 partial sums M x N, tile tickets] (split K only; zero on
+// entry) then the chunk sums of the codes (M x plane_chunks(K) ints).
+struct SkWorkspace {
+  int S;
+  size_t zeroed;  // bytes that must be zero on entry
+  size_t total;
+};
+SkWorkspace skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N) {
+  SkWorkspace w;
+  const int n_wt = static_cast<int>((N + kSkBM - 1) / kSkBM);
+  w.S = choose_splits(M, n_wt, static_cast<int>(K >> 7), N, ctx->num_sms);
+  w.zeroed = w.S == 1 ? 0
+                      : ((static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255)) +
+                            static_cast<size_t>(n_wt) * 4;
+  w.total = ((w.zeroed + 255) & ~size_t(255)) +
+            ((static_cast<size_t>(M) * plane_chunks(static_cast<int>(K)) * 4 + 255) & ~size_t(255));
+  return w;
 }
 
 }  // namespace
@@ -526,14 +619,14 @@ bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N) {
 }
 
 size_t gemm_skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N) {
-  const int n_wt = static_cast<int>((N + kSkBM - 1) / kSkBM);
-  const int S = choose_splits(M, n_wt, static_cast<int>(K >> 7), N, ctx->num_sms);
-  if (S == 1) return 0;
-  return ((static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255)) +
-         static_cast<size_t>(n_wt) * 4;
+  return skinny_workspace(ctx, M, K, N).total;
 }
 
-cudaError_t launch_gemm_skinny(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
+size_t gemm_skinny_zeroed_bytes(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N) {
+  return skinny_workspace(ctx, M, K, N).zeroed;
+}
+
+cudaError_t launch_gemm_skinny(const DeviceContext* ctx, __half* codes_f16, const float* a_scale,
                                const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
                                int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
                                int* status) {
@@ -545,31 +638,48 @@ cudaError_t launch_gemm_skinny(const DeviceContext* ctx, const __half* codes_f16
   }
   const float inv_w = 1.0f / w_scale;  // IEEE division, as in the oracle
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  const int n_wt = (n + kSkBM - 1) / kSkBM;
-  const int S = choose_splits(M, n_wt, k >> 7, N, ctx->num_sms);
+  const SkWorkspace wl = skinny_workspace(ctx, M, K, N);
+  const int S = wl.S;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
   float* ws = nullptr;
   int* tickets = nullptr;
   if (S > 1) {
     // the partial sums are added into a zeroed fp32 [M, N] array
     const size_t ws_bytes = (static_cast<size_t>(M) * static_cast<size_t>(N) * 4 + 255) & ~size_t(255);
-    ws = static_cast<float*>(workspace);
-    tickets = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + ws_bytes);
+    ws = reinterpret_cast<float*>(wsb);
+    tickets = reinterpret_cast<int*>(wsb + ws_bytes);
     if (!workspace_zeroed) {
-      cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes + static_cast<size_t>(n_wt) * 4, s);
+      cudaError_t e = cudaMemsetAsync(workspace, 0, wl.zeroed, s);
       if (e != cudaSuccess) return e;
     }
   }
+  int* rowsum_part = reinterpret_cast<int*>(wsb + ((wl.zeroed + 255) & ~size_t(255)));
+  {
+    // the codes as the two e4m3 planes, in place, and their chunk sums
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plane_chunks(k)), static_cast<unsigned>(m));
+    cfg.blockDim = dim3(kPlaneThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_token_planes, codes_f16, k, rowsum_part);
+    if (e != cudaSuccess) return e;
+  }
+  const uint8_t* planes = reinterpret_cast<const uint8_t*>(codes_f16);
   const int bn = m <= 16 ? 16 : m <= 32 ? 32 : 64;
   switch (bn) {
     case 16:
-      return launch_bn<16>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, k, n, S, y, acc_out, ws, tickets,
-                           pdl, s, status);
+      return launch_bn<16>(ctx, encode, planes, a_scale, rowsum_part, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
+                           tickets, s, status);
     case 32:
-      return launch_bn<32>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, k, n, S, y, acc_out, ws, tickets,
-                           pdl, s, status);
+      return launch_bn<32>(ctx, encode, planes, a_scale, rowsum_part, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
+                           tickets, s, status);
     default:
-      return launch_bn<64>(ctx, encode, codes_f16, a_scale, packed_w, inv_w, m, k, n, S, y, acc_out, ws, tickets,
-                           pdl, s, status);
+      return launch_bn<64>(ctx, encode, planes, a_scale, rowsum_part, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
+                           tickets, s, status);
   }
 }
 

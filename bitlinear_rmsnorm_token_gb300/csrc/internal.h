@@ -130,13 +130,16 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
                            cudaStream_t s, int* status, const float* head_w = nullptr, int head_dim = 0,
                            float eps = 0.0f, bool* head_fused = nullptr);
 
-// Tensor-core contraction for 9..63 tokens (weights as the MMA's M side, K
-// split across CTAs).  Needs gemm_skinny_workspace() bytes of device memory
-// (0 when K is not split), zero on entry: zeroed here on the stream unless
-// workspace_zeroed.
+// Tensor-core contraction for 9..63 tokens (8-bit operands, weights as the
+// MMA's M side, K split across CTAs where that pays).  The fp16 codes (scratch
+// of the caller) are rewritten in place as the operand's two e4m3 planes.
+// Needs gemm_skinny_workspace() bytes of device memory, of which the first
+// gemm_skinny_zeroed_bytes() (0 when K is not split) must be zero on entry:
+// zeroed here on the stream unless workspace_zeroed.
 bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N);
 size_t gemm_skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
-cudaError_t launch_gemm_skinny(const DeviceContext* ctx, const __half* codes_f16, const float* a_scale,
+size_t gemm_skinny_zeroed_bytes(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemm_skinny(const DeviceContext* ctx, __half* codes_f16, const float* a_scale,
                                const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
                                int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
                                int* status);

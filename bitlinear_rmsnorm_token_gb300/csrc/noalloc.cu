@@ -133,7 +133,8 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   const bool skinny = sk_shape && fits;
   uint8_t* gws = static_cast<uint8_t*>(scratch) + code_bytes + scale_bytes;
   void* tc_ws = (!sk_shape && fits && gws_bytes) ? static_cast<void*>(gws) : nullptr;
-  cudaError_t e = (fits && gws_bytes) ? cudaMemsetAsync(gws, 0, gws_bytes, s) : cudaSuccess;
+  const size_t zero_bytes = skinny ? gemm_skinny_zeroed_bytes(ctx, M, K, N) : gws_bytes;
+  cudaError_t e = (fits && zero_bytes) ? cudaMemsetAsync(gws, 0, zero_bytes, s) : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr, true, s);
   int st = BITNET_OK;

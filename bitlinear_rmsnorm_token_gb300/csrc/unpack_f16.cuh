@@ -51,36 +51,4 @@ __device__ __forceinline__ void unpack_row_slab(const uint32_t (&wd)[8], int hf,
   }
 }
 
-// Sixteen bytes (bytes 16h .. 16h + 15 of one row's I2_S block: elements
-// 32 s + 16 h + j, j = 0..15, of slot s) as 32 TMEM columns of fp16 pairs, the
-// layout of an MMA A operand held in tensor memory: column 8 s + c holds
-// elements (32 s + 16 h + 2c, + 1), weight value code - 1.  For slot s the
-// masked field (t & (0xC0 >> 2s)) ORed into the fp16 pattern 0x6400 is
-// 1024 + code * 4^(3-s); one fp16x2 fma by 4^(s-3) with addend
-// -(1024 * 4^(s-3) + 1) leaves code - 1 exactly (every value involved is an
-// integer or a power-of-two fraction well inside fp16's precision).
-__device__ __forceinline__ uint32_t fma_f16x2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ void unpack_half_block_cols(const uint4& u, uint32_t (&out)[32]) {
-  // fp16x2 scale 4^(s-3) and addend -(1024 * 4^(s-3) + 1), slots 0..3
-  constexpr uint32_t kScale[4] = {0x24002400u, 0x2C002C00u, 0x34003400u, 0x3C003C00u};   // 1/64, 1/16, 1/4, 1
-  constexpr uint32_t kAddend[4] = {0xCC40CC40u, 0xD410D410u, 0xDC04DC04u, 0xE401E401u};  // -17, -65, -257, -1025
-  const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t lo = prmt(wd[i], 0u, 0x4140u);  // bytes 0, 1 (elements 4i, 4i + 1) in the low bytes of each half
-    const uint32_t hi = prmt(wd[i], 0u, 0x4342u);  // bytes 2, 3
-#pragma unroll
-    for (int sl = 0; sl < 4; ++sl) {
-      const uint32_t m = 0x00C000C0u >> (2 * sl);
-      out[8 * sl + 2 * i] = fma_f16x2((lo & m) | 0x64006400u, kScale[sl], kAddend[sl]);
-      out[8 * sl + 2 * i + 1] = fma_f16x2((hi & m) | 0x64006400u, kScale[sl], kAddend[sl]);
-    }
-  }
-}
-
 }  // namespace bitnet
