@@ -305,14 +305,18 @@ __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
     }
   } else if (warp >= L::kMmaWarp0) {
     // -------------------------------------------------------- MMA issuers
-    // pipeline j issues the stages of running index g = j mod P; it walks
-    // every stage to keep its place in the token ring
+    // pipeline j issues the stages of running index g = j mod P (over the
+    // CTA's units); ring positions follow from the running counts of stages,
+    // packed groups and token slots, so the loop visits its own stages only
+    // (walking every stage put ~1000 cycles of loop overhead between two of a
+    // warp's stages)
     if (lane == 0) {
       const int j = warp - L::kMmaWarp0;
       constexpr uint32_t idesc = idesc_e4m3_f32(kSkBM, L::kN2);
-      int n = 0, b = 0, g = 0, tl = 0;
+      int n = 0, g0 = 0, tg0 = 0, tl = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++tl) {
         const SkUnit w = sk_unit(u, S, nkb);
+        const int len = w.len();
         const int a = L::kAccBufs == 2 ? (tl & 1) : 0;
         const int use = L::kAccBufs == 2 ? (tl >> 1) : tl;  // earlier uses of buffer a
         // also keeps a pipeline without stages in this unit from arriving on
@@ -321,93 +325,97 @@ __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((kP * a + j) * L::kN2);
         bool ok = true, any = false;
-        for (int i = 0; i < w.len(); ++i, ++g) {
-          if (g % kP == j) {
-            const int s = L::kAPerPipe * j + n % L::kAPerPipe;
-            if (!mbar_wait(&afull[s], (n / L::kAPerPipe) & 1, err, abort_flag)) {  // also covers the tokens
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(L::kACol0 + s * kSkAStageCols);
-            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + b * L::kTSlot + (i % kTG) * L::kB));
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              tc_mma_f8_ta(d_tmem, a_tmem + static_cast<uint32_t>(8 * t), bdesc + static_cast<uint64_t>(2 * t),
-                           idesc, (any || t) ? 1u : 0u);
-            any = true;
-            tc_commit(&aempty[s]);
-            tc_commit(&tempty[b]);
-            // a unit's last token slot may hold fewer than kTG of its stages:
-            // arrive for the missing ones (the slot is released once the
-            // commits of the stages it does hold have arrived as well)
-            if (i == w.len() - 1)
-              for (int r = i % kTG + 1; r < kTG; ++r) mbar_arrive(&tempty[b]);
-            ++n;
+        for (int i = ((j - g0) % kP + kP) % kP; i < len; i += kP) {
+          const int s = L::kAPerPipe * j + n % L::kAPerPipe;
+          if (!mbar_wait(&afull[s], (n / L::kAPerPipe) & 1, err, abort_flag)) {  // also covers the tokens
+            ok = false;
+            break;
           }
-          if (i % kTG == kTG - 1 || i == w.len() - 1)
-            if (++b == kTS) b = 0;
+          tc_fence_after();
+          const int b = (tg0 + i / kTG) % kTS;
+          const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(L::kACol0 + s * kSkAStageCols);
+          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + b * L::kTSlot + (i % kTG) * L::kB));
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            tc_mma_f8_ta(d_tmem, a_tmem + static_cast<uint32_t>(8 * t), bdesc + static_cast<uint64_t>(2 * t), idesc,
+                         (any || t) ? 1u : 0u);
+          any = true;
+          tc_commit(&aempty[s]);
+          tc_commit(&tempty[b]);
+          // a unit's last token slot may hold fewer than kTG of its stages:
+          // arrive for the missing ones (the slot is released once the
+          // commits of the stages it does hold have arrived as well)
+          if (i == len - 1)
+            for (int r = i % kTG + 1; r < kTG; ++r) mbar_arrive(&tempty[b]);
+          ++n;
         }
         if (!ok) break;
         if (any) tc_commit(&acc_full[a]);
         else mbar_arrive(&acc_full[a]);
+        g0 += len;
+        tg0 += (len + kTG - 1) / kTG;
       }
     }
   } else if (warp < L::kUnpackWarps) {
     // --------------------------------------------------------------- unpack
+    // pipeline pj's stages, group by group; every unpack warp releases each
+    // packed group once, after its own stages in it (a full group holds 4 / P
+    // stages of every pipeline; a unit's short last group may hold none)
     const int pj = warp >> 2;            // pipeline: stages of running index pj mod P
     const int q = warp & 3;              // TMEM lane quadrant: weight rows 32q .. 32q + 31
     const int row = 32 * q + lane;       // weight row of the tile
     const uint32_t tq = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(L::kACol0);
-    int n = 0, p = 0, pph = 0, b = 0, bph = 0, g = 0;
-    bool pk_ready = false;  // the current packed group has been waited for
+    int n = 0, g0 = 0, pg0 = 0, tg0 = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const SkUnit w = sk_unit(u, S, nkb);
-      for (int i = 0; i < w.len(); ++i, ++g) {
-        const int gi = i % kSkPkGroup;  // column within the packed group (groups stay whole)
-        if (g % kP == pj) {
-          if (!pk_ready && !mbar_wait(&pk_full[p], pph, err, abort_flag)) goto unpack_done;
-          pk_ready = true;
-          // the row's 32 bytes of block column gi: chunks 2 gi, 2 gi + 1,
-          // stored at chunk c ^ (row & 7)
-          const uint8_t* src = sPk + p * L::kPk + row * 128;
-          const uint4 c0 = *reinterpret_cast<const uint4*>(src + (((2 * gi) ^ (row & 7)) << 4));
-          const uint4 c1 = *reinterpret_cast<const uint4*>(src + (((2 * gi + 1) ^ (row & 7)) << 4));
-          const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          uint32_t cols[32];
+      const int len = w.len();
+      const int ngroups = (len + kSkPkGroup - 1) / kSkPkGroup;
+      int i = ((pj - g0) % kP + kP) % kP;  // this pipeline's first stage of the unit
+      for (int G = 0; G < ngroups; ++G) {
+        const int pidx = pg0 + G;
+        const int p = pidx % L::kPkSlots;
+        const int gend = min(kSkPkGroup * (G + 1), len);
+        if (i < gend) {
+          if (!mbar_wait(&pk_full[p], (pidx / L::kPkSlots) & 1, err, abort_flag)) goto unpack_done;
+          for (; i < gend; i += kP) {
+            const int gi = i - kSkPkGroup * G;  // column within the packed group
+            // the row's 32 bytes of block column gi: chunks 2 gi, 2 gi + 1,
+            // stored at chunk c ^ (row & 7)
+            const uint8_t* src = sPk + p * L::kPk + row * 128;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(src + (((2 * gi) ^ (row & 7)) << 4));
+            const uint4 c1 = *reinterpret_cast<const uint4*>(src + (((2 * gi + 1) ^ (row & 7)) << 4));
+            const uint32_t wd[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t cols[32];
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
+            for (int c = 0; c < 8; ++c)
 #pragma unroll
-            for (int sl = 0; sl < 4; ++sl) cols[8 * sl + c] = (wd[c] >> (6 - 2 * sl)) & 0x03030303u;
-          const int s = L::kAPerPipe * pj + n % L::kAPerPipe;
-          // the MMAs of the A stage's previous use must be done with it
-          if (!mbar_wait(&aempty[s], ((n / L::kAPerPipe) & 1) ^ 1, err, abort_flag)) goto unpack_done;
-          tc_fence_after();
-          __syncwarp();
-          tmem_st_32x32b_x32(tq + static_cast<uint32_t>(s * kSkAStageCols), cols);
-          tmem_st_wait();
-          tc_fence_before();
-          // the packed bytes are consumed: order the reads before the next TMA
-          // into the slot
-          fence_proxy_async_smem();
-          // afull also tells the MMA thread that the stage's token planes have
-          // landed: it then waits on one barrier per stage instead of two
-          if (!mbar_wait(&tfull[b], bph, err, abort_flag)) goto unpack_done;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[s]);
-          ++n;
+              for (int sl = 0; sl < 4; ++sl) cols[8 * sl + c] = (wd[c] >> (6 - 2 * sl)) & 0x03030303u;
+            const int s = L::kAPerPipe * pj + n % L::kAPerPipe;
+            // the MMAs of the A stage's previous use must be done with it
+            if (!mbar_wait(&aempty[s], ((n / L::kAPerPipe) & 1) ^ 1, err, abort_flag)) goto unpack_done;
+            tc_fence_after();
+            __syncwarp();
+            tmem_st_32x32b_x32(tq + static_cast<uint32_t>(s * kSkAStageCols), cols);
+            tmem_st_wait();
+            tc_fence_before();
+            // the packed bytes are consumed: order the reads before the next
+            // TMA into the slot
+            fence_proxy_async_smem();
+            // afull also tells the MMA thread that the stage's token planes
+            // have landed: it then waits on one barrier per stage, not two
+            const int tidx = tg0 + i / kTG;
+            if (!mbar_wait(&tfull[tidx % kTS], (tidx / kTS) & 1, err, abort_flag)) goto unpack_done;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[s]);
+            ++n;
+          }
         }
-        if (i % kTG == kTG - 1 || i == w.len() - 1)
-          if (++b == kTS) { b = 0; bph ^= 1; }
-        // every unpack warp of every pipeline releases the packed group once
-        // it is past the group's last stage
-        if (gi == kSkPkGroup - 1 || i == w.len() - 1) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&pk_empty[p]);
-          if (++p == L::kPkSlots) { p = 0; pph ^= 1; }
-          pk_ready = false;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pk_empty[p]);
       }
+      g0 += len;
+      pg0 += ngroups;
+      tg0 += (len + kTG - 1) / kTG;
     }
   unpack_done:;
   } else {
