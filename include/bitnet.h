@@ -185,7 +185,10 @@ BITNET_API int bitnet_bitlinear_forward_group(const bitnet_projection* projs, in
  *     (int8 for M <= 8, fp16 otherwise: M*K or 2*M*K bytes) and per-token
  *     scales (4*M bytes), each rounded up to 256 bytes, then the fp32 partial
  *     sums of a K split (up to 4*M*N bytes plus 4 bytes per output tile) where
- *     the contraction splits K.  Problems whose codes and scales do not fit
+ *     the contraction splits K, and for 9..63 tokens the sums of the codes per
+ *     2048-value chunk (4*M*ceil(K/2048) bytes; the fp16 codes are rewritten
+ *     in place there as the contraction's 8-bit operand).  Problems whose
+ *     codes and scales do not fit
  *     return BITNET_ERR_SCRATCH_LIMIT without launching anything.  When the
  *     codes and scales fit but the partial sums do not, the contraction runs
  *     without the K split (the same y; a slower plan than
