@@ -228,8 +228,8 @@ int bitnet_i2s_gemm(const int8_t* a_codes, const float* a_scale, const uint8_t* 
   cudaError_t e = launch_codes_to_f16(a_codes, f16, M * K, s);
   int st = BITNET_OK;
   if (e == cudaSuccess)
-    e = skinny ? launch_gemm_skinny(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, acc_out, gws, false, true, s,
-                                    &st)
+    e = skinny ? launch_gemm_skinny(ctx, f16, nullptr, a_scale, packed_w, w_scale, M, K, N, y, acc_out, gws, false,
+                                    true, s, &st)
                : launch_gemm_tc(ctx, f16, a_scale, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, acc_out, gws, false, true, s, &st);
   pool_free(buf, s);
   if (st != BITNET_OK) return st;
@@ -255,6 +255,22 @@ cudaError_t launch_norm_any(const float* x, const float* up, int act, const floa
   if (e != cudaSuccess) return e;
   return launch_rmsnorm_quant(h_buf, g, M, K, eps, codes_i8, codes_f16, a_scale, nullptr, nullptr, pdl, s);
 }
+
+// The same for the 9..63-token contraction: the codes as its two e4m3 planes
+// (`planes` 256-byte aligned) and their row sums.
+cudaError_t launch_norm_planes_any(const float* x, const float* up, int act, const float* g, int64_t M, int K,
+                                   float eps, void* planes, float* a_scale, int32_t* rowsum, float* h_buf, bool pdl,
+                                   cudaStream_t s) {
+  if (act == 0)
+    return launch_rmsnorm_quant_planes(x, BITNET_DTYPE_F32, g, M, K, eps, planes, a_scale, rowsum, pdl, s);
+  if (rmsnorm_quant_glu_fused_supported(K))
+    return launch_rmsnorm_quant_glu_planes(x, up, act, g, M, K, eps, planes, a_scale, rowsum, pdl, s);
+  cudaError_t e = launch_glu(x, up, act, M * K, h_buf, s);
+  if (e != cudaSuccess) return e;
+  return launch_rmsnorm_quant_planes(h_buf, BITNET_DTYPE_F32, g, M, K, eps, planes, a_scale, rowsum, pdl, s);
+}
+
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
 size_t glu_buffer_bytes(int act, int64_t M, int64_t K) {
   return (act != 0 && !rmsnorm_quant_glu_fused_supported(static_cast<int>(K)))
@@ -335,20 +351,28 @@ int forward_impl(const float* x, const float* up, int act, const float* norm_w, 
   // accesses) follows it
   const size_t gws_raw = skinny ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N);
   const size_t gws_bytes = (gws_raw + 255) & ~size_t(255);
+  const size_t rs_bytes = skinny ? (static_cast<size_t>(M) * 4 + 255) & ~size_t(255) : 0;
   uint8_t* ws = nullptr;
-  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws), code_bytes + scale_bytes + gws_bytes + h_bytes, s)))
+  if ((rc = pool_alloc(ctx, reinterpret_cast<void**>(&ws),
+                       code_bytes + scale_bytes + gws_bytes + h_bytes + rs_bytes, s)))
     return rc;
   __half* f16 = reinterpret_cast<__half*>(ws);
   float* as = reinterpret_cast<float*>(ws + code_bytes);
   uint8_t* gws = ws + code_bytes + scale_bytes;
   float* h = h_bytes ? reinterpret_cast<float*>(ws + code_bytes + scale_bytes + gws_bytes) : nullptr;
+  // 9..63 tokens: the norm launch writes the contraction's planes and row sums
+  // directly (its block layout needs a 256-byte aligned array)
+  int32_t* rs = skinny && aligned256(f16)
+                    ? reinterpret_cast<int32_t*>(ws + code_bytes + scale_bytes + gws_bytes + h_bytes)
+                    : nullptr;
   const size_t zero_bytes = skinny ? gemm_skinny_zeroed_bytes(ctx, M, K, N) : gws_bytes;
   cudaError_t e = zero_bytes ? cudaMemsetAsync(gws, 0, zero_bytes, s) : cudaSuccess;
   if (e == cudaSuccess)
-    e = launch_norm_any(x, up, act, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, h, true, s);
+    e = rs ? launch_norm_planes_any(x, up, act, norm_w, M, static_cast<int>(K), eps, f16, as, rs, h, true, s)
+           : launch_norm_any(x, up, act, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, h, true, s);
   int st = BITNET_OK;
   if (e == cudaSuccess)
-    e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
+    e = skinny ? launch_gemm_skinny(ctx, f16, rs, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
                : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, nullptr, gws_bytes ? gws : nullptr, true,
                                 true, s, &st, head_w, head_dim, eps, head_fused);
   pool_free(ws, s);
@@ -391,7 +415,8 @@ int forward_typed(const void* x, int x_dtype, const void* norm_w, int g_dtype, c
   const size_t scale_bytes = few ? 0 : round256(static_cast<size_t>(M) * 4);
   const size_t gws_bytes =
       few ? 0 : round256(skinny ? gemm_skinny_workspace(ctx, M, K, N) : gemm_tc_workspace(ctx, M, K, N));
-  const size_t total = g_bytes + x_bytes + y_bytes + code_bytes + scale_bytes + gws_bytes;
+  const size_t rs_bytes = skinny ? round256(static_cast<size_t>(M) * 4) : 0;
+  const size_t total = g_bytes + x_bytes + y_bytes + code_bytes + scale_bytes + gws_bytes + rs_bytes;
   uint8_t* pool = nullptr;
   if (total && (rc = pool_alloc(ctx, reinterpret_cast<void**>(&pool), total, s))) return rc;
   uint8_t* at = pool;
@@ -406,6 +431,8 @@ int forward_typed(const void* x, int x_dtype, const void* norm_w, int g_dtype, c
   __half* f16 = reinterpret_cast<__half*>(take(code_bytes));
   float* as = reinterpret_cast<float*>(take(scale_bytes));
   uint8_t* gws = take(gws_bytes);
+  int32_t* rs = reinterpret_cast<int32_t*>(take(rs_bytes));
+  if (rs && !aligned256(f16)) rs = nullptr;  // the planes' block layout needs a 256-byte aligned array
   const float* g = g32 ? g32 : static_cast<const float*>(norm_w);
   cudaError_t e = cudaSuccess;
   if (g32) e = launch_convert(norm_w, g_dtype, g32, BITNET_DTYPE_F32, K, s);
@@ -421,10 +448,11 @@ int forward_typed(const void* x, int x_dtype, const void* norm_w, int g_dtype, c
     const size_t zero_bytes = skinny ? gemm_skinny_zeroed_bytes(ctx, M, K, N) : gws_bytes;
     if (e == cudaSuccess && zero_bytes) e = cudaMemsetAsync(gws, 0, zero_bytes, s);
     if (e == cudaSuccess)
-      e = launch_rmsnorm_quant_f16_in(x, x_dtype, g, M, static_cast<int>(K), eps, f16, as, true, s);
+      e = rs ? launch_rmsnorm_quant_planes(x, x_dtype, g, M, static_cast<int>(K), eps, f16, as, rs, true, s)
+             : launch_rmsnorm_quant_f16_in(x, x_dtype, g, M, static_cast<int>(K), eps, f16, as, true, s);
     if (e == cudaSuccess)
-      e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y32 ? y32 : static_cast<float*>(y),
-                                      nullptr, gws, true, true, s, &st)
+      e = skinny ? launch_gemm_skinny(ctx, f16, rs, as, packed_w, w_scale, M, K, N,
+                                      y32 ? y32 : static_cast<float*>(y), nullptr, gws, true, true, s, &st)
                  : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, y_dtype, nullptr,
                                   gws_bytes ? gws : nullptr, true, true, s, &st);
   }

@@ -64,9 +64,8 @@
 // unwinds without trapping.
 #include "common.cuh"
 #include "internal.h"
+#include "planes.cuh"
 #include "rowquant.cuh"
-
-#include <cuda_fp8.h>
 
 namespace bitnet {
 namespace {
@@ -120,10 +119,6 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t e4m3_byte(int v) {
-  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(static_cast<float>(v), __NV_SATFINITE, __NV_E4M3));
-}
-
 // One CTA per (token row, 2048-value chunk): the chunk's fp16 codes rewritten
 // in place as the two e4m3 planes, block by block (a warp reads its two
 // 256-byte blocks, both loads in flight, before writing them back), and the
@@ -152,14 +147,14 @@ __global__ void __launch_bounds__(kPlaneThreads) k_token_planes(__half* codes, i
     const __half2 h23 = *reinterpret_cast<const __half2*>(&v[h].y);
     const int q[4] = {static_cast<int>(__low2float(h01)), static_cast<int>(__high2float(h01)),
                       static_cast<int>(__low2float(h23)), static_cast<int>(__high2float(h23))};
-    uint32_t hi = 0, lo = 0;
+    uint32_t packed = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int l = q[i] & 15;
-      lo |= e4m3_byte(l) << (8 * i);
-      hi |= e4m3_byte((q[i] - l) / 16) << (8 * i);
+      packed |= (static_cast<uint32_t>(q[i]) & 0xFFu) << (8 * i);
       sum += q[i];
     }
+    uint32_t hi, lo;
+    plane_words4(packed, hi, lo);
     uint8_t* blk = row + (kb0 + h) * 256;
     *reinterpret_cast<uint32_t*>(blk + lane * 4) = hi;
     *reinterpret_cast<uint32_t*>(blk + 128 + lane * 4) = lo;
@@ -204,8 +199,9 @@ __device__ __forceinline__ SkUnit sk_unit(int u, int S, int nkb) {
 template <int BN>
 __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
     k_gemm_skinny(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_w,
-                  const float* __restrict__ a_scale, const int* __restrict__ rowsum_part, float inv_w, int M, int N,
-                  int K, int S, float* __restrict__ y, int32_t* __restrict__ acc_out, float* __restrict__ ws,
+                  const float* __restrict__ a_scale, const int* __restrict__ rowsum_part, int nparts, float inv_w,
+                  int M, int N, int K, int S, float* __restrict__ y, int32_t* __restrict__ acc_out,
+                  float* __restrict__ ws,
                   int* __restrict__ tickets, unsigned* err) {
   using L = SkLayout<BN>;
   constexpr int kP = L::kPipes;
@@ -426,7 +422,7 @@ __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
       sInv[t] = t < M ? __frcp_rn(__ldg(a_scale + t)) : 0.0f;
       int rs = 0;
       if (t < M)
-        for (int c = 0; c < plane_chunks(K); ++c) rs += __ldg(rowsum_part + t * plane_chunks(K) + c);
+        for (int c = 0; c < nparts; ++c) rs += __ldg(rowsum_part + t * nparts + c);
       sRs[t] = rs;
     }
     epi_bar();
@@ -541,7 +537,7 @@ int choose_splits(int64_t M, int n_wt, int nkb, int64_t N, int ctas) {
 
 template <int BN>
 cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const uint8_t* planes, const float* a_scale,
-                      const int* rowsum_part, const uint8_t* packed_w, float inv_w, int M, int K, int N, int S, float* y,
+                      const int* rowsum_part, int nparts, const uint8_t* packed_w, float inv_w, int M, int K, int N, int S, float* y,
                       int32_t* acc_out, float* ws, int* tickets, cudaStream_t s, int* status) {
   using L = SkLayout<BN>;
   CUtensorMap tm_tok, tm_w;
@@ -590,8 +586,8 @@ cudaError_t launch_bn(const DeviceContext* ctx, EncodeTiledFn encode, const uint
   attr[0].val.programmaticStreamSerializationAllowed = 1;  // behind the plane conversion
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, rowsum_part, inv_w, M, N, K, S, y, acc_out, ws,
-                            tickets, ctx->err_word);
+  return cudaLaunchKernelEx(&cfg, kern, tm_tok, tm_w, a_scale, rowsum_part, nparts, inv_w, M, N, K, S, y, acc_out,
+                            ws, tickets, ctx->err_word);
 }
 
 // Workspace: [fp32 partial sums M x N, tile tickets] (split K only; zero on
@@ -634,7 +630,12 @@ size_t gemm_skinny_zeroed_bytes(const DeviceContext* ctx, int64_t M, int64_t K, 
   return skinny_workspace(ctx, M, K, N).zeroed;
 }
 
-cudaError_t launch_gemm_skinny(const DeviceContext* ctx, __half* codes_f16, const float* a_scale,
+int32_t* gemm_skinny_rowsum_area(const DeviceContext* ctx, void* workspace, int64_t M, int64_t K, int64_t N) {
+  const SkWorkspace w = skinny_workspace(ctx, M, K, N);
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ((w.zeroed + 255) & ~size_t(255)));
+}
+
+cudaError_t launch_gemm_skinny(const DeviceContext* ctx, void* codes, const int32_t* rowsum, const float* a_scale,
                                const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
                                int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
                                int* status) {
@@ -661,8 +662,12 @@ cudaError_t launch_gemm_skinny(const DeviceContext* ctx, __half* codes_f16, cons
       if (e != cudaSuccess) return e;
     }
   }
-  int* rowsum_part = reinterpret_cast<int*>(wsb + ((wl.zeroed + 255) & ~size_t(255)));
-  {
+  const int* rowsum_part = rowsum;
+  int nparts = 1;
+  if (!rowsum) {
+    int* parts = reinterpret_cast<int*>(wsb + ((wl.zeroed + 255) & ~size_t(255)));
+    rowsum_part = parts;
+    nparts = plane_chunks(k);
     // the codes as the two e4m3 planes, in place, and their chunk sums
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plane_chunks(k)), static_cast<unsigned>(m));
@@ -673,20 +678,20 @@ cudaError_t launch_gemm_skinny(const DeviceContext* ctx, __half* codes_f16, cons
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_token_planes, codes_f16, k, rowsum_part);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_token_planes, static_cast<__half*>(codes), k, parts);
     if (e != cudaSuccess) return e;
   }
-  const uint8_t* planes = reinterpret_cast<const uint8_t*>(codes_f16);
+  const uint8_t* planes = static_cast<const uint8_t*>(codes);
   const int bn = m <= 16 ? 16 : m <= 32 ? 32 : 64;
   switch (bn) {
     case 16:
-      return launch_bn<16>(ctx, encode, planes, a_scale, rowsum_part, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
+      return launch_bn<16>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
                            tickets, s, status);
     case 32:
-      return launch_bn<32>(ctx, encode, planes, a_scale, rowsum_part, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
+      return launch_bn<32>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
                            tickets, s, status);
     default:
-      return launch_bn<64>(ctx, encode, planes, a_scale, rowsum_part, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
+      return launch_bn<64>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
                            tickets, s, status);
   }
 }

@@ -73,6 +73,16 @@ cudaError_t launch_rmsnorm_quant_glu(const float* gate, const float* up, int act
                                      float* xn_out, bool pdl, cudaStream_t s);
 cudaError_t launch_glu(const float* gate, const float* up, int act, int64_t count, float* h, cudaStream_t s);
 
+// The norm/quant writing the codes as the 9..63-token contraction's two e4m3
+// planes (planes.cuh; `planes` 256-byte aligned, 2*M*K bytes) and their row
+// sums (rowsum[M], required): x in x_dtype, or the down projection's
+// act(gate) * up for K <= 3072.
+cudaError_t launch_rmsnorm_quant_planes(const void* x, int x_dtype, const float* g, int64_t M, int K, float eps,
+                                       void* planes, float* a_scale, int32_t* rowsum, bool pdl, cudaStream_t s);
+cudaError_t launch_rmsnorm_quant_glu_planes(const float* gate, const float* up, int act, const float* g, int64_t M,
+                                           int K, float eps, void* planes, float* a_scale, int32_t* rowsum, bool pdl,
+                                           cudaStream_t s);
+
 // int8 codes -> fp16 codes (for the tensor-core path of the int8 API).
 cudaError_t launch_codes_to_f16(const int8_t* codes, __half* out, int64_t count, cudaStream_t s);
 
@@ -131,15 +141,20 @@ cudaError_t launch_gemm_tc(const DeviceContext* ctx, const __half* codes_f16, co
                            float eps = 0.0f, bool* head_fused = nullptr);
 
 // Tensor-core contraction for 9..63 tokens (8-bit operands, weights as the
-// MMA's M side, K split across CTAs where that pays).  The fp16 codes (scratch
-// of the caller) are rewritten in place as the operand's two e4m3 planes.
-// Needs gemm_skinny_workspace() bytes of device memory, of which the first
-// gemm_skinny_zeroed_bytes() (0 when K is not split) must be zero on entry:
-// zeroed here on the stream unless workspace_zeroed.
+// MMA's M side, K split across CTAs where that pays).  `codes` holds either the
+// fp16 codes (scratch of the caller; rowsum null), rewritten in place here as
+// the operand's two e4m3 planes, or the planes already (launch_rmsnorm_quant_
+// planes) with their row sums in rowsum.  Needs gemm_skinny_workspace() bytes
+// of device memory, of which the first gemm_skinny_zeroed_bytes() (0 when K
+// is not split) must be zero on entry: zeroed here on the stream unless
+// workspace_zeroed.
 bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N);
 size_t gemm_skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
 size_t gemm_skinny_zeroed_bytes(const DeviceContext* ctx, int64_t M, int64_t K, int64_t N);
-cudaError_t launch_gemm_skinny(const DeviceContext* ctx, __half* codes_f16, const float* a_scale,
+// M ints inside that workspace (not zeroed) where a norm launch that writes
+// the planes may put their row sums.
+int32_t* gemm_skinny_rowsum_area(const DeviceContext* ctx, void* workspace, int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemm_skinny(const DeviceContext* ctx, void* codes, const int32_t* rowsum, const float* a_scale,
                                const uint8_t* packed_w, float w_scale, int64_t M, int64_t K, int64_t N, float* y,
                                int32_t* acc_out, void* workspace, bool workspace_zeroed, bool pdl, cudaStream_t s,
                                int* status);

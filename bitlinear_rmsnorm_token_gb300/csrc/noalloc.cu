@@ -135,11 +135,16 @@ extern "C" int bitnet_bitlinear_forward_noalloc(const float* x, const float* nor
   void* tc_ws = (!sk_shape && fits && gws_bytes) ? static_cast<void*>(gws) : nullptr;
   const size_t zero_bytes = skinny ? gemm_skinny_zeroed_bytes(ctx, M, K, N) : gws_bytes;
   cudaError_t e = (fits && zero_bytes) ? cudaMemsetAsync(gws, 0, zero_bytes, s) : cudaSuccess;
+  // 9..63 tokens: the norm launch writes the contraction's planes, and their
+  // row sums into the workspace (the array is 256-byte aligned)
+  int32_t* rs = skinny ? gemm_skinny_rowsum_area(ctx, gws, M, K, N) : nullptr;
   if (e == cudaSuccess)
-    e = launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr, true, s);
+    e = rs ? launch_rmsnorm_quant_planes(x, BITNET_DTYPE_F32, norm_w, M, static_cast<int>(K), eps, f16, as, rs, true,
+                                         s)
+           : launch_rmsnorm_quant(x, norm_w, M, static_cast<int>(K), eps, nullptr, f16, as, nullptr, nullptr, true, s);
   int st = BITNET_OK;
   if (e == cudaSuccess)
-    e = skinny ? launch_gemm_skinny(ctx, f16, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
+    e = skinny ? launch_gemm_skinny(ctx, f16, rs, as, packed_w, w_scale, M, K, N, y, nullptr, gws, true, true, s, &st)
                : launch_gemm_tc(ctx, f16, as, packed_w, w_scale, M, K, N, y, BITNET_DTYPE_F32, nullptr, tc_ws, true, true, s, &st);
   if (st != BITNET_OK) return st;
   return e == cudaSuccess ? BITNET_OK : BITNET_ERR_CUDA;

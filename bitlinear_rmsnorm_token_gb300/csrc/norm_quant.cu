@@ -13,6 +13,7 @@
 // held in registers, longer ones are re-read through L1/L2.
 #include "common.cuh"
 #include "internal.h"
+#include "planes.cuh"
 #include "rowquant.cuh"
 
 namespace bitnet {
@@ -38,6 +39,20 @@ __device__ __forceinline__ void store_codes4<__half>(__half* dst, float4 n, floa
   v.x = quant_pack2_f16(n.x, n.y, a_scale);
   v.y = quant_pack2_f16(n.z, n.w, a_scale);
   *reinterpret_cast<uint2*>(dst) = v;
+}
+
+// The codes as the two e4m3 planes of the 9..63-token contraction (planes.cuh),
+// in the footprint of fp16 codes; the int8 codes' arithmetic, and their row sum.
+struct PlaneCode {
+  uint16_t bits;
+};
+template <>
+__device__ __forceinline__ void store_codes4<PlaneCode>(PlaneCode* dst, float4 n, float a_scale, int& rs) {
+  const uint32_t p = quant_pack4_i8(n, a_scale);
+  rs = __dp4a(static_cast<int>(p), 0x01010101, rs);
+  uint32_t hi, lo;
+  plane_words4(p, hi, lo);
+  store_planes4(dst, hi, lo);
 }
 
 // kNC > 0: the row (at most kNC float4 groups per lane; exactly kNC when kExact,
@@ -415,6 +430,32 @@ cudaError_t launch_rmsnorm_quant_f16_in(const void* x, int x_dtype, const float*
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_rmsnorm_quant_planes(const void* x, int x_dtype, const float* g, int64_t M, int K, float eps,
+                                       void* planes, float* a_scale, int32_t* rowsum, bool pdl, cudaStream_t s) {
+  PlaneCode* out = static_cast<PlaneCode*>(planes);
+  switch (x_dtype) {
+    case BITNET_DTYPE_F32:
+      return launch_nq_k<float, PlaneCode>(static_cast<const float*>(x), g, M, K, eps, out, a_scale, rowsum, nullptr,
+                                           pdl, s);
+    case BITNET_DTYPE_F16:
+      return launch_nq_k<__half, PlaneCode>(static_cast<const __half*>(x), g, M, K, eps, out, a_scale, rowsum,
+                                            nullptr, pdl, s);
+    case BITNET_DTYPE_BF16:
+      return launch_nq_k<__nv_bfloat16, PlaneCode>(static_cast<const __nv_bfloat16*>(x), g, M, K, eps, out, a_scale,
+                                                   rowsum, nullptr, pdl, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_rmsnorm_quant_glu_planes(const float* gate, const float* up, int act, const float* g, int64_t M,
+                                           int K, float eps, void* planes, float* a_scale, int32_t* rowsum, bool pdl,
+                                           cudaStream_t s) {
+  if (!rmsnorm_quant_glu_fused_supported(K)) return cudaErrorInvalidValue;
+  return launch_nq_glu_k<PlaneCode>(gate, up, act, g, M, K, eps, static_cast<PlaneCode*>(planes), a_scale, rowsum,
+                                    nullptr, pdl, s);
 }
 
 cudaError_t launch_codes_to_f16(const int8_t* codes, __half* out, int64_t count, cudaStream_t s) {
