@@ -29,9 +29,11 @@
 // removing the +1 offset of the weight codes.  Partial sums of split tiles are
 // integers below 2^24, combined with exact fp32 atomic additions.
 //
-// k_token_planes rewrites the tokens' fp16 codes in place: each 128-value
-// block of a row (256 bytes as fp16) becomes its 128 hi bytes then its 128 lo
-// bytes, and sums of the codes per 2048-value chunk go to a small array.
+// The planes (layout in planes.cuh) and the row sums come from the norm
+// launch, or, for int8 codes given by the caller, from k_token_planes, which
+// rewrites their fp16 copy in place (each 128-value block of a row, 256 bytes
+// as fp16, becomes its 128 hi bytes then its 128 lo bytes) and sums the codes
+// per 2048-value chunk.
 //
 // One stage = one I2_S block column (128 values of K) of the tile:
 //   producer warp: the token planes of TG consecutive stages in one 4-D TMA
@@ -55,7 +57,8 @@
 //   A stage is a chain of dependent steps (loads, unpack, tensor-memory store,
 //   fences, barrier hand-offs, MMAs, commit) that leaves the SM's pipes idle
 //   most of the time (one pipeline: ~1200 cycles per stage measured on
-//   sm_103a), so several pipelines overlap their chains.
+//   sm_103a), so several pipelines overlap their chains; each of these warps
+//   visits only its own stages, ring positions following from running counts.
 //   4 epilogue warps: warp q reads TMEM lanes 32q..32q+31 = 32 weight rows of
 //              every pipeline's accumulator and adds them (exact integers);
 //              each thread owns one weight row, so for every token the warp
