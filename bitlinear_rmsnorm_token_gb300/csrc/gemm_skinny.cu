@@ -44,7 +44,8 @@
 //              contiguous bytes, 128-byte swizzle: 8 consecutive rows read 8
 //              different bank groups) into a ring of 6 slots (96 KB in flight
 //              per SM keeps the HBM stream busy); K is split in whole groups
-//   P stage pipelines (4, or 2 for 64-token tiles) take the stages of running
+//   P stage pipelines (4; 3 for 48-token and 2 for 64-token tiles, whose
+//   accumulators take more of the tensor memory) take the stages of running
 //   index j mod P (over the CTA's units), each with
 //     4 unpack warps: warp q holds weight rows 32q .. 32q + 31 (the TMEM lanes
 //              it may write); each thread turns its row's 32 packed bytes into
@@ -78,11 +79,11 @@ constexpr int kSkAStageCols = 32;  // TMEM columns per A stage: 128 K values of 
 constexpr int kSkTmemCols = 512;
 constexpr int kSkPkGroup = 4;      // block columns per packed-weight load: 128 bytes per row
 
-// BN: token tile (16, 32 or 64 tokens); the MMA's N is 2 BN (two planes).
+// BN: token tile (16, 32, 48 or 64 tokens); the MMA's N is 2 BN (two planes).
 template <int BN>
 struct SkLayout {
   static constexpr int kN2 = 2 * BN;                     // MMA N
-  static constexpr int kPipes = BN == 64 ? 2 : 4;
+  static constexpr int kPipes = BN == 64 ? 2 : BN == 48 ? 3 : 4;
   static constexpr int kUnpackWarps = 4 * kPipes;        // warps 0 .. 4P - 1
   static constexpr int kEpiWarp0 = kUnpackWarps;         // 4 warps
   static constexpr int kProducerWarp = kEpiWarp0 + 4;
@@ -97,7 +98,7 @@ struct SkLayout {
   static constexpr int kPkSlots = 6;
   static constexpr int kPk = kSkBM * 32 * kSkPkGroup;  // packed bytes of a slot: 128 rows x 128 B
   static constexpr int kB = kN2 * 128;                 // a stage's token rows (2 per token) of 128 B
-  static constexpr int kTG = BN == 64 ? 2 : 4;         // stages per token copy (a divisor of kSkPkGroup)
+  static constexpr int kTG = BN >= 48 ? 2 : 4;         // stages per token copy (a divisor of kSkPkGroup)
   static constexpr int kTSlot = kTG * kB;              // bytes of a token slot
   static constexpr int kTSlots = (96 * 1024) / kTSlot; // token slots
   static constexpr int offB = 0;                           // [token slots][kTG stages][kB]
@@ -358,8 +359,8 @@ __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
   } else if (warp < L::kUnpackWarps) {
     // --------------------------------------------------------------- unpack
     // pipeline pj's stages, group by group; every unpack warp releases each
-    // packed group once, after its own stages in it (a full group holds 4 / P
-    // stages of every pipeline; a unit's short last group may hold none)
+    // packed group once, after its own stages in it (a full group of 4 stages
+    // holds 1 or 2 of every pipeline; a unit's short last group may hold none)
     const int pj = warp >> 2;            // pipeline: stages of running index pj mod P
     const int q = warp & 3;              // TMEM lane quadrant: weight rows 32q .. 32q + 31
     const int row = 32 * q + lane;       // weight row of the tile
@@ -685,7 +686,7 @@ cudaError_t launch_gemm_skinny(const DeviceContext* ctx, void* codes, const int3
     if (e != cudaSuccess) return e;
   }
   const uint8_t* planes = static_cast<const uint8_t*>(codes);
-  const int bn = m <= 16 ? 16 : m <= 32 ? 32 : 64;
+  const int bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 48 ? 48 : 64;
   switch (bn) {
     case 16:
       return launch_bn<16>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
@@ -693,6 +694,9 @@ cudaError_t launch_gemm_skinny(const DeviceContext* ctx, void* codes, const int3
     case 32:
       return launch_bn<32>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
                            tickets, s, status);
+    case 48:
+      return launch_bn<48>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out,
+                           ws, tickets, s, status);
     default:
       return launch_bn<64>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
                            tickets, s, status);

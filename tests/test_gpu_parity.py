@@ -199,11 +199,11 @@ GEMM_CASES = [
     # decode (dp4a) path
     (1, 128, 1), (1, 1024, 2048), (2, 640, 33), (3, 3072, 200), (5, 1024, 129), (8, 1024, 2048), (8, 8192, 64),
     (1, 16384, 4096), (4, 16384, 2500),
-    # split-K tensor-core path (9..64 tokens with K >= 4096 or N >= 16384): 128 weight
-    # rows x 16/32/64 tokens, K split into ranges of I2_S blocks combined by atomic fp32
-    # additions, ragged weight tiles
+    # split-K 8-bit tensor-core path (9..63 tokens with K >= 4096 or N >= 16384): 128 weight
+    # rows x 16/32/48/64 tokens, K split into ranges of I2_S blocks combined by atomic fp32
+    # additions, ragged weight tiles (64 tokens: the boundary, taken by the next kernel)
     (16, 16384, 1024), (64, 4096, 4096), (33, 8192, 130), (9, 65536, 256), (12, 4096, 3000),
-    (48, 6144, 1000), (20, 1024, 16500), (64, 256, 16384),
+    (48, 6144, 1000), (20, 1024, 16500), (64, 256, 16384), (44, 4096, 2100), (57, 16384, 700),
     # tensor-core path, tokens as the MMA's M side: 128 tokens x 64/128/256 weights, ragged tails
     (9, 128, 128), (16, 256, 130), (64, 1024, 256), (100, 640, 1000), (40, 2048, 1000), (64, 128, 5000),
     (24, 3072, 2049), (17, 1920, 300), (129, 1024, 384), (300, 3072, 257), (600, 2048, 1024), (1000, 128, 5),
