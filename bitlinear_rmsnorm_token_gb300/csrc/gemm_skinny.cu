@@ -490,11 +490,24 @@ __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
       if (*last_flag) {
         __threadfence();
         if (n_ok) {
-          for (int t = 0; t < M && t < BN; ++t) {
-            // both exact integers below 2^24: the difference is exact
-            const float accf = __fsub_rn(__ldcg(ws + static_cast<int64_t>(t) * N + n), static_cast<float>(sRs[t]));
-            y[static_cast<int64_t>(t) * N + n] = rescale_elem(accf, sInv[t], inv_w);
-            if (acc_out) acc_out[static_cast<int64_t>(t) * N + n] = __float2int_rn(accf);
+          // 16 tokens' sums loaded before any is used: one L2 round trip per
+          // 16 tokens instead of one per token
+#pragma unroll 1
+          for (int t0 = 0; t0 < M && t0 < BN; t0 += 16) {
+            float part[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              part[i] = t0 + i < M ? __ldcg(ws + static_cast<int64_t>(t0 + i) * N + n) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int t = t0 + i;
+              if (t < M) {
+                // both exact integers below 2^24: the difference is exact
+                const float accf = __fsub_rn(part[i], static_cast<float>(sRs[t]));
+                y[static_cast<int64_t>(t) * N + n] = rescale_elem(accf, sInv[t], inv_w);
+                if (acc_out) acc_out[static_cast<int64_t>(t) * N + n] = __float2int_rn(accf);
+              }
+            }
           }
         }
       }
@@ -510,16 +523,21 @@ __global__ void __launch_bounds__(SkLayout<BN>::kThreads, 1)
   }
 }
 
+// Token tile of the contraction for M tokens (16, 32, 48 or 64).
+int skinny_tile(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
+
 // Number of K splits: the one with the least estimated time, which is the
-// busiest CTA's stages plus, with a split, the epilogues' fp32 atomic
-// additions (M N S of them, a throughput the whole GPU shares) and the per-unit
-// ticket and read-back.  Fitted to GB300 timings with forced split counts:
-// ~85 atomic additions per ns, ~1 us per split unit (M = 63, K = N = 16384,
-// fp16 operands: 70 us unsplit, 89 / 121 / 182 us with S = 2 / 4 / 8, where a
-// count of stages alone picks 8), and ~0.35 us per stage with 8-bit operands.
-// Ties go to fewer splits.
+// busiest CTA's stages plus, with a split, a fixed cost (the partial sums'
+// zeroing, the tickets, the last split's read-back) and the epilogues' fp32
+// atomic additions (M N S of them, a throughput the whole GPU shares).  Fitted
+// to GB300 timings of 12 shapes (9..63 tokens, K = 4096..65536, N =
+// 1024..16384) at forced split counts, within ~1 us rms: per stage ~185 /
+// 210 / 235 / 400 ns for tiles of 16 / 32 / 48 / 64 tokens, ~1.9 us fixed and
+// ~128 atomic additions per ns.  Ties go to fewer splits.
 int choose_splits(int64_t M, int n_wt, int nkb, int64_t N, int ctas) {
-  constexpr double kStageNs = 350.0, kAtomicsPerNs = 85.0, kSplitUnitNs = 1000.0;
+  constexpr double kSplitNs = 1900.0, kAtomicsPerNs = 128.0;
+  const int bn = skinny_tile(M);
+  const double stage_ns = bn == 16 ? 185.0 : bn == 32 ? 210.0 : bn == 48 ? 235.0 : 400.0;
   const int ngrp = (nkb + kSkPkGroup - 1) / kSkPkGroup;
   int best = 1;
   double best_cost = 0.0;
@@ -527,10 +545,8 @@ int choose_splits(int64_t M, int n_wt, int nkb, int64_t N, int ctas) {
   for (int S = 1; S <= max_s; ++S) {
     const int64_t units = static_cast<int64_t>(n_wt) * S;
     const int64_t per_cta = (units + ctas - 1) / ctas;
-    double cost = static_cast<double>(per_cta) * kSkPkGroup * ((ngrp + S - 1) / S) * kStageNs;
-    if (S > 1)
-      cost += static_cast<double>(M) * static_cast<double>(N) * S / kAtomicsPerNs +
-              static_cast<double>(per_cta) * kSplitUnitNs;
+    double cost = static_cast<double>(per_cta) * kSkPkGroup * ((ngrp + S - 1) / S) * stage_ns;
+    if (S > 1) cost += kSplitNs + static_cast<double>(M) * static_cast<double>(N) * S / kAtomicsPerNs;
     if (S == 1 || cost < best_cost) {
       best_cost = cost;
       best = S;
@@ -620,8 +636,8 @@ SkWorkspace skinny_workspace(const DeviceContext* ctx, int64_t M, int64_t K, int
 // that (K <= 2048 and N <= 8192, a few us) the tokens-as-M kernel is faster.
 // From 64 tokens on the tokens-as-M kernel is used: its tiles hold 128 tokens,
 // so its time hardly depends on the count.  Measured on GB300 at
-// K = N = 16384: 67 / 69 / 70 us for 16 / 32 / 63 tokens here against 78-79 us
-// there.
+// K = N = 16384: 37 / 40 / 45 / 50 us for 16 / 32 / 48 / 63 tokens here against
+// 78-79 us there.
 bool gemm_skinny_supported(int64_t M, int64_t K, int64_t N) {
   return M > kDecodeMaxM && M < 64 && K >= 128 && K % 128 == 0 && N >= 1 && (K >= 4096 || N >= 16384);
 }
@@ -686,8 +702,7 @@ cudaError_t launch_gemm_skinny(const DeviceContext* ctx, void* codes, const int3
     if (e != cudaSuccess) return e;
   }
   const uint8_t* planes = static_cast<const uint8_t*>(codes);
-  const int bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 48 ? 48 : 64;
-  switch (bn) {
+  switch (skinny_tile(M)) {
     case 16:
       return launch_bn<16>(ctx, encode, planes, a_scale, rowsum_part, nparts, packed_w, inv_w, m, k, n, S, y, acc_out, ws,
                            tickets, s, status);
