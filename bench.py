@@ -136,7 +136,7 @@ class ClockSampler:
             os.unlink(self.out.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
         window = "timed"
         if not inside:
             inside, window = rows, "whole run"
@@ -304,8 +304,10 @@ def run_decode(args, rank, world, local):
             if n % chunk:
                 graph_of(n % chunk).replay()
 
-    # Timed region: exactly `steps` steps between two events, repeated
-    # `repeats` times; the per-step time is the median repeat's.  Each repeat
+    # Timed region: exactly `steps` steps between two events, repeated in
+    # batches of `batch` until the timed phase has lasted `min_wall_s` (so that
+    # the clock samples are taken under this load); the per-step time is the
+    # median repeat's.  Each repeat
     # starts with one graph holding an untimed pre-roll of `preroll` steps and
     # then the first timed steps.  The start event is recorded inside that graph
     # on a side branch that waits for the last pre-roll step, so it fires when
@@ -314,7 +316,7 @@ def run_decode(args, rank, world, local):
     # exactly `steps` step-to-step intervals of the steady state.  The rest of
     # the steps follow as whole graphs; the end event follows the last step.
     preroll = min(chunk, 64)
-    repeats = 5
+    batch, min_wall_s = 8, 0.6
     first_n = min(args.steps, chunk)
     side = torch.cuda.Stream(device)
 
@@ -333,7 +335,7 @@ def run_decode(args, rank, world, local):
         return g_
 
     try:
-        starts = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(repeats)]
+        starts = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(batch)]
         firsts = [first_graph(e) for e in starts]
         start_event = "recorded inside the first graph on a branch after the last pre-roll step"
     except (TypeError, RuntimeError):
@@ -341,7 +343,7 @@ def run_decode(args, rank, world, local):
         # graph and the timed steps instead (the first timed step then loses its
         # overlap with the pre-roll)
         torch.cuda.synchronize()
-        starts, firsts = [torch.cuda.Event(enable_timing=True) for _ in range(repeats)], None
+        starts, firsts = [torch.cuda.Event(enable_timing=True) for _ in range(batch)], None
         first_n = 0
         start_event = "recorded on the stream between the pre-roll graph and the first timed step"
     rest = args.steps - first_n
@@ -356,23 +358,27 @@ def run_decode(args, rank, world, local):
     stream.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    evs = [(starts[r], torch.cuda.Event(enable_timing=True)) for r in range(repeats)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(batch)]
+    rep_ms = []
     t0 = time.time()
     with torch.cuda.stream(stream):
-        for r, (ev0, ev1) in enumerate(evs):
-            if firsts is not None:
-                firsts[r].replay()
-            else:
-                graph_of(preroll).replay()
-                ev0.record(stream)
-            run_steps(rest)
-            ev1.record(stream)
-    evs[-1][1].synchronize()
+        while True:
+            for r in range(batch):
+                if firsts is not None:
+                    firsts[r].replay()
+                else:
+                    graph_of(preroll).replay()
+                    starts[r].record(stream)
+                run_steps(rest)
+                ends[r].record(stream)
+            ends[-1].synchronize()
+            rep_ms += [starts[r].elapsed_time(ends[r]) for r in range(batch)]
+            if time.time() - t0 >= min_wall_s:
+                break
     t1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
     sampler.stop()
-    rep_ms = [a.elapsed_time(b) for a, b in evs]
     ms_local = float(np.median(rep_ms))
     ms, _, value = aggregate(ms_local, float(step_bytes) * args.steps, world)
     value /= 1e9
@@ -508,8 +514,12 @@ def run_decode(args, rank, world, local):
         "config": decode_config(world),
         "setup": {"weight_pool_layers": n_layers, "weight_pool_bytes": n_layers * weight_bytes,
                   "launch": "one grouped kernel per step, CUDA graph replay, programmatic dependent launch"},
-        "timing": {"repeats": repeats, "ms_per_repeat": [round(v, 6) for v in rep_ms],
-                   "statistic": "median repeat; each repeat times exactly `steps` steps between two events",
+        "timing": {"repeats": len(rep_ms), "ms_per_repeat_min": round(min(rep_ms), 6),
+                   "ms_per_repeat_median": round(ms_local, 6), "ms_per_repeat_max": round(max(rep_ms), 6),
+                   "timed_phase_s": round(t1 - t0, 3),
+                   "statistic": "median repeat; each repeat times exactly `steps` steps between two events; "
+                                f"repeats run in batches of {batch} until the timed phase has lasted "
+                                f"{min_wall_s} s, so that the clock samples fall under this load",
                    "preroll_steps": preroll, "start_event": start_event},
         "roofline": {"bound": "hbm", "kernel": "k_decode (grouped BitLinear GEMV)", "achieved": round(achieved, 2),
                      "peak": hbm, "peak_kind": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
